@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the content-dependent block-sparse attention forward.
+
+One step = one ``bsa_forward`` (block mean-pool -> coarse scoring + top-k ->
+fine attention over the selected blocks) on the 32k-token workload:
+bh = 8 heads, n = 32768, d = 64, bf16, key block 64, top-16, planted block
+centres; inputs resident in HBM, L2 flushed (a 256 MiB write) before every
+timed step.  Prints ONE JSON line (rank 0):
+
+  value      effective TFLOP/s over all ranks (selected FLOPs only, page
+             "sparse-attention-triton-bench" convention: 87.24 GFLOP/forward)
+  e2e        the same metric through the public API with host buffers:
+             pinned-host -> device copies of Q, K, V and the device -> host
+             copy of O inside every timed step
+  roofline   the dominant kernel (fine attention), timed alone with CUDA
+             events on its stream, against the measured bf16 tensor peak
+  cpu_baseline  the fp64 oracle on a bounded row sample, host cores (rank 0)
+
+``--impl reference`` times the oracle itself as the reference arm.
+Multi-GPU (torchrun): every rank runs its own independent problem (weak
+scaling, no collective on the data path); the barrier and max-over-ranks
+timing use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+from content_dependent_block_gb300 import metrics  # noqa: E402
+
+METRIC = "sparse-attn fwd ms & effective TFLOP/s at N=32k (1 GB300); % of roofline"
+WORKLOAD = "dyn_n32768"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU seconds of the oracle sample")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    return args
+
+
+# ---------------------------------------------------------------- ranks
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def aggregate(dist, total_ms: float, units: float, device=None):
+    """Max of the timed region and sum of the work over ranks."""
+    if dist is None:
+        return total_ms, units
+    import torch
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.path is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = [r for r in csv.reader(io.StringIO(open(self.path).read())) if len(r) >= 9]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- peaks
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source has not changed since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    ent = table.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, ent["source"])
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return ent["bytes_per_launch"] if sha == ent.get("source_sha") else None
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_sample(w, t, seconds: float):
+    """Time the oracle's whole dynamic path on a row sample; returns
+    (TFLOP/s, rows, seconds, cores, description)."""
+    import numpy as np
+    import oracle
+    cores = oracle.num_threads()
+    per_row = metrics.sparse_flops(1, 1, w.d, w.key_block, w.topk)
+
+    def run(nrows):
+        rows = workloads.sample_rows(w.bh, w.n, max(1, nrows // w.bh), seed=7)
+        t0 = time.perf_counter()
+        kbar = oracle.pool(t.k, w.key_block)
+        s = oracle.scores(t.q, kbar, rows)
+        idx, _ = oracle.topk(s, w.topk)
+        oracle.fine(t.q, t.k, t.v, w.key_block, idx, rows)
+        return rows.size, time.perf_counter() - t0
+
+    r0, t0 = run(256 * w.bh)
+    # bounded: at most 32768 rows (the oracle keeps every row's scores)
+    nrows = int(min(w.bh * w.n, 32768, max(r0, r0 * seconds / max(t0, 1e-3))))
+    r1, t1 = run(nrows)
+    tflops = r1 * per_row / t1 / 1e12
+    desc = (f"{r1} of {w.bh * w.n} query rows (seeded sample), full pool + scores + top-k + "
+            f"fine per row, fp64, {cores} threads")
+    return tflops, r1, t1, cores, desc
+
+
+def reference_arm(args, rank, world, w):
+    """The oracle as the reference arm: each step a bounded row sample."""
+    if rank != 0:
+        return 0
+    import oracle  # noqa: F401
+    t = workloads.generate(w)
+    cores = None
+    per_row = metrics.sparse_flops(1, 1, w.d, w.key_block, w.topk)
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    _, rows, secs, cores, desc = oracle_sample(w, t, budget)
+    import oracle as orc
+    times = []
+    rws = workloads.sample_rows(w.bh, w.n, max(1, rows // w.bh), seed=7)
+    for it in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        kbar = orc.pool(t.k, w.key_block)
+        s = orc.scores(t.q, kbar, rws)
+        idx, _ = orc.topk(s, w.topk)
+        orc.fine(t.q, t.k, t.v, w.key_block, idx, rws)
+        if it >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = rws.size * per_row * len(times) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rws.size} of {w.bh * w.n} query rows per step; " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w):
+    return {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "key_block": w.key_block,
+            "topk": w.topk, "dtype": w.dtype, "inputs": w.note,
+            "l2": "flushed before every timed step (256 MiB write)",
+            "parallelism": "independent problem per rank (weak)"}
+
+
+# ------------------------------------------------------------- GPU arm
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, rank, world, w)
+
+    import torch
+    from content_dependent_block_gb300 import _build, bsa
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    if rank == 0:
+        _build.build()
+    barrier(dist, device)
+    bsa.lib()
+
+    t = workloads.generate(w, seed=w.seed + rank)
+    torch.cuda.reset_peak_memory_stats(device)
+    mem0 = torch.cuda.memory_allocated(device)
+    q, k, v = (torch.from_numpy(getattr(t, x).view("int16")).view(torch.bfloat16).to(device)
+               for x in "qkv")
+    fwd = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk, device=device)
+    fwd(q, k, v)
+    torch.cuda.synchronize(device)
+    peak_mb = (torch.cuda.max_memory_allocated(device) - mem0) / 2**20
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    flops = metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk)
+    fine_flops = metrics.pairs_flops(w.n * w.bh * min(w.topk, w.nb) * w.key_block, w.d)
+
+    def flush_l2():
+        flush.fill_(1)
+
+    def timed(fn, steps):
+        evs = []
+        for _ in range(steps):
+            flush_l2()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    with ClockSampler(gpu_index) as clocks:
+        for _ in range(args.warmup):
+            flush_l2()
+            fwd(q, k, v)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        torch.cuda.synchronize(device)
+        step_ms = timed(lambda: fwd(q, k, v), args.steps)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        total_ms, total_flops = aggregate(dist, sum(step_ms), flops * args.steps, device)
+
+        # stages, each timed alone on the launching stream
+        kbar = torch.empty((w.bh, w.nb, w.d), dtype=torch.float32, device=device)
+        idx = torch.empty((w.bh, w.n, w.topk), dtype=torch.int32, device=device)
+        out = torch.empty_like(q)
+        ws_c = bsa.lib().bsa_coarse_topk_workspace_size(fwd.shape, w.key_block, w.topk)
+        ws_cb = bsa._workspace(ws_c, device)
+        shp = fwd.shape
+        L = bsa.lib()
+        S = bsa._stream
+        P = bsa._ptr
+
+        def pool():
+            bsa._check(L.bsa_pool_blocks(shp, P(k), w.key_block, P(kbar), S()))
+
+        def coarse():
+            bsa._check(L.bsa_coarse_topk(shp, P(q), P(kbar), w.key_block, w.topk, P(idx),
+                                         P(ws_cb), ws_c, S()))
+
+        ld = bsa.ListDesc(1, w.key_block, w.topk, 1)
+        msk = bsa.mask_struct()
+        ws_f = L.bsa_fine_attention_workspace_size(shp, ld, msk)
+        ws_fb = bsa._workspace(ws_f, device)
+
+        def fine():
+            bsa._check(L.bsa_fine_attention(shp, P(q), P(k), P(v), P(idx), ld, msk, 0.0, P(out),
+                                            P(ws_fb), ws_f, S()))
+
+        stage_steps = max(3, min(args.steps, 20))
+        pool_ms = statistics.mean(timed(pool, stage_steps))
+        coarse_ms = statistics.mean(timed(coarse, stage_steps))
+        fine_ms = statistics.mean(timed(fine, stage_steps))
+
+        # end to end through the public API with host buffers
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        ho = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+        dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            o = fwd(dq, dk, dv)
+            ho.copy_(o, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        e2e_ms = timed(e2e_step, args.steps)
+        e2e_total, _ = aggregate(dist, sum(e2e_ms), 0.0, device)
+    clk = clocks.summary()
+
+    status = bsa.device_status()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0 if status == 0 else 1
+
+    ms = total_ms / args.steps
+    value = total_flops / (total_ms * 1e-3) / 1e12
+    peaks = measured_peaks()
+    tc_peak = peaks["bf16_tflops"]
+    achieved = fine_flops / (fine_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+        "roofline": {"kernel": "fine attention (bsa_fine_attention over the top-k list)",
+                     "bound": "tensor", "achieved": achieved, "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": achieved / tc_peak,
+                     "peak_source": f"bf16_tflops burst, {peaks['source']}",
+                     "traffic": kernel_traffic("fine_attention"),
+                     "algorithmic_flops_per_launch": fine_flops,
+                     "launch_ms": fine_ms},
+        "e2e": {"value": flops * world / (e2e_total / args.steps * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "ms_per_step": e2e_total / args.steps,
+                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+                "d2h_bytes_per_step": q.numel() * q.element_size()},
+        "gpu_launches": fwd.launches * args.steps,
+        "clocks": clk,
+        "stages_ms": {"pool": pool_ms, "coarse_topk": coarse_ms, "fine": fine_ms},
+        "peak_hbm_mb": peak_mb,
+        "flops_per_forward": flops,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        tf, rows, secs, cores, desc = oracle_sample(w, t, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0 if status == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,243 @@
+"""Thin ctypes binding over libbsa.so (include/bsa.h).
+
+Argument marshalling only: every step of the method runs in the library's
+CUDA kernels.  Device tensors come from PyTorch (it provides device memory,
+streams and events); work is enqueued on PyTorch's current stream.  If
+libbsa.so has not been built, every call raises ``BsaError`` -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+
+from . import _build
+
+BF16, FP32 = 0, 1
+MASK_NONE, MASK_LOCAL_GLOBAL, MASK_SLIDING = 0, 1, 2
+
+STATUS = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
+          3: "BSA_ERR_BAD_INDEX", 4: "BSA_ERR_WORKSPACE", 5: "BSA_ERR_CUDA",
+          6: "BSA_ERR_TIMEOUT", 7: "BSA_ERR_ALIGNMENT"}
+
+# Every symbol include/bsa.h declares.
+EXPORTS = (
+    "bsa_pool_blocks", "bsa_coarse_topk_workspace_size", "bsa_coarse_topk",
+    "bsa_fine_attention_workspace_size", "bsa_fine_attention",
+    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_launches",
+    "bsa_static_max_blocks",
+    "bsa_static_blocks", "bsa_get_device_status", "bsa_status_string",
+    "bsa_last_error", "bsa_version",
+)
+
+
+class BsaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("bh", ctypes.c_int64), ("n", ctypes.c_int64),
+                ("d", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class Mask(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("stride", ctypes.c_int32), ("sliding", ctypes.c_int32)]
+
+
+class ListDesc(ctypes.Structure):
+    _fields_ = [("q_group", ctypes.c_int32), ("key_block", ctypes.c_int32),
+                ("max_blocks", ctypes.c_int32), ("per_head", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libbsa.so (built in-tree); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise BsaError(5, f"{path} is missing: build it with content_dependent_block_gb300._build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, sz, f32 = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                             ctypes.c_size_t, ctypes.c_float)
+    sig = {
+        "bsa_pool_blocks": ([Shape, vp, i32, vp, vp], i32),
+        "bsa_coarse_topk_workspace_size": ([Shape, i32, i32], sz),
+        "bsa_coarse_topk": ([Shape, vp, vp, i32, i32, vp, vp, sz, vp], i32),
+        "bsa_fine_attention_workspace_size": ([Shape, ListDesc, Mask], sz),
+        "bsa_fine_attention": ([Shape, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, sz, vp], i32),
+        "bsa_forward_workspace_size": ([Shape, i32, i32], sz),
+        "bsa_forward": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp], i32),
+        "bsa_forward_launches": ([Shape, i32, i32], i32),
+        "bsa_static_max_blocks": ([i64, i32, i32, Mask], i32),
+        "bsa_static_blocks": ([i64, i32, i32, Mask, vp, i32, vp, vp], i32),
+        "bsa_get_device_status": ([vp, vp], i32),
+        "bsa_status_string": ([i32], ctypes.c_char_p),
+        "bsa_last_error": ([], ctypes.c_char_p),
+        "bsa_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(code: int):
+    if code != 0:
+        raise BsaError(code, lib().bsa_last_error().decode())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _shape(t) -> Shape:
+    torch = _torch()
+    if t.dim() != 3 or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError("tensors must be contiguous CUDA [bh, n, d]")
+    if t.dtype == torch.bfloat16:
+        dt = BF16
+    elif t.dtype == torch.float32:
+        dt = FP32
+    else:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return Shape(t.shape[0], t.shape[1], t.shape[2], dt)
+
+
+def _workspace(nbytes: int, device):
+    if nbytes == 0:
+        return None
+    return _torch().empty(nbytes, dtype=_torch().uint8, device=device)
+
+
+def mask_struct(kind: int = MASK_NONE, window: int = -1, stride: int = 0, sliding: int = 0) -> Mask:
+    return Mask(kind, window, stride, sliding)
+
+
+def pool_blocks(k, key_block: int):
+    """Block means Kbar [bh, ceil(n/B), d] fp32 of bf16 keys."""
+    s = _shape(k)
+    nb = -(-s.n // key_block)
+    kbar = _torch().empty((s.bh, nb, s.d), dtype=_torch().float32, device=k.device)
+    _check(lib().bsa_pool_blocks(s, _ptr(k), key_block, _ptr(kbar), _stream()))
+    return kbar
+
+
+def coarse_topk(q, kbar, key_block: int, topk: int):
+    """Top-k block ids [bh, n, topk] int32 (ascending, -1 padded)."""
+    s = _shape(q)
+    idx = _torch().empty((s.bh, s.n, topk), dtype=_torch().int32, device=q.device)
+    ws_n = lib().bsa_coarse_topk_workspace_size(s, key_block, topk)
+    ws = _workspace(ws_n, q.device)
+    _check(lib().bsa_coarse_topk(s, _ptr(q), _ptr(kbar), key_block, topk, _ptr(idx),
+                                 _ptr(ws), ws_n, _stream()))
+    return idx
+
+
+def fine_attention(q, k, v, block_list=None, *, key_block: int, q_group: int = 1,
+                   per_head: bool = True, mask: Optional[Mask] = None, scale: float = 0.0,
+                   out=None):
+    """Softmax attention of each query over its listed blocks' tokens.
+
+    ``block_list``: int32 device tensor [bh or 1, ceil(n/q_group), max_blocks]
+    (or 2-D [rows, max_blocks] when shared by all heads), None = all blocks.
+    """
+    s = _shape(q)
+    mask = mask or mask_struct()
+    if block_list is not None:
+        if block_list.dtype != _torch().int32 or not block_list.is_contiguous():
+            raise TypeError("block_list must be a contiguous int32 tensor")
+        ld = ListDesc(q_group, key_block, block_list.shape[-1], 1 if per_head else 0)
+    else:
+        ld = ListDesc(1, key_block, 0, 0)
+    out = _torch().empty_like(q) if out is None else out
+    ws_n = lib().bsa_fine_attention_workspace_size(s, ld, mask)
+    ws = _workspace(ws_n, q.device)
+    _check(lib().bsa_fine_attention(s, _ptr(q), _ptr(k), _ptr(v), _ptr(block_list), ld, mask,
+                                    float(scale), _ptr(out), _ptr(ws), ws_n, _stream()))
+    return out
+
+
+class Forward:
+    """Reusable forward: owns the output, selection and workspace buffers for
+    one shape so repeated calls allocate nothing."""
+
+    def __init__(self, bh: int, n: int, d: int, key_block: int, topk: int, device="cuda",
+                 scale: float = 0.0):
+        torch = _torch()
+        self.shape = Shape(bh, n, d, BF16)
+        self.key_block, self.topk, self.scale = key_block, topk, scale
+        self.ws_bytes = lib().bsa_forward_workspace_size(self.shape, key_block, topk)
+        self.ws = _workspace(self.ws_bytes, device)
+        self.out = torch.empty((bh, n, d), dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty((bh, n, topk), dtype=torch.int32, device=device)
+
+    @property
+    def launches(self) -> int:
+        """Kernel launches one call enqueues."""
+        return int(lib().bsa_forward_launches(self.shape, self.key_block, self.topk))
+
+    def __call__(self, q, k, v, keep_idx: bool = True):
+        s = _shape(q)
+        if (s.bh, s.n, s.d) != (self.shape.bh, self.shape.n, self.shape.d):
+            raise ValueError("shape differs from the one this Forward was built for")
+        _check(lib().bsa_forward(self.shape, _ptr(q), _ptr(k), _ptr(v), self.key_block,
+                                 self.topk, float(self.scale), _ptr(self.out),
+                                 _ptr(self.idx if keep_idx else None), _ptr(self.ws),
+                                 self.ws_bytes, _stream()))
+        return self.out
+
+
+def forward(q, k, v, key_block: int, topk: int, scale: float = 0.0) -> Tuple[object, object]:
+    """Whole dynamic forward; returns (out, idx)."""
+    s = _shape(q)
+    f = Forward(s.bh, s.n, s.d, key_block, topk, device=q.device, scale=scale)
+    out = f(q, k, v, keep_idx=True)
+    return out, f.idx
+
+
+def static_blocks(n: int, q_group: int, key_block: int, mask: Mask):
+    """Host-built static list: (list [rows, max_blocks] int32, counts, active_pairs)."""
+    L = lib()
+    mb = L.bsa_static_max_blocks(n, q_group, key_block, mask)
+    if mb < 0:
+        raise BsaError(-mb, L.bsa_last_error().decode() or "bad static-list arguments")
+    rows = -(-n // q_group)
+    lst = np.empty((rows, max(mb, 1)), dtype=np.int32)
+    counts = np.empty(rows, dtype=np.int32)
+    pairs = ctypes.c_int64(0)
+    _check(L.bsa_static_blocks(n, q_group, key_block, mask,
+                               lst.ctypes.data_as(ctypes.c_void_p), lst.shape[1],
+                               counts.ctypes.data_as(ctypes.c_void_p), ctypes.byref(pairs)))
+    return lst, counts, int(pairs.value)
+
+
+def device_status() -> int:
+    """Read and clear the device status word (synchronises the stream)."""
+    v = ctypes.c_int32(0)
+    _check(lib().bsa_get_device_status(ctypes.byref(v), _stream()))
+    return int(v.value)

@@ -1,0 +1,286 @@
+// C-ABI layer of libbsa.so: argument validation, workspace carving and the
+// launch sequence of every entry point declared in include/bsa.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "bsa.h"
+#include "bsa_internal.h"
+
+namespace {
+
+constexpr int32_t kVersion = 100;   // 0.1.0
+constexpr int kMaxDevices = 64;
+
+thread_local char g_last_error[256] = "";
+
+bsa_status fail(bsa_status code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bsa_status ok() {
+    g_last_error[0] = '\0';
+    return BSA_OK;
+}
+
+// Device status word: first kernel-detected error since the last read.
+__device__ int32_t g_device_status = 0;
+
+int32_t *device_status_ptr() {
+    static std::mutex mu;
+    static int32_t *cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<int32_t *>(p);
+    }
+    return cache[dev];
+}
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bsa_status check_shape(const bsa_shape &s) {
+    if (s.bh < 1 || s.n < 1) return fail(BSA_ERR_INVALID_ARG, "bh and n must be >= 1");
+    if (s.bh > 65535) return fail(BSA_ERR_UNSUPPORTED, "bh must be <= 65535");
+    if (s.n > (int64_t(1) << 31) - 1) return fail(BSA_ERR_UNSUPPORTED, "n must fit in int32");
+    if (s.d != 64 && s.d != 128) return fail(BSA_ERR_UNSUPPORTED, "d must be 64 or 128 (got %d)", s.d);
+    if (s.dtype != BSA_BF16 && s.dtype != BSA_FP32) return fail(BSA_ERR_INVALID_ARG, "bad dtype %d", s.dtype);
+    return BSA_OK;
+}
+
+bsa_status check_key_block(int32_t kb) {
+    if (kb != 16 && kb != 32 && kb != 64 && kb != 128)
+        return fail(BSA_ERR_UNSUPPORTED, "key_block must be 16, 32, 64 or 128 (got %d)", kb);
+    return BSA_OK;
+}
+
+bsa_status check_ptr(const void *p, const char *name) {
+    if (p == nullptr) return fail(BSA_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, 16)) return fail(BSA_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+    return BSA_OK;
+}
+
+bsa_status check_ws(const void *ws, size_t have, size_t need) {
+    if (need == 0) return BSA_OK;
+    if (ws == nullptr || have < need)
+        return fail(BSA_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", need, ws ? have : size_t(0));
+    if (!aligned(ws, 256)) return fail(BSA_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+    return BSA_OK;
+}
+
+bsa_status launched(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+#define BSA_TRY(expr)                      \
+    do {                                   \
+        bsa_status st_ = (expr);           \
+        if (st_ != BSA_OK) return st_;     \
+    } while (0)
+
+// Workspace of the whole forward: block means, then the selection.
+struct ForwardLayout {
+    size_t kbar = 0, idx = 0, total = 0;
+};
+
+ForwardLayout forward_layout(const bsa_shape &s, int32_t kb, int32_t topk) {
+    ForwardLayout L;
+    const int64_t nb = ceil_div(s.n, kb);
+    size_t off = 0;
+    L.kbar = off;
+    off = round_up(off + size_t(s.bh) * nb * s.d * sizeof(float), 256);
+    L.idx = off;
+    off = round_up(off + size_t(s.bh) * s.n * topk * sizeof(int32_t), 256);
+    L.total = off;
+    return L;
+}
+
+float softmax_scale_log2(float scale, int32_t d) {
+    const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(float(d));
+    return sc * 1.4426950408889634f;   // log2(e)
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t bsa_version(void) { return kVersion; }
+
+const char *bsa_last_error(void) { return g_last_error; }
+
+const char *bsa_status_string(int32_t status) {
+    switch (status) {
+        case BSA_OK: return "ok";
+        case BSA_ERR_INVALID_ARG: return "invalid argument";
+        case BSA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case BSA_ERR_BAD_INDEX: return "block index out of range";
+        case BSA_ERR_WORKSPACE: return "workspace missing or too small";
+        case BSA_ERR_CUDA: return "CUDA runtime error";
+        case BSA_ERR_TIMEOUT: return "device wait timed out";
+        case BSA_ERR_ALIGNMENT: return "misaligned pointer";
+        default: return "unknown status";
+    }
+}
+
+bsa_status bsa_get_device_status(int32_t *status, void *stream) {
+    if (status == nullptr) return fail(BSA_ERR_INVALID_ARG, "status is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+    int32_t *p = device_status_ptr();
+    if (p == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    int32_t v = 0;
+    e = cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof v);
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+    *status = v;
+    return ok();
+}
+
+bsa_status bsa_pool_blocks(bsa_shape shape, const void *k, int32_t key_block, float *kbar,
+                           void *stream) {
+    BSA_TRY(check_shape(shape));
+    if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "pooling takes bf16 keys");
+    BSA_TRY(check_key_block(key_block));
+    BSA_TRY(check_ptr(k, "k"));
+    BSA_TRY(check_ptr(kbar, "kbar"));
+    return launched(bsa::launch_pool(k, shape.bh, shape.n, shape.d, key_block, kbar, nullptr,
+                                     nullptr, 0, static_cast<cudaStream_t>(stream)),
+                    "pool launch");
+}
+
+size_t bsa_coarse_topk_workspace_size(bsa_shape, int32_t, int32_t) { return 0; }
+
+bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, int32_t key_block,
+                           int32_t topk, int32_t *idx, void *ws, size_t ws_bytes, void *stream) {
+    BSA_TRY(check_shape(shape));
+    if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "scoring takes bf16 queries");
+    BSA_TRY(check_key_block(key_block));
+    if (topk < 1 || topk > 32) return fail(BSA_ERR_UNSUPPORTED, "topk must be in [1, 32] (got %d)", topk);
+    BSA_TRY(check_ptr(q, "q"));
+    BSA_TRY(check_ptr(kbar, "kbar"));
+    BSA_TRY(check_ptr(idx, "idx"));
+    BSA_TRY(check_ws(ws, ws_bytes, bsa_coarse_topk_workspace_size(shape, key_block, topk)));
+    const int64_t nb = ceil_div(shape.n, key_block);
+    return launched(bsa::launch_coarse_topk_simt(q, kbar, shape.bh, shape.n, shape.d, nb, topk, idx,
+                                                 static_cast<cudaStream_t>(stream)),
+                    "coarse top-k launch");
+}
+
+size_t bsa_fine_attention_workspace_size(bsa_shape, bsa_list_desc, bsa_mask) { return 0; }
+
+bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, const void *v,
+                              const int32_t *list, bsa_list_desc ld, bsa_mask mask, float scale,
+                              void *out, void *ws, size_t ws_bytes, void *stream) {
+    BSA_TRY(check_shape(shape));
+    BSA_TRY(check_key_block(ld.key_block));
+    BSA_TRY(check_ptr(q, "q"));
+    BSA_TRY(check_ptr(k, "k"));
+    BSA_TRY(check_ptr(v, "v"));
+    BSA_TRY(check_ptr(out, "out"));
+    if (list != nullptr) {
+        if (!aligned(list, 4)) return fail(BSA_ERR_ALIGNMENT, "list is not 4-byte aligned");
+        if (ld.q_group < 1 || ld.max_blocks < 1)
+            return fail(BSA_ERR_INVALID_ARG, "list needs q_group >= 1 and max_blocks >= 1");
+    }
+    if (mask.kind < BSA_MASK_NONE || mask.kind > BSA_MASK_SLIDING)
+        return fail(BSA_ERR_INVALID_ARG, "bad mask kind %d", mask.kind);
+    if (mask.kind == BSA_MASK_SLIDING && mask.sliding < 1)
+        return fail(BSA_ERR_INVALID_ARG, "sliding window needs W >= 1");
+    BSA_TRY(check_ws(ws, ws_bytes, bsa_fine_attention_workspace_size(shape, ld, mask)));
+    bsa::FineArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.list = list;
+    a.bh = shape.bh;
+    a.n = shape.n;
+    a.kb = ld.key_block;
+    a.nb = ceil_div(shape.n, ld.key_block);
+    a.d = shape.d;
+    a.q_group = list ? ld.q_group : 1;
+    a.max_blocks = list ? ld.max_blocks : 0;
+    a.per_head = ld.per_head ? 1 : 0;
+    a.list_rows = ceil_div(shape.n, a.q_group);
+    a.mask_kind = mask.kind;
+    a.window = mask.window;
+    a.stride = mask.stride;
+    a.sliding = mask.sliding;
+    a.scale_log2 = softmax_scale_log2(scale, shape.d);
+    a.status = device_status_ptr();
+    if (a.status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    return launched(bsa::launch_fine_query_major(a, shape.dtype, static_cast<cudaStream_t>(stream)),
+                    "fine attention launch");
+}
+
+size_t bsa_forward_workspace_size(bsa_shape shape, int32_t key_block, int32_t topk) {
+    if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1) return 0;
+    return forward_layout(shape, key_block, topk).total;
+}
+
+int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk) {
+    if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1 || topk > 32)
+        return -int32_t(BSA_ERR_INVALID_ARG);
+    return 3;   // pool, score + top-k, fine attention
+}
+
+bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void *v,
+                       int32_t key_block, int32_t topk, float scale, void *out, int32_t *idx_out,
+                       void *ws, size_t ws_bytes, void *stream) {
+    BSA_TRY(check_shape(shape));
+    if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "the dynamic forward takes bf16");
+    BSA_TRY(check_key_block(key_block));
+    if (topk < 1 || topk > 32) return fail(BSA_ERR_UNSUPPORTED, "topk must be in [1, 32] (got %d)", topk);
+    BSA_TRY(check_ptr(q, "q"));
+    BSA_TRY(check_ptr(k, "k"));
+    BSA_TRY(check_ptr(v, "v"));
+    BSA_TRY(check_ptr(out, "out"));
+    if (idx_out != nullptr) BSA_TRY(check_ptr(idx_out, "idx_out"));
+    const ForwardLayout L = forward_layout(shape, key_block, topk);
+    BSA_TRY(check_ws(ws, ws_bytes, L.total));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(ws);
+    float *kbar = reinterpret_cast<float *>(base + L.kbar);
+    int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(base + L.idx);
+    const int64_t nb = ceil_div(shape.n, key_block);
+
+    BSA_TRY(launched(bsa::launch_pool(k, shape.bh, shape.n, shape.d, key_block, kbar, nullptr,
+                                      nullptr, 0, st), "pool launch"));
+    BSA_TRY(launched(bsa::launch_coarse_topk_simt(q, kbar, shape.bh, shape.n, shape.d, nb, topk,
+                                                  idx, st), "coarse top-k launch"));
+    bsa::FineArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.list = idx;
+    a.bh = shape.bh;
+    a.n = shape.n;
+    a.kb = key_block;
+    a.nb = nb;
+    a.d = shape.d;
+    a.q_group = 1;
+    a.max_blocks = topk;
+    a.per_head = 1;
+    a.list_rows = shape.n;
+    a.mask_kind = BSA_MASK_NONE;
+    a.scale_log2 = softmax_scale_log2(scale, shape.d);
+    a.status = device_status_ptr();
+    if (a.status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
+}
+
+}  // extern "C"

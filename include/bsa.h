@@ -1,0 +1,216 @@
+/*
+ * bsa.h -- C ABI of libbsa.so: content-dependent block-sparse attention
+ * (forward) on one NVIDIA GB300 (sm_103a).
+ *
+ * The method (page "sparse-attention-triton-bench", section "Two-stage
+ * block indexer"):
+ *   Stage 1  mean-pool every B-token key block into a representative Kbar_b,
+ *            score every query against every block (q . Kbar_b) and keep the
+ *            k best blocks per query, ties to the lower block index;
+ *   Stage 2  softmax attention, scale 1/sqrt(d) by default, over only the
+ *            k*B tokens of the selected blocks, accumulated with an online
+ *            softmax state (running max m, running sum l, accumulator acc;
+ *            same page, section "The Triton kernel").
+ * The fine stage also runs over static block lists (page "yayme/CUDA-kernel"
+ * README: local window |i-j| <= w plus global stride j % s == 0, walked as a
+ * precomputed active-tile list; page "Block-Sparse & Linear Attention
+ * Kernels", section 2: block-sparse loop and the causal sliding window).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors Q, K, V, O are [bh][n][d] row-major (d fastest), contiguous,
+ *     element type given by bsa_shape.dtype.  bh = batch * heads.
+ *   - Every tensor pointer is a DEVICE pointer unless the parameter says
+ *     host.  Device pointers must be 16-byte aligned; workspaces 256-byte.
+ *   - The caller owns every buffer.  The library never allocates memory and
+ *     keeps no per-call state; calls only enqueue work on `stream` (a
+ *     cudaStream_t passed as void*, NULL = legacy default stream) and return
+ *     at once.  Results are ready when the stream reaches that point.
+ *   - Argument errors are detected on the host and returned synchronously;
+ *     nothing is enqueued then.  bsa_last_error() gives a one-line reason.
+ *   - Errors found by a kernel (a listed block index outside [0, nb), a
+ *     bounded wait that ran out) never trap: the kernel skips the offending
+ *     work, records the first such code in a device status word and
+ *     returns.  bsa_get_device_status() reads and clears that word.
+ *   - Supported: d in {64, 128}; key_block B in {16, 32, 64, 128};
+ *     dtype bf16 everywhere, fp32 for the fine stage.
+ */
+#ifndef BSA_H_
+#define BSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSA_OK = 0,
+    BSA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad enum value      */
+    BSA_ERR_UNSUPPORTED = 2,   /* valid request outside the supported set     */
+    BSA_ERR_BAD_INDEX = 3,     /* (device) a listed block id outside [0, nb)  */
+    BSA_ERR_WORKSPACE = 4,     /* workspace null or smaller than required     */
+    BSA_ERR_CUDA = 5,          /* a CUDA runtime call failed                  */
+    BSA_ERR_TIMEOUT = 6,       /* (device) a bounded barrier wait ran out     */
+    BSA_ERR_ALIGNMENT = 7      /* pointer not 16-byte (workspace: 256) aligned */
+} bsa_status;
+
+typedef enum { BSA_BF16 = 0, BSA_FP32 = 1 } bsa_dtype;
+
+/* Shape of Q, K, V and O: [bh][n][d], element type `dtype` (bsa_dtype). */
+typedef struct {
+    int64_t bh;
+    int64_t n;
+    int32_t d;
+    int32_t dtype;
+} bsa_shape;
+
+typedef enum {
+    BSA_MASK_NONE = 0,          /* every token of a listed block is attended   */
+    BSA_MASK_LOCAL_GLOBAL = 1,  /* |i-j| <= window  or  j % stride == 0        */
+    BSA_MASK_SLIDING = 2        /* causal window: i - sliding < j <= i         */
+} bsa_mask_kind;
+
+/*
+ * Token-level predicate applied inside the listed blocks (page
+ * "yayme/CUDA-kernel" README, sparsity pattern; page "Block-Sparse & Linear
+ * Attention Kernels", section 2, sliding window).  LOCAL_GLOBAL: window < 0
+ * disables the band, stride <= 0 disables the global columns.  SLIDING:
+ * sliding >= 1 is W, the number of keys up to and including the query.
+ */
+typedef struct {
+    int32_t kind;
+    int32_t window;
+    int32_t stride;
+    int32_t sliding;
+} bsa_mask;
+
+/*
+ * Layout of a block-index list.  The list is int32
+ *   [per_head ? bh : 1][ceil(n / q_group)][max_blocks]:
+ * row r serves queries [r*q_group, (r+1)*q_group); each row holds key-block
+ * ids (block b = tokens [b*key_block, min(n, (b+1)*key_block))) in strictly
+ * ascending order, padded with -1 at the tail only.
+ *   dynamic lists (stage 2):  q_group = 1, max_blocks = k, per_head = 1;
+ *   static lists:             q_group = the query-tile height, per_head = 0.
+ */
+typedef struct {
+    int32_t q_group;
+    int32_t key_block;
+    int32_t max_blocks;
+    int32_t per_head;
+} bsa_list_desc;
+
+/*
+ * Stage 1, pooling (page "sparse-attention-triton-bench", Two-stage block
+ * indexer, Stage 1: "mean-pooling the keys within" each block).
+ *   k     [bh][n][d] bf16 keys (device).
+ *   kbar  [bh][nb][d] fp32 output, nb = ceil(n / key_block) (device);
+ *         kbar[h][b] = mean of the valid keys of block b (a ragged last
+ *         block averages its n - b*key_block tokens).
+ */
+bsa_status bsa_pool_blocks(bsa_shape shape, const void *k, int32_t key_block,
+                           float *kbar, void *stream);
+
+/*
+ * Stage 1 scoring + Stage 2 selection (same page and section: score every
+ * query against every block representative, "take the top-k
+ * highest-scoring blocks").  Scores are q . Kbar_b (unscaled: a positive
+ * scale cannot change the ranking) and are never written to memory.
+ *   q     [bh][n][d] bf16 queries (device).
+ *   kbar  [bh][nb][d] fp32 block means, as written by bsa_pool_blocks.
+ *   idx   [bh][n][topk] int32 output (device): the min(topk, nb) selected
+ *         block ids of each query in ascending order, ties in score going to
+ *         the lower block id; entries past nb are -1.
+ *   ws    device workspace of bsa_coarse_topk_workspace_size() bytes.
+ * topk in [1, 32].
+ */
+size_t bsa_coarse_topk_workspace_size(bsa_shape shape, int32_t key_block,
+                                      int32_t topk);
+bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar,
+                           int32_t key_block, int32_t topk, int32_t *idx,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Stage 2, fine attention over a block list (page
+ * "sparse-attention-triton-bench", Stage 2 and "The Triton kernel": dense
+ * softmax attention over the listed blocks' tokens with an online-softmax
+ * state; page "Block-Sparse & Linear Attention Kernels", section 2: skip
+ * every unlisted block).
+ *   q, k, v  [bh][n][d] of shape.dtype (bf16 or fp32), device.
+ *   list     int32 block list laid out as `ld` says (device), or NULL for
+ *            every block of the sequence.
+ *   mask     token-level predicate inside listed blocks.
+ *   scale    softmax scale; <= 0 selects 1/sqrt(d).
+ *   out      [bh][n][d] of shape.dtype (device); a query whose list admits
+ *            no key gets zeros.
+ *   ws       device workspace of bsa_fine_attention_workspace_size() bytes.
+ * A listed id outside [0, nb) is skipped and reported as BSA_ERR_BAD_INDEX
+ * through bsa_get_device_status().
+ */
+size_t bsa_fine_attention_workspace_size(bsa_shape shape, bsa_list_desc ld,
+                                         bsa_mask mask);
+bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k,
+                              const void *v, const int32_t *list,
+                              bsa_list_desc ld, bsa_mask mask, float scale,
+                              void *out, void *ws, size_t ws_bytes,
+                              void *stream);
+
+/*
+ * The whole dynamic forward: pool -> score + top-k -> fine attention, all
+ * enqueued on `stream` (page "sparse-attention-triton-bench", Two-stage
+ * block indexer).  bf16 only, non-causal.
+ *   idx_out  optional [bh][n][topk] int32 (device) receiving the selection;
+ *            NULL keeps it in the workspace.
+ *   ws       device workspace of bsa_forward_workspace_size() bytes.
+ */
+size_t bsa_forward_workspace_size(bsa_shape shape, int32_t key_block,
+                                  int32_t topk);
+bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k,
+                       const void *v, int32_t key_block, int32_t topk,
+                       float scale, void *out, int32_t *idx_out, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Number of kernel launches one bsa_forward call enqueues for this problem
+ * (for launch accounting by callers); negative bsa_status on bad arguments. */
+int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk);
+
+/*
+ * Static block lists, built on the host, synchronously (page
+ * "yayme/CUDA-kernel" README: "precompute the list of active (row_tile,
+ * col_tile) pairs on the CPU and pass it in").  A key block is listed for a
+ * query tile iff at least one (query, key) pair inside it satisfies `mask`
+ * (BSA_MASK_NONE lists every block).
+ *   list          HOST int32 [ceil(n/q_group)][max_blocks], -1 padded.
+ *   counts        optional HOST int32 [ceil(n/q_group)]: blocks per row.
+ *   active_pairs  optional HOST int64: number of (i, j) pairs the mask
+ *                 admits over the whole sequence (one head).
+ * bsa_static_max_blocks() returns the smallest max_blocks that fits, or a
+ * negative bsa_status on invalid arguments.
+ */
+int32_t bsa_static_max_blocks(int64_t n, int32_t q_group, int32_t key_block,
+                              bsa_mask mask);
+bsa_status bsa_static_blocks(int64_t n, int32_t q_group, int32_t key_block,
+                             bsa_mask mask, int32_t *list, int32_t max_blocks,
+                             int32_t *counts, int64_t *active_pairs);
+
+/*
+ * Reads the device status word into *status (a bsa_status value), then
+ * clears it.  Synchronises `stream` first.
+ */
+bsa_status bsa_get_device_status(int32_t *status, void *stream);
+
+/* Static description of a status code. */
+const char *bsa_status_string(int32_t status);
+
+/* One-line reason for the last error returned on the calling thread. */
+const char *bsa_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t bsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSA_H_ */

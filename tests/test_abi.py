@@ -1,0 +1,112 @@
+"""The C-ABI library: it builds, loads, exports every declared symbol and
+rejects bad arguments on the host (no GPU needed: validation runs before any
+CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from content_dependent_block_gb300 import _build, bsa
+
+HEADER = os.path.join(_build.INCLUDE, "bsa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return bsa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert set(declared_functions()) == set(bsa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    assert L.bsa_version() >= 100
+    assert L.bsa_status_string(0) == b"ok"
+    assert L.bsa_status_string(3) == b"block index out of range"
+    assert L.bsa_status_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(0x10000)          # aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def _shape(bh=1, n=128, d=64, dtype=bsa.BF16):
+    return bsa.Shape(bh, n, d, dtype)
+
+
+@pytest.mark.parametrize("shape,code", [
+    (_shape(d=96), 2), (_shape(n=0), 1), (_shape(bh=0), 1), (_shape(dtype=7), 1),
+    (_shape(bh=70000), 2), (_shape(dtype=bsa.FP32), 2),
+])
+def test_forward_rejects_bad_shapes(L, shape, code):
+    r = L.bsa_forward(shape, FAKE, FAKE, FAKE, 64, 4, 0.0, FAKE, None, FAKE, 1 << 30, None)
+    assert r == code, L.bsa_last_error()
+
+
+@pytest.mark.parametrize("kb,topk,code", [(48, 4, 2), (64, 0, 2), (64, 33, 2), (256, 4, 2)])
+def test_forward_rejects_bad_block_or_k(L, kb, topk, code):
+    r = L.bsa_forward(_shape(), FAKE, FAKE, FAKE, kb, topk, 0.0, FAKE, None, FAKE, 1 << 30, None)
+    assert r == code
+
+
+def test_forward_rejects_null_misaligned_and_small_workspace(L):
+    s = _shape()
+    assert L.bsa_forward(s, None, FAKE, FAKE, 64, 4, 0.0, FAKE, None, FAKE, 1 << 30, None) == 1
+    assert L.bsa_forward(s, FAKE, MISALIGNED, FAKE, 64, 4, 0.0, FAKE, None, FAKE, 1 << 30, None) == 7
+    need = L.bsa_forward_workspace_size(s, 64, 4)
+    assert need > 0
+    assert L.bsa_forward(s, FAKE, FAKE, FAKE, 64, 4, 0.0, FAKE, None, FAKE, need - 1, None) == 4
+    assert L.bsa_forward(s, FAKE, FAKE, FAKE, 64, 4, 0.0, FAKE, None, None, need, None) == 4
+    assert L.bsa_forward(s, FAKE, FAKE, FAKE, 64, 4, 0.0, FAKE, None, ctypes.c_void_p(0x10010),
+                         need, None) == 7
+    assert b"workspace" in L.bsa_last_error() or b"aligned" in L.bsa_last_error()
+
+
+def test_fine_attention_rejects_bad_mask_and_list(L):
+    s = _shape(dtype=bsa.FP32)
+    ld = bsa.ListDesc(16, 16, 4, 0)
+    assert L.bsa_fine_attention(s, FAKE, FAKE, FAKE, FAKE, ld, bsa.mask_struct(5), 0.0, FAKE,
+                                None, 0, None) == 1
+    assert L.bsa_fine_attention(s, FAKE, FAKE, FAKE, FAKE, ld, bsa.mask_struct(2, sliding=0), 0.0,
+                                FAKE, None, 0, None) == 1
+    assert L.bsa_fine_attention(s, FAKE, FAKE, FAKE, FAKE, bsa.ListDesc(0, 16, 4, 0),
+                                bsa.mask_struct(), 0.0, FAKE, None, 0, None) == 1
+    assert L.bsa_fine_attention(s, FAKE, FAKE, FAKE, FAKE, bsa.ListDesc(16, 24, 4, 0),
+                                bsa.mask_struct(), 0.0, FAKE, None, 0, None) == 2
+
+
+def test_pool_and_coarse_reject_fp32(L):
+    s = _shape(dtype=bsa.FP32)
+    assert L.bsa_pool_blocks(s, FAKE, 64, FAKE, None) == 2
+    assert L.bsa_coarse_topk(s, FAKE, FAKE, 64, 4, FAKE, None, 0, None) == 2
+
+
+def test_static_blocks_rejects_bad_arguments(L):
+    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=0)
+    assert L.bsa_static_max_blocks(100, 16, 16, m) < 0
+    lst = (ctypes.c_int32 * 64)()
+    m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, 32, 512)
+    # too few slots per row
+    assert L.bsa_static_blocks(4096, 16, 16, m, ctypes.cast(lst, ctypes.c_void_p), 2, None, None) == 1
+    assert L.bsa_static_blocks(4096, 16, 16, m, None, 16, None, None) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(bsa, "_lib", None)
+    monkeypatch.setattr(bsa, "library_path", lambda: str(tmp_path / "absent.so"))
+    with pytest.raises(bsa.BsaError):
+        bsa.lib()

@@ -1,0 +1,212 @@
+"""CUDA path vs the fp64 oracle, element by element, on seeded inputs.
+
+Small workloads are compared on every row; the long-context ones (n = 32k
+and 131k) on seeded row samples the oracle computes one by one, through the
+same reusable ``Forward`` object the benchmark times.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from content_dependent_block_gb300 import _build, bsa
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    _build.build()
+    bsa.lib()
+    assert bsa.device_status() == 0
+
+
+_cache = {}
+
+
+def tensors(name, **kw):
+    key = (name, tuple(sorted(kw.items())))
+    if key not in _cache:
+        _cache.clear()
+        w = W[name]
+        t = workloads.generate(w, **kw)
+        dev = tuple(parity.to_device(getattr(t, x), t.dtype) for x in "qkv")
+        _cache[key] = (w, t, dev)
+    return _cache[key]
+
+
+def rows_for(w, bh, n, full_limit=70000, per_head=48):
+    if bh * n <= full_limit:
+        return oracle.all_rows(bh, n)
+    return workloads.sample_rows(bh, n, per_head, extra=(w.key_block - 1, w.key_block, n // 2))
+
+
+DYN = ["dyn_n1024", "dyn_n8192", "dyn_n32768", "dyn_n131072"]
+
+
+@pytest.mark.parametrize("name", DYN)
+def test_pool_matches_oracle(name):
+    w, t, (q, k, v) = tensors(name)
+    kbar = bsa.pool_blocks(k, w.key_block)
+    ref = oracle.pool(t.k, w.key_block)
+    got = kbar.cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref).max() <= 1e-5 * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("name", DYN)
+def test_coarse_topk_matches_oracle_within_tie_band(name):
+    w, t, (q, k, v) = tensors(name)
+    kbar = bsa.pool_blocks(k, w.key_block)
+    idx = bsa.coarse_topk(q, kbar, w.key_block, w.topk)
+    rows = rows_for(w, w.bh, w.n)
+    res_kbar = oracle.pool(t.k, w.key_block)
+    s = oracle.scores(t.q, res_kbar, rows)
+    oidx, kth = oracle.topk(s, w.topk)
+    gidx = idx.cpu().numpy().reshape(-1, w.topk)[rows]
+    differing = parity.check_selection(gidx, oidx, s, kth, w.nb)
+    assert differing <= max(2, rows.size // 200), f"{differing} rows differ (all within band)"
+    assert bsa.device_status() == 0
+
+
+@pytest.mark.parametrize("name", DYN)
+def test_fine_stage_on_oracle_indices(name):
+    w, t, (q, k, v) = tensors(name)
+    rows = rows_for(w, w.bh, w.n)
+    s = oracle.scores(t.q, oracle.pool(t.k, w.key_block), rows)
+    oidx, _ = oracle.topk(s, w.topk)
+    # the list is the GPU's own selection except on the compared rows, which
+    # carry the oracle's selection
+    kbar = bsa.pool_blocks(k, w.key_block)
+    lst = bsa.coarse_topk(q, kbar, w.key_block, w.topk).reshape(-1, w.topk)
+    import torch
+    lst[torch.from_numpy(rows).cuda()] = torch.from_numpy(oidx).cuda()
+    out = bsa.fine_attention(q, k, v, lst.reshape(w.bh, w.n, w.topk), key_block=w.key_block)
+    o_ref, _, _ = oracle.fine(t.q, t.k, t.v, w.key_block, oidx, rows)
+    got = parity.from_device(out).reshape(-1, w.d)[rows]
+    parity.assert_close(got, o_ref, "bf16", f"{name} fine stage")
+    assert bsa.device_status() == 0
+
+
+@pytest.mark.parametrize("name", DYN)
+def test_forward_matches_oracle(name):
+    w, t, (q, k, v) = tensors(name)
+    f = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk)
+    out = f(q, k, v)
+    rows = rows_for(w, w.bh, w.n)
+    s = oracle.scores(t.q, oracle.pool(t.k, w.key_block), rows)
+    oidx, kth = oracle.topk(s, w.topk)
+    gidx = f.idx.cpu().numpy().reshape(-1, w.topk)[rows]
+    parity.check_selection(gidx, oidx, s, kth, w.nb)
+    # the oracle recomputes the fine stage on the GPU's (validated) selection
+    o_ref, _, psum = oracle.fine(t.q, t.k, t.v, w.key_block, gidx, rows)
+    np.testing.assert_allclose(psum, 1.0, atol=1e-12)
+    got = parity.from_device(out).reshape(-1, w.d)[rows]
+    parity.assert_close(got, o_ref, "bf16", f"{name} forward")
+    assert bsa.device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["local_global_n4096", "local_global_n4100"])
+def test_static_local_global_fp32(name):
+    w, t, (q, k, v) = tensors(name)
+    m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, w.window, w.stride)
+    lst, counts, pairs = bsa.static_blocks(w.n, w.q_group, w.key_block, m)
+    import torch
+    dl = torch.from_numpy(lst).cuda()
+    out = bsa.fine_attention(q, k, v, dl, key_block=w.key_block, q_group=w.q_group,
+                             per_head=False, mask=m)
+    rows = oracle.all_rows(w.bh, w.n)
+    o_ref, _, _ = oracle.masked(t.q, t.k, t.v, oracle.MASK_LOCAL_GLOBAL, rows, w=w.window, s=w.stride)
+    parity.assert_close(parity.from_device(out).reshape(-1, w.d), o_ref, "fp32", name)
+    assert bsa.device_status() == 0
+
+
+def test_static_sliding_n131072_sampled():
+    w, t, (q, k, v) = tensors("dyn_n131072")       # same tensors, as the workload says
+    sw = W["sliding_n131072"]
+    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=sw.sliding)
+    lst, _, _ = bsa.static_blocks(sw.n, sw.q_group, sw.key_block, m)
+    import torch
+    out = bsa.fine_attention(q, k, v, torch.from_numpy(lst).cuda(), key_block=sw.key_block,
+                             q_group=sw.q_group, per_head=False, mask=m)
+    rows = workloads.sample_rows(sw.bh, sw.n, 24, extra=(1, 63, 64, 4095, 4096, 4097))
+    o_ref, _, _ = oracle.masked(t.q, t.k, t.v, oracle.MASK_SLIDING, rows, W=sw.sliding)
+    got = parity.from_device(out).reshape(-1, sw.d)[rows]
+    parity.assert_close(got, o_ref, "bf16", "sliding n131072")
+    assert bsa.device_status() == 0
+
+
+# ------------------------------------------------------------ edge cases
+def _small(bh, n, d, seed, dtype="bf16", sigma=0.0, kb=64):
+    w = workloads.Workload("edge", bh=bh, n=n, d=d, dtype=dtype, kind="dynamic", key_block=kb,
+                           topk=4, centre_sigma=sigma, seed=seed)
+    t = workloads.generate(w)
+    return t, tuple(parity.to_device(getattr(t, x), dtype) for x in "qkv")
+
+
+@pytest.mark.parametrize("bh,n,d,kb,topk", [
+    (1, 1000, 64, 64, 4),      # ragged last block (40 tokens)
+    (2, 300, 128, 32, 5),      # d=128, ragged, odd k
+    (1, 40, 64, 64, 2),        # n < B: one partial block, k > nb
+    (1, 1, 64, 16, 1),         # a single token
+    (3, 256, 64, 64, 8),       # k*B >= n: dense attention
+    (1, 4100, 64, 16, 32),     # many blocks, k = 32
+])
+def test_forward_edge_shapes(bh, n, d, kb, topk):
+    t, (q, k, v) = _small(bh, n, d, seed=n + d, sigma=0.5, kb=kb)
+    out, idx = bsa.forward(q, k, v, kb, topk)
+    rows = oracle.all_rows(bh, n)
+    nb = -(-n // kb)
+    s = oracle.scores(t.q, oracle.pool(t.k, kb), rows)
+    oidx, kth = oracle.topk(s, topk)
+    gidx = idx.cpu().numpy().reshape(-1, topk)
+    parity.check_selection(gidx, oidx, s, kth, nb)
+    o_ref, _, _ = oracle.fine(t.q, t.k, t.v, kb, gidx, rows)
+    parity.assert_close(parity.from_device(out).reshape(-1, d), o_ref, "bf16", "edge forward")
+    if topk * kb >= n:
+        dense, _, _ = oracle.masked(t.q, t.k, t.v, 0, rows)
+        parity.assert_close(parity.from_device(out).reshape(-1, d), dense, "bf16", "dense limit")
+    assert bsa.device_status() == 0
+
+
+def test_fine_empty_rows_give_zeros_and_bad_index_is_reported():
+    import torch
+    t, (q, k, v) = _small(1, 512, 64, seed=5)
+    nb = 8
+    lst = np.tile(np.array([[0, 3, 5, -1]], np.int32), (512, 1))
+    lst[10] = -1                       # empty row -> zeros
+    lst[11] = [1, 2, 99, -1]           # out-of-range id -> skipped + reported
+    out = bsa.fine_attention(q, k, v, torch.from_numpy(lst).cuda().reshape(1, 512, 4), key_block=64)
+    assert bsa.device_status() == 3   # BSA_ERR_BAD_INDEX
+    got = parity.from_device(out).reshape(-1, 64)
+    assert (parity.out_f64(got[10]) == 0).all()
+    ref_list = lst.copy()
+    ref_list[11] = [1, 2, -1, -1]
+    rows = oracle.all_rows(1, 512)
+    o_ref, _, _ = oracle.fine(t.q, t.k, t.v, 64, ref_list, rows)
+    keep = np.ones(512, bool)
+    keep[10] = False
+    parity.assert_close(got[keep], o_ref[keep], "bf16", "listed rows")
+    assert nb == 8
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_fine_explicit_scale_and_dtype(dtype):
+    import torch
+    t, (q, k, v) = _small(2, 640, 64, seed=9, dtype=dtype)
+    rng = np.random.default_rng(0)
+    lst = np.stack([np.sort(rng.choice(10, 3, replace=False)) for _ in range(2 * 640)]).astype(np.int32)
+    out = bsa.fine_attention(q, k, v, torch.from_numpy(lst).cuda().reshape(2, 640, 3),
+                             key_block=64, scale=0.3)
+    o_ref, _, _ = oracle.fine(t.q, t.k, t.v, 64, lst, oracle.all_rows(2, 640), scale=0.3)
+    parity.assert_close(parity.from_device(out).reshape(-1, 64), o_ref, dtype, "scaled fine")
+
+
+def test_dense_list_null_is_full_attention():
+    t, (q, k, v) = _small(1, 200, 64, seed=3, dtype="fp32")
+    out = bsa.fine_attention(q, k, v, None, key_block=32)
+    rows = oracle.all_rows(1, 200)
+    dense, _, _ = oracle.masked(t.q, t.k, t.v, 0, rows)
+    parity.assert_close(parity.from_device(out).reshape(-1, 64), dense, "fp32", "null list")
