@@ -192,7 +192,7 @@ def oracle_sample(w, t, seconds: float):
     import numpy as np
     import oracle
     cores = oracle.num_threads()
-    per_row = metrics.sparse_flops(1, 1, w.d, w.key_block, w.topk)
+    per_row = metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk) / (w.n * w.bh)
 
     def run(nrows):
         rows = workloads.sample_rows(w.bh, w.n, max(1, nrows // w.bh), seed=7)
@@ -220,7 +220,7 @@ def reference_arm(args, rank, world, w):
     import oracle  # noqa: F401
     t = workloads.generate(w)
     cores = None
-    per_row = metrics.sparse_flops(1, 1, w.d, w.key_block, w.topk)
+    per_row = metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk) / (w.n * w.bh)
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     _, rows, secs, cores, desc = oracle_sample(w, t, budget)
     import oracle as orc
