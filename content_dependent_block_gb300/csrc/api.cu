@@ -90,21 +90,36 @@ bsa_status launched(cudaError_t e, const char *what) {
         if (st_ != BSA_OK) return st_;     \
     } while (0)
 
-// Workspace of the whole forward: block means, then the selection.
+// Workspace of the whole forward: fp32 block means, their bf16 hi/lo pair
+// (tensor-core scoring), then the selection.
 struct ForwardLayout {
-    size_t kbar = 0, idx = 0, total = 0;
+    size_t kbar = 0, hi = 0, lo = 0, idx = 0, total = 0;
 };
 
 ForwardLayout forward_layout(const bsa_shape &s, int32_t kb, int32_t topk) {
     ForwardLayout L;
     const int64_t nb = ceil_div(s.n, kb);
+    const size_t means = size_t(s.bh) * nb * s.d;
     size_t off = 0;
     L.kbar = off;
-    off = round_up(off + size_t(s.bh) * nb * s.d * sizeof(float), 256);
+    off = round_up(off + means * sizeof(float), 256);
+    L.hi = off;
+    off = round_up(off + means * sizeof(uint16_t), 256);
+    L.lo = off;
+    off = round_up(off + means * sizeof(uint16_t), 256);
     L.idx = off;
     off = round_up(off + size_t(s.bh) * s.n * topk * sizeof(int32_t), 256);
     L.total = off;
     return L;
+}
+
+// Scoring + selection from fp32 means (and their bf16 pair when present).
+cudaError_t run_coarse(const bsa_shape &s, const void *q, const float *kbar, const uint16_t *hi,
+                       const uint16_t *lo, int64_t nb, int32_t topk, int32_t *idx,
+                       int32_t *status, cudaStream_t st) {
+    if (hi != nullptr && bsa::coarse_tc_supported(nb))
+        return bsa::launch_coarse_topk_tc(q, hi, lo, s.bh, s.n, s.d, nb, topk, idx, status, st);
+    return bsa::launch_coarse_topk_simt(q, kbar, s.bh, s.n, s.d, nb, topk, idx, st);
 }
 
 float softmax_scale_log2(float scale, int32_t d) {
@@ -161,7 +176,13 @@ bsa_status bsa_pool_blocks(bsa_shape shape, const void *k, int32_t key_block, fl
                     "pool launch");
 }
 
-size_t bsa_coarse_topk_workspace_size(bsa_shape, int32_t, int32_t) { return 0; }
+size_t bsa_coarse_topk_workspace_size(bsa_shape shape, int32_t key_block, int32_t) {
+    if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK) return 0;
+    const int64_t nb = ceil_div(shape.n, key_block);
+    if (!bsa::coarse_tc_supported(nb)) return 0;
+    const size_t half = round_up(size_t(shape.bh) * nb * shape.d * sizeof(uint16_t), 256);
+    return 2 * half;   // bf16 hi / lo copies of the block means
+}
 
 bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, int32_t key_block,
                            int32_t topk, int32_t *idx, void *ws, size_t ws_bytes, void *stream) {
@@ -172,10 +193,20 @@ bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, in
     BSA_TRY(check_ptr(q, "q"));
     BSA_TRY(check_ptr(kbar, "kbar"));
     BSA_TRY(check_ptr(idx, "idx"));
-    BSA_TRY(check_ws(ws, ws_bytes, bsa_coarse_topk_workspace_size(shape, key_block, topk)));
+    const size_t need = bsa_coarse_topk_workspace_size(shape, key_block, topk);
+    BSA_TRY(check_ws(ws, ws_bytes, need));
     const int64_t nb = ceil_div(shape.n, key_block);
-    return launched(bsa::launch_coarse_topk_simt(q, kbar, shape.bh, shape.n, shape.d, nb, topk, idx,
-                                                 static_cast<cudaStream_t>(stream)),
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t *status = device_status_ptr();
+    if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    uint16_t *hi = nullptr, *lo = nullptr;
+    if (need > 0) {
+        hi = static_cast<uint16_t *>(ws);
+        lo = reinterpret_cast<uint16_t *>(static_cast<char *>(ws) + need / 2);
+        BSA_TRY(launched(bsa::launch_split_kbar(kbar, shape.bh * nb * shape.d, hi, lo, st),
+                         "split launch"));
+    }
+    return launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, idx, status, st),
                     "coarse top-k launch");
 }
 
@@ -234,7 +265,7 @@ size_t bsa_forward_workspace_size(bsa_shape shape, int32_t key_block, int32_t to
 int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk) {
     if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1 || topk > 32)
         return -int32_t(BSA_ERR_INVALID_ARG);
-    return 3;   // pool, score + top-k, fine attention
+    return 3;   // pool (+ hi/lo), score + top-k, fine attention
 }
 
 bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void *v,
@@ -254,13 +285,17 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(ws);
     float *kbar = reinterpret_cast<float *>(base + L.kbar);
+    uint16_t *hi = reinterpret_cast<uint16_t *>(base + L.hi);
+    uint16_t *lo = reinterpret_cast<uint16_t *>(base + L.lo);
     int32_t *idx = idx_out ? idx_out : reinterpret_cast<int32_t *>(base + L.idx);
     const int64_t nb = ceil_div(shape.n, key_block);
+    int32_t *status = device_status_ptr();
+    if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
 
-    BSA_TRY(launched(bsa::launch_pool(k, shape.bh, shape.n, shape.d, key_block, kbar, nullptr,
-                                      nullptr, 0, st), "pool launch"));
-    BSA_TRY(launched(bsa::launch_coarse_topk_simt(q, kbar, shape.bh, shape.n, shape.d, nb, topk,
-                                                  idx, st), "coarse top-k launch"));
+    BSA_TRY(launched(bsa::launch_pool(k, shape.bh, shape.n, shape.d, key_block, kbar, hi, lo, nb,
+                                      st), "pool launch"));
+    BSA_TRY(launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, idx, status, st),
+                     "coarse top-k launch"));
     bsa::FineArgs a{};
     a.q = q;
     a.k = k;
@@ -278,8 +313,7 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     a.list_rows = shape.n;
     a.mask_kind = BSA_MASK_NONE;
     a.scale_log2 = softmax_scale_log2(scale, shape.d);
-    a.status = device_status_ptr();
-    if (a.status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    a.status = status;
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }
 

@@ -41,6 +41,16 @@ cudaError_t launch_coarse_topk_simt(const void *q, const float *kbar,
                                     int64_t nb, int32_t topk, int32_t *idx,
                                     cudaStream_t st);
 
+// fp32 block means -> bf16 (hi, lo) pair for the tensor-core scoring.
+cudaError_t launch_split_kbar(const float *kbar, int64_t count, uint16_t *hi, uint16_t *lo,
+                              cudaStream_t st);
+
+// Tensor-core scoring + top-k.  Needs ceil(log2 nb) <= 12 (nb <= 4096).
+bool coarse_tc_supported(int64_t nb);
+cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const uint16_t *kbar_lo,
+                                  int64_t bh, int64_t n, int32_t d, int64_t nb, int32_t topk,
+                                  int32_t *idx, int32_t *status, cudaStream_t st);
+
 cudaError_t launch_fine_query_major(const FineArgs &a, int32_t dtype,
                                     cudaStream_t st);
 

@@ -1,0 +1,318 @@
+// Stage 1 scoring + Stage 2 selection on the tensor cores (page
+// "sparse-attention-triton-bench", Two-stage block indexer: score every
+// query against every block mean -- "Q @ K_block_repr.T" -- and keep the
+// top-k blocks per query).
+//
+// The scoring is a dense contraction S = Q . Kbar^T, so it runs as tcgen05
+// MMAs into tensor memory; the N x N/B score matrix never reaches HBM.
+//
+// One CTA owns a 128-query tile of one head (M = 128 TMEM lanes, one query
+// per lane) and streams the head's block means through shared memory in
+// chunks of kChunk = 128 blocks (MMA N = 128), double-buffered in shared
+// memory and in tensor memory:
+//   warp 0      TMA producer: Q tile once, then Kbar chunks (hi and lo parts)
+//   warp 1      allocates tensor memory; one lane issues the MMAs
+//   warps 2..5  epilogue: each thread reads its query's scores from tensor
+//               memory (tcgen05.ld 32 columns at a time) and keeps a running
+//               top-k in registers
+// Precision: Kbar enters as a bf16 pair (hi = bf16(Kbar), lo = bf16(Kbar -
+// hi)); S = Q.hi + Q.lo accumulates in fp32, i.e. about 2^-16 relative to
+// the fp32 mean -- far inside the 1e-3 relative tie band of the selection.
+// Q is bf16 already, so it is exact.
+//
+// Top-k keys: each score becomes one order-preserving 32-bit key whose low
+// `bits` = ceil(log2 nb) bits hold (mask - block): a larger key is a larger
+// score, and equal truncated scores rank the lower block first.  The
+// truncation drops `bits` mantissa bits (<= 2^-11 relative for nb <= 4096),
+// so two blocks can only swap when their scores agree to that precision.
+// The register list is kept sorted by a compare-exchange pass (min/max).
+#include <climits>
+
+#include <cudaTypedefs.h>
+
+#include "bsa_device.cuh"
+#include "bsa_internal.h"
+#include "tc.cuh"
+
+namespace bsa {
+namespace {
+
+constexpr int kTileM = 128;        // queries per CTA (TMEM lanes)
+constexpr int kChunk = 128;        // blocks per MMA (N)
+constexpr int kStages = 2;         // shared-memory stages of Kbar chunks
+constexpr int kThreads = 192;      // 6 warps
+constexpr int kTmemCols = 2 * kChunk;
+
+template <int D>
+struct CoarseSmem {
+    static constexpr int kSub = D / 64;                       // 128-byte K slabs
+    static constexpr int kQBytes = kSub * kTileM * 128;
+    static constexpr int kKBytes = kSub * kChunk * 128;       // one of hi / lo
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kTiles = kQBytes + kStages * kStageBytes;
+    static constexpr int kTotal = kTiles + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+__device__ __forceinline__ uint32_t score_key(float s, uint32_t col, uint32_t mask) {
+    uint32_t u = __float_as_uint(s);
+    u ^= uint32_t(int32_t(u) >> 31) | 0x80000000u;
+    return (u & ~mask) | (mask - col);
+}
+
+template <int KMAX>
+__device__ __forceinline__ void key_insert(uint32_t (&L)[KMAX], uint32_t key) {
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+        const uint32_t o = L[t];
+        L[t] = max(o, key);
+        key = min(o, key);
+    }
+}
+
+template <int D, int KMAX>
+__global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_hi,
+    const __grid_constant__ CUtensorMap tm_lo, int64_t n, int64_t nb, int32_t topk,
+    uint32_t key_mask, int32_t *__restrict__ idx, int32_t *status) {
+    using S = CoarseSmem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sK = smem + S::kQBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kTiles);
+    uint64_t *q_full = bars + 0;
+    uint64_t *kv_full = bars + 1;       // [kStages]
+    uint64_t *kv_empty = bars + 3;      // [kStages]
+    uint64_t *acc_full = bars + 5;      // [2]
+    uint64_t *acc_empty = bars + 7;     // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t h = blockIdx.y;
+    const int64_t row0 = int64_t(blockIdx.x) * kTileM;
+    const int nchunks = int((nb + kChunk - 1) / kChunk);
+    // A wait elsewhere already ran out: do no work (results are invalid anyway).
+    if (status != nullptr && *reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
+
+    if (threadIdx.x == 0) {
+        tc::mbar_init(q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(kv_full + s, 1);
+            tc::mbar_init(kv_empty + s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(acc_full + s, 1);
+            tc::mbar_init(acc_empty + s, kTileM);
+        }
+        tc::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tensormap(&tm_q);
+        tc::prefetch_tensormap(&tm_hi);
+        tc::prefetch_tensormap(&tm_lo);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------- TMA producer
+            tc::mbar_arrive_expect_tx(q_full, S::kQBytes);
+#pragma unroll
+            for (int sub = 0; sub < S::kSub; ++sub)
+                tc::tma_load_3d(sQ + sub * kTileM * 128, &tm_q, q_full, sub * 64, int32_t(row0),
+                                int32_t(h));
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kStages;
+                const int use = c / kStages;
+                if (use > 0 && !tc::mbar_wait(kv_empty + s, (use - 1) & 1, status)) break;
+                uint8_t *hi = sK + s * S::kStageBytes;
+                uint8_t *lo = hi + S::kKBytes;
+                tc::mbar_arrive_expect_tx(kv_full + s, S::kStageBytes);
+#pragma unroll
+                for (int sub = 0; sub < S::kSub; ++sub) {
+                    tc::tma_load_3d(hi + sub * kChunk * 128, &tm_hi, kv_full + s, sub * 64,
+                                    c * kChunk, int32_t(h));
+                    tc::tma_load_3d(lo + sub * kChunk * 128, &tm_lo, kv_full + s, sub * 64,
+                                    c * kChunk, int32_t(h));
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileM, kChunk);
+            bool ok = tc::mbar_wait(q_full, 0, status);
+            const uint32_t q_addr = tc::smem_u32(sQ);
+            for (int c = 0; ok && c < nchunks; ++c) {
+                const int s = c % kStages;
+                const int buf = c & 1;
+                if (!tc::mbar_wait(kv_full + s, (c / kStages) & 1, status)) break;
+                if (c >= 2 && !tc::mbar_wait(acc_empty + buf, ((c >> 1) - 1) & 1, status)) break;
+                tc::tc_fence_after();
+                const uint32_t hi_addr = tc::smem_u32(sK + s * S::kStageBytes);
+                const uint32_t lo_addr = hi_addr + S::kKBytes;
+                const uint32_t d_tmem = tmem + uint32_t(buf * kChunk);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = uint32_t((kk >> 2) * kTileM * 128 + (kk & 3) * 32);
+                    const uint32_t boff = uint32_t((kk >> 2) * kChunk * 128 + (kk & 3) * 32);
+                    tc::mma_bf16(d_tmem, tc::smem_desc_sw128(q_addr + koff, 1024),
+                                 tc::smem_desc_sw128(hi_addr + boff, 1024), idesc, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = uint32_t((kk >> 2) * kTileM * 128 + (kk & 3) * 32);
+                    const uint32_t boff = uint32_t((kk >> 2) * kChunk * 128 + (kk & 3) * 32);
+                    tc::mma_bf16(d_tmem, tc::smem_desc_sw128(q_addr + koff, 1024),
+                                 tc::smem_desc_sw128(lo_addr + boff, 1024), idesc, 1);
+                }
+                tc::mma_commit(kv_empty + s);
+                tc::mma_commit(acc_full + buf);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int r = quad * 32 + lane;            // row inside the tile
+        uint32_t L[KMAX];
+#pragma unroll
+        for (int t = 0; t < KMAX; ++t) L[t] = 0u;  // 0 = empty (below every real key)
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int buf = c & 1;
+            if (ok) ok = tc::mbar_wait(acc_full + buf, (c >> 1) & 1, status);
+            tc::tc_fence_after();
+            if (ok) {
+                const int valid = int(i64min(kChunk, nb - int64_t(c) * kChunk));
+                for (int j = 0; j < kChunk / 32; ++j) {
+                    if (j * 32 >= valid) break;
+                    uint32_t v[32];
+                    tc::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kChunk + j * 32), v);
+                    tc::tmem_ld_wait();
+                    const uint32_t col0 = uint32_t(c * kChunk + j * 32);
+                    const int lim = valid - j * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if (e < lim) {
+                            const uint32_t key = score_key(__uint_as_float(v[e]), col0 + e, key_mask);
+                            if (key > L[KMAX - 1]) key_insert<KMAX>(L, key);
+                        }
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(acc_empty + buf);
+        }
+        const int64_t i = row0 + r;
+        if (i < n) {
+            int ids[KMAX];
+            const int kk = int(i64min(topk, nb));
+#pragma unroll
+            for (int t = 0; t < KMAX; ++t)
+                ids[t] = (t < kk && L[t] != 0u) ? int(key_mask - (L[t] & key_mask)) : INT_MAX;
+#pragma unroll
+            for (int round = 0; round < KMAX; ++round) {
+#pragma unroll
+                for (int t = round & 1; t + 1 < KMAX; t += 2) {
+                    const int a = ids[t], b = ids[t + 1];
+                    ids[t] = min(a, b);
+                    ids[t + 1] = max(a, b);
+                }
+            }
+            int32_t *dst = idx + (h * n + i) * topk;
+#pragma unroll
+            for (int t = 0; t < KMAX; ++t)
+                if (t < topk) dst[t] = ids[t] == INT_MAX ? -1 : ids[t];
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// --------------------------------------------------------------- host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [outer][rows][d] bf16 tensor, box of 64 x box_rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int64_t outer, int64_t rows, int d, int box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(rows), cuuint64_t(outer)};
+    cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(rows) * d * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int KMAX>
+cudaError_t launch_dk(const CUtensorMap &mq, const CUtensorMap &mh, const CUtensorMap &ml,
+                      int64_t bh, int64_t n, int64_t nb, int32_t topk, uint32_t mask, int32_t *idx,
+                      int32_t *status, cudaStream_t st) {
+    const int smem = CoarseSmem<D>::kTotal;
+    auto kern = coarse_topk_tc_kernel<D, KMAX>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(unsigned((n + kTileM - 1) / kTileM), unsigned(bh));
+    kern<<<grid, kThreads, smem, st>>>(mq, mh, ml, n, nb, topk, mask, idx, status);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap &mq, const CUtensorMap &mh, const CUtensorMap &ml,
+                     int64_t bh, int64_t n, int64_t nb, int32_t topk, uint32_t mask, int32_t *idx,
+                     int32_t *status, cudaStream_t st) {
+    if (topk <= 4) return launch_dk<D, 4>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+    if (topk <= 8) return launch_dk<D, 8>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+    if (topk <= 16) return launch_dk<D, 16>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+    return launch_dk<D, 32>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+}
+
+}  // namespace
+
+int coarse_tc_key_bits(int64_t nb) {
+    int bits = 1;
+    while ((int64_t(1) << bits) < nb) ++bits;
+    return bits;
+}
+
+bool coarse_tc_supported(int64_t nb) { return coarse_tc_key_bits(nb) <= 12; }
+
+cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const uint16_t *kbar_lo,
+                                  int64_t bh, int64_t n, int32_t d, int64_t nb, int32_t topk,
+                                  int32_t *idx, int32_t *status, cudaStream_t st) {
+    CUtensorMap mq, mh, ml;
+    if (!make_map(&mq, q, bh, n, d, kTileM) || !make_map(&mh, kbar_hi, bh, nb, d, kChunk) ||
+        !make_map(&ml, kbar_lo, bh, nb, d, kChunk))
+        return cudaErrorInvalidValue;
+    const uint32_t mask = (1u << coarse_tc_key_bits(nb)) - 1u;
+    if (d == 64) return launch_d<64>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+    return launch_d<128>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+}
+
+}  // namespace bsa

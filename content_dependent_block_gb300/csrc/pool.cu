@@ -89,7 +89,27 @@ __global__ void __launch_bounds__(256) pool_kernel(
     }
 }
 
+// fp32 block means -> bf16 hi/lo pair (hi = bf16(x), lo = bf16(x - hi)).
+__global__ void __launch_bounds__(256) split_kernel(const float *__restrict__ x, int64_t count,
+                                                    uint16_t *__restrict__ hi,
+                                                    uint16_t *__restrict__ lo) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= count) return;
+    const float v = x[i];
+    const uint16_t hb = f32_to_bf16_bits(v);
+    hi[i] = hb;
+    lo[i] = f32_to_bf16_bits(v - __uint_as_float(uint32_t(hb) << 16));
+}
+
 }  // namespace
+
+cudaError_t launch_split_kbar(const float *kbar, int64_t count, uint16_t *hi, uint16_t *lo,
+                              cudaStream_t st) {
+    const int threads = 256;
+    const int64_t blocks = (count + threads - 1) / threads;
+    split_kernel<<<dim3(unsigned(blocks)), threads, 0, st>>>(kbar, count, hi, lo);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_pool(const void *k, int64_t bh, int64_t n, int32_t d,
                         int32_t kb, float *kbar, uint16_t *kbar_hi,
