@@ -170,7 +170,7 @@ def measured_peaks():
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel's
     source has not changed since it was captured; else None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
