@@ -27,7 +27,7 @@ STATUS = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
 EXPORTS = (
     "bsa_pool_blocks", "bsa_coarse_topk_workspace_size", "bsa_coarse_topk",
     "bsa_fine_attention_workspace_size", "bsa_fine_attention",
-    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_launches",
+    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_noalloc", "bsa_forward_launches",
     "bsa_static_max_blocks",
     "bsa_static_blocks", "bsa_get_device_status", "bsa_status_string",
     "bsa_last_error", "bsa_version",
@@ -81,6 +81,7 @@ def lib():
         "bsa_fine_attention": ([Shape, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, sz, vp], i32),
         "bsa_forward_workspace_size": ([Shape, i32, i32], sz),
         "bsa_forward": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp], i32),
+        "bsa_forward_noalloc": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp], i32),
         "bsa_forward_launches": ([Shape, i32, i32], i32),
         "bsa_static_max_blocks": ([i64, i32, i32, Mask], i32),
         "bsa_static_blocks": ([i64, i32, i32, Mask, vp, i32, vp, vp], i32),
@@ -218,6 +219,18 @@ def forward(q, k, v, key_block: int, topk: int, scale: float = 0.0) -> Tuple[obj
     f = Forward(s.bh, s.n, s.d, key_block, topk, device=q.device, scale=scale)
     out = f(q, k, v, keep_idx=True)
     return out, f.idx
+
+
+def forward_noalloc(q, k, v, key_block: int, topk: int, scale: float = 0.0, out=None, idx=None):
+    """Whole dynamic forward using the library's static scratch (no workspace
+    allocation); returns (out, idx).  See bsa_forward_noalloc in bsa.h."""
+    torch = _torch()
+    s = _shape(q)
+    out = torch.empty_like(q) if out is None else out
+    idx = torch.empty((s.bh, s.n, topk), dtype=torch.int32, device=q.device) if idx is None else idx
+    _check(lib().bsa_forward_noalloc(s, _ptr(q), _ptr(k), _ptr(v), key_block, topk, float(scale),
+                                     _ptr(out), _ptr(idx), _stream()))
+    return out, idx
 
 
 def static_blocks(n: int, q_group: int, key_block: int, mask: Mask):

@@ -129,6 +129,10 @@ float softmax_scale_log2(float scale, int32_t d) {
 
 }  // namespace
 
+namespace bsa {
+void set_last_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+}  // namespace bsa
+
 extern "C" {
 
 int32_t bsa_version(void) { return kVersion; }

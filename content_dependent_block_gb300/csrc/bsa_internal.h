@@ -31,6 +31,9 @@ struct FineArgs {
     int32_t *status;       // device status word
 };
 
+// Records the one-line reason bsa_last_error() reports on this thread.
+void set_last_error(const char *msg);
+
 // Launchers return the cudaError_t of the launch.
 cudaError_t launch_pool(const void *k, int64_t bh, int64_t n, int32_t d,
                         int32_t kb, float *kbar, uint16_t *kbar_hi,

@@ -171,6 +171,31 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k,
                        float scale, void *out, int32_t *idx_out, void *ws,
                        size_t ws_bytes, void *stream);
 
+/*
+ * bsa_forward without a workspace argument, for callers that must not
+ * allocate device memory at call time (e.g. a plugin inside an application
+ * whose memory manager owns the device, or a latency-bound loop that cannot
+ * afford cudaMalloc).  The pages have no counterpart: this is a packaging
+ * variant of bsa_forward, same kernels, same results.
+ *   - Scratch is a static device array of 32 MiB inside the library; every
+ *     device that loads the library holds it until the process exits.  A
+ *     problem whose bsa_forward_workspace_size() exceeds 32 MiB is rejected
+ *     with BSA_ERR_WORKSPACE (for example n = 32768, 8 heads, top-16 needs
+ *     about 19 MiB and fits).
+ *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
+ *     call.  The first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - Every call on a device shares the one array: calls whose work can
+ *     overlap on the GPU (different streams, or different host threads)
+ *     race on it and must be serialised by the caller.
+ * Other arguments and errors as bsa_forward.
+ */
+bsa_status bsa_forward_noalloc(bsa_shape shape, const void *q, const void *k,
+                               const void *v, int32_t key_block, int32_t topk,
+                               float scale, void *out, int32_t *idx_out,
+                               void *stream);
+
 /* Number of kernel launches one bsa_forward call enqueues for this problem
  * (for launch accounting by callers); negative bsa_status on bad arguments. */
 int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk);
