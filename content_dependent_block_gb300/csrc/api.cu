@@ -122,6 +122,94 @@ cudaError_t run_coarse(const bsa_shape &s, const void *q, const float *kbar, con
     return bsa::launch_coarse_topk_simt(q, kbar, s.bh, s.n, s.d, nb, topk, idx, st);
 }
 
+// Workspace of the block-major fine stage over per-query lists [bh][n][k].
+struct BmLayout {
+    size_t zero = 0, zero_bytes = 0;     // counts, cursors, per-query counters
+    size_t counts = 0, cursors = 0, qcount = 0;
+    size_t offsets = 0, n_items = 0, items = 0, entries = 0, part_o = 0, part_lse = 0;
+    size_t total = 0;
+};
+
+BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
+    BmLayout L;
+    const int64_t nb = ceil_div(s.n, kb);
+    const size_t nbh = size_t(s.bh) * nb;
+    const size_t pairs = size_t(s.bh) * s.n * k;
+    size_t off = base;
+    L.zero = off;
+    L.counts = off;
+    off += nbh * sizeof(int32_t);
+    L.cursors = off;
+    off += nbh * sizeof(int32_t);
+    L.qcount = off;
+    off += size_t(s.bh) * s.n * sizeof(int32_t);
+    L.zero_bytes = off - L.zero;
+    off = round_up(off, 256);
+    L.offsets = off;
+    off = round_up(off + (nbh + 1) * sizeof(int32_t), 256);
+    L.n_items = off;
+    off += 256;
+    L.items = off;
+    off = round_up(off + bsa::invert_items_capacity(s.bh, s.n, nb, k, bsa::kFineBmItemPairs) *
+                             sizeof(int2), 256);
+    L.entries = off;
+    off = round_up(off + pairs * sizeof(int32_t), 256);
+    L.part_o = off;
+    off = round_up(off + pairs * s.d * sizeof(uint16_t), 256);
+    L.part_lse = off;
+    off = round_up(off + pairs * sizeof(float), 256);
+    L.total = off;
+    return L;
+}
+
+bool bm_path(const bsa_shape &s, int32_t kb, int64_t nb) {
+    return s.dtype == BSA_BF16 && bsa::fine_bm_supported(s.d, kb) && nb <= 16384 &&
+           s.bh * s.n * int64_t(32) < (int64_t(1) << 31);
+}
+
+// Invert the lists and run the block-major fine stage; ws points at L.
+cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const void *v,
+                        const int32_t *list, int32_t kb, int32_t topk, bool full_lists,
+                        float scale_log2, void *out, char *ws, const BmLayout &L,
+                        int32_t *status, cudaStream_t st) {
+    const int64_t nb = ceil_div(s.n, kb);
+    cudaError_t e = cudaMemsetAsync(ws + L.zero, 0, L.zero_bytes, st);
+    if (e != cudaSuccess) return e;
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    int32_t *cursors = reinterpret_cast<int32_t *>(ws + L.cursors);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    int32_t *n_items = reinterpret_cast<int32_t *>(ws + L.n_items);
+    int2 *items = reinterpret_cast<int2 *>(ws + L.items);
+    int32_t *entries = reinterpret_cast<int32_t *>(ws + L.entries);
+    e = bsa::launch_invert(list, s.bh, s.n, nb, topk, bsa::kFineBmItemPairs, counts, cursors,
+                           offsets, items, n_items, entries, static_cast<uint16_t *>(out), s.d,
+                           status, st);
+    if (e != cudaSuccess) return e;
+    bsa::FineBmArgs a{};
+    a.k_ptr = k;
+    a.v_ptr = v;
+    a.q = static_cast<const uint16_t *>(q);
+    a.list = list;
+    a.entries = entries;
+    a.offsets = offsets;
+    a.items = items;
+    a.n_items = n_items;
+    a.bh = s.bh;
+    a.n = s.n;
+    a.nb = nb;
+    a.d = s.d;
+    a.k = topk;
+    a.full_lists = full_lists ? 1 : 0;
+    a.item_pairs = bsa::kFineBmItemPairs;
+    a.scale_log2 = scale_log2;
+    a.part_o = reinterpret_cast<uint16_t *>(ws + L.part_o);
+    a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    a.qcount = reinterpret_cast<int32_t *>(ws + L.qcount);
+    a.out = static_cast<uint16_t *>(out);
+    a.status = status;
+    return bsa::launch_fine_bm(a, st);
+}
+
 float softmax_scale_log2(float scale, int32_t d) {
     const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(float(d));
     return sc * 1.4426950408889634f;   // log2(e)
@@ -214,7 +302,23 @@ bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, in
                     "coarse top-k launch");
 }
 
-size_t bsa_fine_attention_workspace_size(bsa_shape, bsa_list_desc, bsa_mask) { return 0; }
+// Per-query lists (q_group = 1, one list per head) of bf16 inputs with
+// 64-token blocks take the block-major tensor-core schedule; everything else
+// (static tile lists, fp32, other block sizes) the query-major kernel.
+bool fine_uses_bm(const bsa_shape &shape, const int32_t *list, const bsa_list_desc &ld,
+                  const bsa_mask &mask) {
+    return list != nullptr && ld.q_group == 1 && ld.per_head && mask.kind == BSA_MASK_NONE &&
+           ld.max_blocks <= 32 && bm_path(shape, ld.key_block, ceil_div(shape.n, ld.key_block));
+}
+
+size_t bsa_fine_attention_workspace_size(bsa_shape shape, bsa_list_desc ld, bsa_mask mask) {
+    if (check_shape(shape) != BSA_OK || check_key_block(ld.key_block) != BSA_OK) return 0;
+    // a non-null list is assumed; the query-major path needs no workspace
+    if (!(ld.q_group == 1 && ld.per_head && mask.kind == BSA_MASK_NONE && ld.max_blocks >= 1 &&
+          ld.max_blocks <= 32 && bm_path(shape, ld.key_block, ceil_div(shape.n, ld.key_block))))
+        return 0;
+    return bm_layout(shape, ld.key_block, ld.max_blocks, 0).total;
+}
 
 bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, const void *v,
                               const int32_t *list, bsa_list_desc ld, bsa_mask mask, float scale,
@@ -234,7 +338,19 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
         return fail(BSA_ERR_INVALID_ARG, "bad mask kind %d", mask.kind);
     if (mask.kind == BSA_MASK_SLIDING && mask.sliding < 1)
         return fail(BSA_ERR_INVALID_ARG, "sliding window needs W >= 1");
-    BSA_TRY(check_ws(ws, ws_bytes, bsa_fine_attention_workspace_size(shape, ld, mask)));
+    const bool bm = fine_uses_bm(shape, list, ld, mask);
+    const size_t need = bm ? bsa_fine_attention_workspace_size(shape, ld, mask) : 0;
+    BSA_TRY(check_ws(ws, ws_bytes, need));
+    int32_t *status = device_status_ptr();
+    if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const float sl2 = softmax_scale_log2(scale, shape.d);
+    if (bm) {
+        const BmLayout L = bm_layout(shape, ld.key_block, ld.max_blocks, 0);
+        return launched(run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false, sl2,
+                                    out, static_cast<char *>(ws), L, status, st),
+                        "fine attention (block-major) launch");
+    }
     bsa::FineArgs a{};
     a.q = q;
     a.k = k;
@@ -254,22 +370,26 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
     a.window = mask.window;
     a.stride = mask.stride;
     a.sliding = mask.sliding;
-    a.scale_log2 = softmax_scale_log2(scale, shape.d);
-    a.status = device_status_ptr();
-    if (a.status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
-    return launched(bsa::launch_fine_query_major(a, shape.dtype, static_cast<cudaStream_t>(stream)),
-                    "fine attention launch");
+    a.scale_log2 = sl2;
+    a.status = status;
+    return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }
 
 size_t bsa_forward_workspace_size(bsa_shape shape, int32_t key_block, int32_t topk) {
-    if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1) return 0;
-    return forward_layout(shape, key_block, topk).total;
+    if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1 ||
+        topk > 32)
+        return 0;
+    const ForwardLayout F = forward_layout(shape, key_block, topk);
+    if (!bm_path(shape, key_block, ceil_div(shape.n, key_block))) return F.total;
+    return bm_layout(shape, key_block, topk, F.total).total;
 }
 
 int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk) {
     if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1 || topk > 32)
         return -int32_t(BSA_ERR_INVALID_ARG);
-    return 3;   // pool (+ hi/lo), score + top-k, fine attention
+    // pool (+ hi/lo), score + top-k, then either the query-major fine kernel
+    // or count + scan + scatter + block-major fine
+    return bm_path(shape, key_block, ceil_div(shape.n, key_block)) ? 6 : 3;
 }
 
 bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void *v,
@@ -285,7 +405,7 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     BSA_TRY(check_ptr(out, "out"));
     if (idx_out != nullptr) BSA_TRY(check_ptr(idx_out, "idx_out"));
     const ForwardLayout L = forward_layout(shape, key_block, topk);
-    BSA_TRY(check_ws(ws, ws_bytes, L.total));
+    BSA_TRY(check_ws(ws, ws_bytes, bsa_forward_workspace_size(shape, key_block, topk)));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(ws);
     float *kbar = reinterpret_cast<float *>(base + L.kbar);
@@ -300,6 +420,13 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
                                       st), "pool launch"));
     BSA_TRY(launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, idx, status, st),
                      "coarse top-k launch"));
+    const float sl2 = softmax_scale_log2(scale, shape.d);
+    if (bm_path(shape, key_block, nb)) {
+        const BmLayout B = bm_layout(shape, key_block, topk, L.total);
+        return launched(run_fine_bm(shape, q, k, v, idx, key_block, topk, true, sl2, out, base, B,
+                                    status, st),
+                        "fine attention (block-major) launch");
+    }
     bsa::FineArgs a{};
     a.q = q;
     a.k = k;
@@ -316,7 +443,7 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     a.per_head = 1;
     a.list_rows = shape.n;
     a.mask_kind = BSA_MASK_NONE;
-    a.scale_log2 = softmax_scale_log2(scale, shape.d);
+    a.scale_log2 = sl2;
     a.status = status;
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }

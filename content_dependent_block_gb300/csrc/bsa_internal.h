@@ -54,6 +54,38 @@ cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const 
                                   int64_t bh, int64_t n, int32_t d, int64_t nb, int32_t topk,
                                   int32_t *idx, int32_t *status, cudaStream_t st);
 
+// Per-query list -> per-block pair lists (count, scan, scatter launches).
+size_t invert_items_capacity(int64_t bh, int64_t n, int64_t nb, int32_t k, int32_t item_pairs);
+cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
+                          int32_t item_pairs, int32_t *counts, int32_t *cursors,
+                          int32_t *offsets, int2 *items, int32_t *n_items, int32_t *entries,
+                          uint16_t *out_bf16, int32_t d, int32_t *status, cudaStream_t st);
+
+// Block-major tensor-core fine stage over inverted lists (bf16, B = 64).
+struct FineBmArgs {
+    const void *k_ptr;
+    const void *v_ptr;
+    const uint16_t *q;
+    const int32_t *list;       // [bh][n][k] per-query lists
+    const int32_t *entries;
+    const int32_t *offsets;
+    const int2 *items;
+    const int32_t *n_items;
+    int64_t bh, n, nb;
+    int32_t d, k;
+    int32_t full_lists;        // every row holds min(k, nb) valid ids
+    int32_t item_pairs;
+    float scale_log2;
+    uint16_t *part_o;          // [bh*n*k][d] bf16
+    float *part_lse;           // [bh*n*k]
+    int32_t *qcount;           // [bh*n], zeroed
+    uint16_t *out;
+    int32_t *status;
+};
+constexpr int32_t kFineBmItemPairs = 512;
+bool fine_bm_supported(int32_t d, int32_t key_block);
+cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st);
+
 cudaError_t launch_fine_query_major(const FineArgs &a, int32_t dtype,
                                     cudaStream_t st);
 

@@ -158,6 +158,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "r"(taddr));
 }
 
+// Asynchronous 16-byte global -> shared copy (L2 only), generic proxy.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -172,6 +181,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo
     d |= uint64_t((sbo & 0x3FFFFu) >> 4) << 32;       // stride byte offset
     d |= uint64_t(1) << 46;                           // descriptor version (sm_100 family)
     d |= uint64_t(2) << 61;                           // 128-byte swizzle
+    return d;
+}
+
+// Same, for an operand stored MN-major (N contiguous, e.g. V[keys][d] used
+// as B of P.V): atoms of 64 elements along N by 8 rows along K; `lbo` =
+// byte distance between atoms along N, `sbo` = between 8-row groups along K.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t lbo,
+                                                       uint32_t sbo) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr & 0x3FFFFu) >> 4);
+    d |= uint64_t((lbo & 0x3FFFFu) >> 4) << 16;
+    d |= uint64_t((sbo & 0x3FFFFu) >> 4) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(2) << 61;
     return d;
 }
 

@@ -180,8 +180,8 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k,
  *   - Scratch is a static device array of 32 MiB inside the library; every
  *     device that loads the library holds it until the process exits.  A
  *     problem whose bsa_forward_workspace_size() exceeds 32 MiB is rejected
- *     with BSA_ERR_WORKSPACE (for example n = 32768, 8 heads, top-16 needs
- *     about 19 MiB and fits).
+ *     with BSA_ERR_WORKSPACE (2 heads x 1024 tokens, top-4 needs about
+ *     1.2 MiB and fits; the workspace grows with heads * n * k * d).
  *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
  *     call.  The first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current; make that

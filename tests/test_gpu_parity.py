@@ -153,6 +153,7 @@ def _small(bh, n, d, seed, dtype="bf16", sigma=0.0, kb=64):
     (1, 1, 64, 16, 1),         # a single token
     (3, 256, 64, 64, 8),       # k*B >= n: dense attention
     (1, 4100, 64, 16, 32),     # many blocks, k = 32
+    (2, 700, 128, 64, 6),      # d=128 on the tensor-core fine stage, ragged
 ])
 def test_forward_edge_shapes(bh, n, d, kb, topk):
     t, (q, k, v) = _small(bh, n, d, seed=n + d, sigma=0.5, kb=kb)

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _inputs(seed):
-    w = workloads.WORKLOADS["dyn_n8192"]
+    w = workloads.WORKLOADS["dyn_n1024"]
     t = workloads.generate(w, seed=seed)
     return w, tuple(parity.to_device(getattr(t, x), "bf16") for x in "qkv")
 
@@ -57,5 +57,5 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch():
                                None)
     assert rc == 4                                      # BSA_ERR_WORKSPACE
     assert b"static scratch" in L.bsa_last_error()
-    # the 32k-token, 8-head, top-16 problem fits
-    assert L.bsa_forward_workspace_size(bsa.Shape(8, 32768, 64, bsa.BF16), 64, 16) <= (32 << 20)
+    # the 2-head, 1024-token, top-4 problem fits
+    assert L.bsa_forward_workspace_size(bsa.Shape(2, 1024, 64, bsa.BF16), 64, 4) <= (32 << 20)
