@@ -389,11 +389,11 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": config_of(w),
-        "roofline": {"kernel": "fine attention (bsa_fine_attention over the top-k list)",
+        "roofline": {"kernel": "fine attention stage (bsa_fine_attention over the top-k list)",
                      "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "peak_source": f"bf16_tflops burst, {peaks['source']}",
-                     "traffic": kernel_traffic("fine_attention"),
+                     "traffic": kernel_traffic("fine_bm" if fwd.launches == 6 else "fine_query_major"),
                      "algorithmic_flops_per_launch": fine_flops,
                      "launch_ms": fine_ms},
         "e2e": {"value": flops * world / (e2e_total / args.steps * 1e-3) / 1e12,

@@ -60,53 +60,65 @@ __device__ __forceinline__ int list_valid(const int32_t *row, int32_t k, int64_t
     return c;
 }
 
-// Merge the k partial states of query row `qrow` (flat h*n + i) into O.
+// Merge the partial states of query row `qrow` (flat h*n + i) into O with
+// the whole warp: lane s reads slot s's lse, lane l owns D/32 channels, and
+// every partial value of the row is requested before any is used.
 template <int D>
-__device__ void merge_query(int64_t qrow, const int32_t *list, int32_t k, int64_t nb,
-                            const uint16_t *part_o, const float *part_lse, uint16_t *out) {
-    const int32_t *lr = list + qrow * k;
-    float M = -INFINITY;
-    for (int s = 0; s < k; ++s) {
-        const int32_t b = __ldg(lr + s);
-        if (b >= 0 && b < nb) M = fmaxf(M, __ldcg(part_lse + qrow * k + s));
-    }
-    float L = 0.f;
-    for (int s = 0; s < k; ++s) {
-        const int32_t b = __ldg(lr + s);
-        if (b >= 0 && b < nb) L += exp2f(__ldcg(part_lse + qrow * k + s) - M);
-    }
-    const float invL = 1.f / L;
-#pragma unroll 1
-    for (int c0 = 0; c0 < D; c0 += 32) {
-        float acc[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-        for (int s = 0; s < k; ++s) {
-            const int32_t b = __ldg(lr + s);
-            if (b < 0 || b >= nb) continue;
-            const float w = exp2f(__ldcg(part_lse + qrow * k + s) - M) * invL;
-            const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (qrow * k + s) * D + c0);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const uint4 x = __ldcg(src + v);
-                acc[8 * v + 0] = fmaf(w, bf16_low_half(x.x), acc[8 * v + 0]);
-                acc[8 * v + 1] = fmaf(w, bf16_high_half(x.x), acc[8 * v + 1]);
-                acc[8 * v + 2] = fmaf(w, bf16_low_half(x.y), acc[8 * v + 2]);
-                acc[8 * v + 3] = fmaf(w, bf16_high_half(x.y), acc[8 * v + 3]);
-                acc[8 * v + 4] = fmaf(w, bf16_low_half(x.z), acc[8 * v + 4]);
-                acc[8 * v + 5] = fmaf(w, bf16_high_half(x.z), acc[8 * v + 5]);
-                acc[8 * v + 6] = fmaf(w, bf16_low_half(x.w), acc[8 * v + 6]);
-                acc[8 * v + 7] = fmaf(w, bf16_high_half(x.w), acc[8 * v + 7]);
-            }
+__device__ __forceinline__ void merge_query_warp(int64_t qrow, const int32_t *list, int32_t k,
+                                                 int64_t nb, int32_t full_valid, int lane,
+                                                 const uint16_t *part_o, const float *part_lse,
+                                                 uint16_t *out) {
+    constexpr int E = D / 32;     // channels per lane: 2 or 4
+    bool valid = false;
+    if (lane < k) {
+        if (full_valid > 0) {
+            valid = lane < full_valid;
+        } else {
+            const int32_t b = __ldg(list + qrow * k + lane);
+            valid = b >= 0 && b < nb;
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(out + qrow * D + c0);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-            dst[v] = make_uint4(pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]),
-                                pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]),
-                                pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]),
-                                pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]));
     }
+    const float lse = valid ? __ldcg(part_lse + qrow * k + lane) : -INFINITY;
+    uint32_t raw[32][E / 2];
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+        const bool vs = __shfl_sync(0xffffffffu, valid, s);
+        const uint16_t *src = part_o + (qrow * k + s) * D + lane * E;
+        if (E == 2) raw[s][0] = vs ? __ldcg(reinterpret_cast<const unsigned int *>(src)) : 0u;
+        else {
+            const uint2 x = vs ? __ldcg(reinterpret_cast<const uint2 *>(src)) : make_uint2(0u, 0u);
+            raw[s][0] = x.x;
+            raw[s][E / 2 - 1] = x.y;
+        }
+    }
+    const float M = warp_max(lse);
+    const float w = valid ? exp2f(lse - M) : 0.f;
+    const float invL = 1.f / warp_sum(w);
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, w, s);
+#pragma unroll
+        for (int e2 = 0; e2 < E / 2; ++e2) {
+            acc[2 * e2] = fmaf(ws, bf16_low_half(raw[s][e2]), acc[2 * e2]);
+            acc[2 * e2 + 1] = fmaf(ws, bf16_high_half(raw[s][e2]), acc[2 * e2 + 1]);
+        }
+    }
+    uint16_t *dst = out + qrow * D + lane * E;
+    if (E == 2) {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * invL, acc[1] * invL);
+    } else {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * invL, acc[1] * invL),
+                                                     pack_bf16x2(acc[E - 2] * invL, acc[E - 1] * invL));
+    }
+}
+
+__device__ __forceinline__ int atomic_add_acq_rel(int32_t *p, int32_t v) {
+    int32_t old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 template <int D>
@@ -280,15 +292,22 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
                                 pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l));
                     }
                 }
+                bool last = false;
                 if (has) {
                     part_lse[pid] = m2 + __log2f(l);
-                    __threadfence();
-                    const int done = atomicAdd(qcount + qrow, 1) + 1;
+                    // release: this pair's partial is visible before the count;
+                    // acquire: the last writer sees every other slot's partial
+                    const int done = atomic_add_acq_rel(qcount + qrow, 1) + 1;
                     const int need = full_lists ? kvalid_all : list_valid(list + qrow * k, k, nb);
-                    if (done == need) {
-                        __threadfence();
-                        merge_query<D>(qrow, list, k, nb, part_o, part_lse, out);
-                    }
+                    last = done == need;
+                }
+                unsigned todo = __ballot_sync(0xffffffffu, last);
+                while (todo != 0u) {
+                    const int src_lane = __ffs(todo) - 1;
+                    todo &= todo - 1u;
+                    const int64_t r = __shfl_sync(0xffffffffu, qrow, src_lane);
+                    merge_query_warp<D>(r, list, k, nb, full_lists ? kvalid_all : 0, t & 31, part_o,
+                                        part_lse, out);
                 }
             }
             tc::tc_fence_before();
@@ -337,14 +356,19 @@ cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorM
     auto kern = fine_bm_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
     if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+        return e;
+    int dev = 0, sms = 0, smem_sm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, S::kTotal)) != cudaSuccess)
+    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
         return e;
-    per_sm = per_sm < 1 ? 1 : per_sm;
+    // resident CTAs per SM: shared memory (+1 KB reserved per CTA) and TMEM
+    int per_sm = smem_sm / (S::kTotal + 1024);
     const int tmem_limit = int(512 / S::kTmemCols);
     if (per_sm > tmem_limit) per_sm = tmem_limit;
+    if (per_sm < 1) per_sm = 1;
     const int grid = sms * per_sm;
     kern<<<grid, kThreads, S::kTotal, st>>>(mk, mv, a.q, a.list, a.entries, a.offsets, a.items,
                                             a.n_items, a.n, a.nb, a.k, a.full_lists, a.item_pairs,
