@@ -133,7 +133,7 @@ struct BmLayout {
 BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     BmLayout L;
     const int64_t nb = ceil_div(s.n, kb);
-    const size_t nbh = size_t(s.bh) * nb;
+    const size_t nbh = size_t(bsa::invert_bins(s.bh, s.n, nb, k));
     const size_t pairs = size_t(s.bh) * s.n * k;
     size_t off = base;
     L.zero = off;
@@ -197,6 +197,7 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     a.bh = s.bh;
     a.n = s.n;
     a.nb = nb;
+    a.bins_per_head = bsa::invert_bins(1, s.n, nb, topk);
     a.d = s.d;
     a.k = topk;
     a.full_lists = full_lists ? 1 : 0;

@@ -55,6 +55,8 @@ cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const 
                                   int32_t *idx, int32_t *status, cudaStream_t st);
 
 // Per-query list -> per-block pair lists (count, scan, scatter launches).
+int64_t invert_query_range(int64_t n, int64_t nb, int32_t k);
+int64_t invert_bins(int64_t bh, int64_t n, int64_t nb, int32_t k);
 size_t invert_items_capacity(int64_t bh, int64_t n, int64_t nb, int32_t k, int32_t item_pairs);
 cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
                           int32_t item_pairs, int32_t *counts, int32_t *cursors,
@@ -72,6 +74,7 @@ struct FineBmArgs {
     const int2 *items;
     const int32_t *n_items;
     int64_t bh, n, nb;
+    int64_t bins_per_head;     // query ranges per head * nb
     int32_t d, k;
     int32_t full_lists;        // every row holds min(k, nb) valid ids
     int32_t item_pairs;

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
     const uint16_t *__restrict__ q, const int32_t *__restrict__ list,
     const int32_t *__restrict__ entries, const int32_t *__restrict__ offsets,
     const int2 *__restrict__ items, const int32_t *__restrict__ n_items, int64_t n, int64_t nb,
-    int32_t k, int32_t full_lists, int32_t item_pairs, float scale_log2,
+    int64_t bins_per_head, int32_t k, int32_t full_lists, int32_t item_pairs, float scale_log2,
     uint16_t *__restrict__ part_o, float *__restrict__ part_lse, int32_t *__restrict__ qcount,
     uint16_t *__restrict__ out, int32_t *status) {
     using S = BmSmem<D>;
@@ -176,9 +176,9 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
     const int total = *n_items;
     for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
         const int2 item = items[it];
-        const int64_t hb = item.x;
-        const int64_t h = hb / nb;
-        const int64_t b = hb - h * nb;
+        const int64_t hb = item.x;                // bin = (head, query range, block)
+        const int64_t h = hb / bins_per_head;
+        const int64_t b = hb % nb;
         const int32_t cnt = offsets[hb + 1] - offsets[hb];
         const int32_t end = min(cnt, item.y + item_pairs);
         const int32_t *ent = entries + offsets[hb];
@@ -371,7 +371,8 @@ cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorM
     if (per_sm < 1) per_sm = 1;
     const int grid = sms * per_sm;
     kern<<<grid, kThreads, S::kTotal, st>>>(mk, mv, a.q, a.list, a.entries, a.offsets, a.items,
-                                            a.n_items, a.n, a.nb, a.k, a.full_lists, a.item_pairs,
+                                            a.n_items, a.n, a.nb, a.bins_per_head, a.k,
+                                            a.full_lists, a.item_pairs,
                                             a.scale_log2, a.part_o, a.part_lse, a.qcount, a.out,
                                             a.status);
     return cudaGetLastError();

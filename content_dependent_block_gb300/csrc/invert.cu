@@ -5,7 +5,12 @@
 // chose it ("Block-Sparse & Linear Attention Kernels", section 4: gather
 // through precomputed block indices; dynamic scheduling for balance).
 //
-//   count    per (head, block): how many (query, slot) pairs selected it;
+// Bins are (head, query range, block): the queries of a head are cut into
+// ranges of R queries (R a power of two >= 1024, about two 128-pair tiles
+// per bin on average), so that the fine stage finishes one range's partial
+// states -- and merges them -- while they are still resident in L2.
+//
+//   count    per bin: how many (query, slot) pairs selected the block;
 //            CTA-local shared-memory histograms, one global atomic per
 //            touched bin and CTA
 //   scan     exclusive prefix over (head, block) -> CSR offsets, plus the
@@ -31,6 +36,7 @@ __device__ __forceinline__ bool valid_block(int32_t b, int64_t nb) { return b >=
 // grid: (ceil(n / kQueriesPerCta), bh); dynamic smem: nb ints
 __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restrict__ list,
                                                          int64_t n, int64_t nb, int32_t k,
+                                                         int64_t range, int64_t nranges,
                                                          int32_t *__restrict__ counts,
                                                          int32_t *status) {
     extern __shared__ int32_t hist[];
@@ -48,11 +54,13 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restri
     }
     if (bad) report_status(status, kStatusBadIndex);
     __syncthreads();
+    const int64_t bin0 = (h * nranges + i0 / range) * nb;
     for (int64_t b = threadIdx.x; b < nb; b += kThreads)
-        if (hist[b] != 0) atomicAdd(counts + h * nb + b, hist[b]);
+        if (hist[b] != 0) atomicAdd(counts + bin0 + b, hist[b]);
 }
 
-// One CTA of 1024 threads.  offsets[nbh + 1], items[...] = {hb, first pair}
+// One CTA of 1024 threads over the nbh bins (head, query range, block):
+// offsets[nbh + 1], items[...] = {bin, first pair}
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t *__restrict__ counts,
                                                     int64_t nbh, int32_t item_pairs,
                                                     int32_t *__restrict__ offsets,
@@ -119,8 +127,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t *__restrict__ 
 // grid: (ceil(n / kQueriesPerCta), bh); dynamic smem: 2 * nb ints
 template <typename OutT>
 __global__ void __launch_bounds__(kThreads) scatter_kernel(
-    const int32_t *__restrict__ list, int64_t n, int64_t nb, int32_t k,
-    const int32_t *__restrict__ offsets, int32_t *__restrict__ cursors,
+    const int32_t *__restrict__ list, int64_t n, int64_t nb, int32_t k, int64_t range,
+    int64_t nranges, const int32_t *__restrict__ offsets, int32_t *__restrict__ cursors,
     int32_t *__restrict__ entries, OutT *__restrict__ out, int32_t d) {
     extern __shared__ int32_t sm[];
     int32_t *hist = sm;          // pairs of this CTA per block
@@ -136,9 +144,10 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
         if (valid_block(b, nb)) atomicAdd(&hist[b], 1);
     }
     __syncthreads();
+    const int64_t bin0 = (h * nranges + i0 / range) * nb;
     for (int64_t b = threadIdx.x; b < nb; b += kThreads) {
         const int32_t c = hist[b];
-        base[b] = c ? offsets[h * nb + b] + atomicAdd(cursors + h * nb + b, c) : 0;
+        base[b] = c ? offsets[bin0 + b] + atomicAdd(cursors + bin0 + b, c) : 0;
         hist[b] = 0;
     }
     __syncthreads();
@@ -162,8 +171,20 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
 
 }  // namespace
 
+int64_t invert_query_range(int64_t n, int64_t nb, int32_t k) {
+    // about two full 128-pair tiles per (range, block) on average
+    int64_t r = kQueriesPerCta;
+    while (r * k < int64_t(256) * nb && r < n) r *= 2;
+    return r;
+}
+
+int64_t invert_bins(int64_t bh, int64_t n, int64_t nb, int32_t k) {
+    const int64_t r = invert_query_range(n, nb, k);
+    return bh * ((n + r - 1) / r) * nb;
+}
+
 size_t invert_items_capacity(int64_t bh, int64_t n, int64_t nb, int32_t k, int32_t item_pairs) {
-    return size_t(bh * nb) + size_t((bh * n * k + item_pairs - 1) / item_pairs);
+    return size_t(invert_bins(bh, n, nb, k)) + size_t((bh * n * k + item_pairs - 1) / item_pairs);
 }
 
 cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
@@ -184,10 +205,12 @@ cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * smem1));
         if (e != cudaSuccess) return e;
     }
-    count_kernel<<<grid, kThreads, smem1, st>>>(list, n, nb, k, counts, status);
-    scan_kernel<<<1, 1024, 0, st>>>(counts, bh * nb, item_pairs, offsets, items, n_items);
-    scatter_kernel<uint16_t><<<grid, kThreads, 2 * smem1, st>>>(list, n, nb, k, offsets, cursors,
-                                                                entries, out_bf16, d);
+    const int64_t range = invert_query_range(n, nb, k);
+    const int64_t nranges = (n + range - 1) / range;
+    count_kernel<<<grid, kThreads, smem1, st>>>(list, n, nb, k, range, nranges, counts, status);
+    scan_kernel<<<1, 1024, 0, st>>>(counts, bh * nranges * nb, item_pairs, offsets, items, n_items);
+    scatter_kernel<uint16_t><<<grid, kThreads, 2 * smem1, st>>>(list, n, nb, k, range, nranges,
+                                                                offsets, cursors, entries, out_bf16, d);
     return cudaGetLastError();
 }
 
