@@ -124,41 +124,48 @@ cudaError_t run_coarse(const bsa_shape &s, const void *q, const float *kbar, con
 
 // Workspace of the block-major fine stage over per-query lists [bh][n][k].
 struct BmLayout {
-    size_t zero = 0, zero_bytes = 0;     // counts, cursors, per-query counters
-    size_t counts = 0, cursors = 0, qcount = 0;
-    size_t offsets = 0, n_items = 0, items = 0, entries = 0, part_o = 0, part_lse = 0;
+    bsa::InvertPlan plan;
+    size_t zero = 0, zero_bytes = 0;     // counts, cursors, queue head, range counters
+    size_t counts = 0, cursors = 0, queue_head = 0, range_done = 0, merge_done = 0;
+    size_t offsets = 0, fitem_off = 0, fpre = 0, mpre = 0, range_total = 0, range_merges = 0;
+    size_t n_items = 0, items = 0, entries = 0, part_o = 0, part_lse = 0;
     size_t total = 0;
 };
 
 BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     BmLayout L;
     const int64_t nb = ceil_div(s.n, kb);
-    const size_t nbh = size_t(bsa::invert_bins(s.bh, s.n, nb, k));
-    const size_t pairs = size_t(s.bh) * s.n * k;
+    L.plan = bsa::invert_plan(s.bh, s.n, nb, k);
+    const size_t nbins = size_t(L.plan.nbins), nr = size_t(L.plan.nr);
+    const size_t ring_slots = size_t(bsa::kPartialRing) * size_t(L.plan.range) * size_t(k);
     size_t off = base;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, 16);
+        return at;
+    };
     L.zero = off;
-    L.counts = off;
-    off += nbh * sizeof(int32_t);
-    L.cursors = off;
-    off += nbh * sizeof(int32_t);
-    L.qcount = off;
-    off += size_t(s.bh) * s.n * sizeof(int32_t);
+    L.counts = take(nbins * 4);
+    L.cursors = take(nbins * 4);
+    L.queue_head = take(4);
+    L.range_done = take(nr * 4);
+    L.merge_done = take(nr * 4);
     L.zero_bytes = off - L.zero;
     off = round_up(off, 256);
-    L.offsets = off;
-    off = round_up(off + (nbh + 1) * sizeof(int32_t), 256);
-    L.n_items = off;
-    off += 256;
-    L.items = off;
-    off = round_up(off + bsa::invert_items_capacity(s.bh, s.n, nb, k, bsa::kFineBmItemPairs) *
-                             sizeof(int2), 256);
-    L.entries = off;
-    off = round_up(off + pairs * sizeof(int32_t), 256);
-    L.part_o = off;
-    off = round_up(off + pairs * s.d * sizeof(uint16_t), 256);
-    L.part_lse = off;
-    off = round_up(off + pairs * sizeof(float), 256);
-    L.total = off;
+    L.offsets = take((nbins + 1) * 4);
+    L.fitem_off = take((nbins + 1) * 4);
+    L.fpre = take((nr + 2) * 4);
+    L.mpre = take((nr + 1) * 4);
+    L.range_total = take(nr * 4);
+    L.range_merges = take(nr * 4);
+    L.n_items = take(4);
+    L.items = take(size_t(L.plan.items_cap) * sizeof(int2));
+    L.entries = take(size_t(s.bh) * s.n * k * 4);
+    off = round_up(off, 256);
+    L.part_o = take(ring_slots * s.d * 2);
+    off = round_up(off, 256);
+    L.part_lse = take(ring_slots * 4);
+    L.total = round_up(off, 256);
     return L;
 }
 
@@ -175,14 +182,19 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     const int64_t nb = ceil_div(s.n, kb);
     cudaError_t e = cudaMemsetAsync(ws + L.zero, 0, L.zero_bytes, st);
     if (e != cudaSuccess) return e;
-    int32_t *counts = reinterpret_cast<int32_t *>(ws + L.counts);
-    int32_t *cursors = reinterpret_cast<int32_t *>(ws + L.cursors);
-    int32_t *offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
-    int32_t *n_items = reinterpret_cast<int32_t *>(ws + L.n_items);
-    int2 *items = reinterpret_cast<int2 *>(ws + L.items);
-    int32_t *entries = reinterpret_cast<int32_t *>(ws + L.entries);
-    e = bsa::launch_invert(list, s.bh, s.n, nb, topk, bsa::kFineBmItemPairs, counts, cursors,
-                           offsets, items, n_items, entries, static_cast<uint16_t *>(out), s.d,
+    bsa::InvertBuffers w{};
+    w.counts = reinterpret_cast<int32_t *>(ws + L.counts);
+    w.cursors = reinterpret_cast<int32_t *>(ws + L.cursors);
+    w.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    w.fitem_off = reinterpret_cast<int32_t *>(ws + L.fitem_off);
+    w.fpre = reinterpret_cast<int32_t *>(ws + L.fpre);
+    w.mpre = reinterpret_cast<int32_t *>(ws + L.mpre);
+    w.range_total = reinterpret_cast<int32_t *>(ws + L.range_total);
+    w.range_merges = reinterpret_cast<int32_t *>(ws + L.range_merges);
+    w.items = reinterpret_cast<int2 *>(ws + L.items);
+    w.n_items = reinterpret_cast<int32_t *>(ws + L.n_items);
+    w.entries = reinterpret_cast<int32_t *>(ws + L.entries);
+    e = bsa::launch_invert(list, s.bh, s.n, nb, topk, L.plan, w, static_cast<uint16_t *>(out), s.d,
                            status, st);
     if (e != cudaSuccess) return e;
     bsa::FineBmArgs a{};
@@ -190,22 +202,20 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     a.v_ptr = v;
     a.q = static_cast<const uint16_t *>(q);
     a.list = list;
-    a.entries = entries;
-    a.offsets = offsets;
-    a.items = items;
-    a.n_items = n_items;
+    a.w = w;
+    a.p = L.plan;
+    a.queue_head = reinterpret_cast<int32_t *>(ws + L.queue_head);
+    a.range_done = reinterpret_cast<int32_t *>(ws + L.range_done);
+    a.merge_done = reinterpret_cast<int32_t *>(ws + L.merge_done);
     a.bh = s.bh;
     a.n = s.n;
     a.nb = nb;
-    a.bins_per_head = bsa::invert_bins(1, s.n, nb, topk);
     a.d = s.d;
     a.k = topk;
     a.full_lists = full_lists ? 1 : 0;
-    a.item_pairs = bsa::kFineBmItemPairs;
     a.scale_log2 = scale_log2;
     a.part_o = reinterpret_cast<uint16_t *>(ws + L.part_o);
     a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
-    a.qcount = reinterpret_cast<int32_t *>(ws + L.qcount);
     a.out = static_cast<uint16_t *>(out);
     a.status = status;
     return bsa::launch_fine_bm(a, st);

@@ -54,38 +54,55 @@ cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const 
                                   int64_t bh, int64_t n, int32_t d, int64_t nb, int32_t topk,
                                   int32_t *idx, int32_t *status, cudaStream_t st);
 
-// Per-query list -> per-block pair lists (count, scan, scatter launches).
-int64_t invert_query_range(int64_t n, int64_t nb, int32_t k);
-int64_t invert_bins(int64_t bh, int64_t n, int64_t nb, int32_t k);
-size_t invert_items_capacity(int64_t bh, int64_t n, int64_t nb, int32_t k, int32_t item_pairs);
-cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
-                          int32_t item_pairs, int32_t *counts, int32_t *cursors,
-                          int32_t *offsets, int2 *items, int32_t *n_items, int32_t *entries,
-                          uint16_t *out_bf16, int32_t d, int32_t *status, cudaStream_t st);
+// ---- block-major fine stage over per-query lists [bh][n][k] ----------
+constexpr int32_t kFineBmItemPairs = 512;   // pairs per fine work item (<= 4 tiles)
+constexpr int32_t kMergeQueries = 256;      // queries per merge work item
+constexpr int32_t kPartialRing = 3;         // query ranges whose partials coexist
 
-// Block-major tensor-core fine stage over inverted lists (bf16, B = 64).
+// Bins are (head, query range of `range` queries, key block).
+struct InvertPlan {
+    int64_t range = 0, nranges = 0, nr = 0, nbins = 0, items_cap = 0;
+    int32_t item_pairs = 0, qm = 0;
+};
+InvertPlan invert_plan(int64_t bh, int64_t n, int64_t nb, int32_t k);
+
+struct InvertBuffers {
+    int32_t *counts;        // [nbins], zeroed
+    int32_t *cursors;       // [nbins], zeroed
+    int32_t *offsets;       // [nbins + 1]
+    int32_t *fitem_off;     // [nbins + 1]
+    int32_t *fpre;          // [nr + 2]
+    int32_t *mpre;          // [nr + 1]
+    int32_t *range_total;   // [nr] pairs per range
+    int32_t *range_merges;  // [nr] merge items per range
+    int2 *items;            // [items_cap]
+    int32_t *n_items;
+    int32_t *entries;       // [bh * n * k]
+};
+// count + scan + scatter launches
+cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
+                          const InvertPlan &p, const InvertBuffers &w, uint16_t *out_bf16,
+                          int32_t d, int32_t *status, cudaStream_t st);
+
 struct FineBmArgs {
     const void *k_ptr;
     const void *v_ptr;
     const uint16_t *q;
-    const int32_t *list;       // [bh][n][k] per-query lists
-    const int32_t *entries;
-    const int32_t *offsets;
-    const int2 *items;
-    const int32_t *n_items;
+    const int32_t *list;          // [bh][n][k]
+    InvertBuffers w;
+    InvertPlan p;
+    int32_t *queue_head;          // zeroed
+    int32_t *range_done;          // [nr] zeroed: pairs with partials written
+    int32_t *merge_done;          // [nr] zeroed: merge items finished
     int64_t bh, n, nb;
-    int64_t bins_per_head;     // query ranges per head * nb
     int32_t d, k;
-    int32_t full_lists;        // every row holds min(k, nb) valid ids
-    int32_t item_pairs;
+    int32_t full_lists;           // every row holds min(k, nb) valid ids, first
     float scale_log2;
-    uint16_t *part_o;          // [bh*n*k][d] bf16
-    float *part_lse;           // [bh*n*k]
-    int32_t *qcount;           // [bh*n], zeroed
+    uint16_t *part_o;             // [ring][range * k][d] bf16
+    float *part_lse;              // [ring][range * k]
     uint16_t *out;
     int32_t *status;
 };
-constexpr int32_t kFineBmItemPairs = 512;
 bool fine_bm_supported(int32_t d, int32_t key_block);
 cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st);
 

@@ -3,27 +3,27 @@
 // selected tokens; "The Triton kernel": running max m, running sum l and
 // accumulator acc merged block by block).
 //
-// Schedule.  The per-query lists are inverted (invert.cu) so that every
-// (head, key block) knows the (query, slot) pairs that selected it.  A work
-// item is one key block and up to kItemTiles x 128 of its pairs.  Per item
-// the CTA loads K_b and V_b once (TMA, 128-byte swizzle); per tile of 128
-// pairs it
-//   1. gathers the 128 query rows (cp.async, swizzled by hand),
-//   2. S = Q_g . K_b^T            tcgen05 MMA, M = 128, N = B, fp32 in TMEM
-//   3. per row (one thread per TMEM lane): m = max s, p = exp2(s - m),
-//      l = sum p, P -> shared memory as bf16 (the A operand of step 4)
-//   4. O = P . V_b                tcgen05 MMA, M = 128, N = d (V MN-major)
-//   5. writes the pair's partial state: o = O / l (bf16) and
-//      lse = m + log2 l (fp32, base-2 units of the scaled score)
-// and the thread that writes a query's last partial (a per-query counter)
-// merges that query's partials in slot order -- the online-softmax merge
-// of (m, l, acc) across its blocks -- and writes O.  The merge reads every
-// partial in a fixed order, so results do not depend on scheduling.
-//
-// The grid is persistent (SMs x resident CTAs); items are taken round-robin
-// in head-major order so that a head's partials are produced and consumed
-// while they are still in L2.  Four 128-thread CTAs share an SM (d = 64),
-// which overlaps one CTA's gathers with another's MMAs and exponentials.
+// Schedule.  The per-query lists are inverted (invert.cu) into bins
+// (head, query range, key block), each listing the (query, slot) pairs
+// that selected the block.  A persistent grid pulls work items from one
+// queue (an atomic counter) in the order the scan kernel laid out:
+//   fine items   one bin and up to 512 of its pairs.  The CTA loads K_b and
+//                V_b once (TMA, 128-byte swizzle); per tile of 128 pairs it
+//                gathers the query rows (cp.async), S = Q_g . K_b^T
+//                (tcgen05, M = 128, N = 64, fp32 in TMEM), per row
+//                m = max s, p = exp2(s - m), l = sum p, P -> shared memory
+//                (bf16), O = P . V_b (tcgen05, N = d), and stores the pair's
+//                partial state o = O / l (bf16) and lse = m + log2 l.
+//   merge items  256 queries of a range whose fine items are all done: the
+//                k partial states of each query are merged in slot order
+//                (online-softmax merge of (m, l, acc)) into O, and the
+//                merged partial lines are discarded from L2 so they are
+//                never written back to memory.
+// Merge items of range r sit after the fine items of range r + 1, so every
+// wait is on work taken from the queue earlier (no deadlock), and partial
+// states live in a ring of kPartialRing ranges (bounded, L2-sized memory).
+// Results do not depend on scheduling: partial states are per pair and the
+// merge reads them in slot order.
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -51,23 +51,40 @@ struct BmSmem {
     static constexpr uint32_t kTmemCols = (kB + D) <= 128 ? 128 : 256;
 };
 
-__device__ __forceinline__ int list_valid(const int32_t *row, int32_t k, int64_t nb) {
-    int c = 0;
-    for (int s = 0; s < k; ++s) {
-        const int32_t b = __ldg(row + s);
-        c += (b >= 0 && b < nb) ? 1 : 0;
-    }
-    return c;
+__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-// Merge the partial states of query row `qrow` (flat h*n + i) into O with
-// the whole warp: lane s reads slot s's lse, lane l owns D/32 channels, and
-// every partial value of the row is requested before any is used.
+// Bounded wait until *p >= target (acquire).  False on timeout, or when
+// another CTA already reported one.
+__device__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status) {
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = tc::global_ns();
+    for (;;) {
+        __nanosleep(128);
+        if (ld_acquire(p) >= target) return true;
+        if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return false;
+        if (tc::global_ns() - t0 > tc::kWaitLimitNs) {
+            report_status(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// Merge query row `qrow` (flat h*n + i): lane s reads slot s's lse; lane l
+// owns D/32 channels; all of the row's partial values are requested before
+// any is used.  `base` indexes the query's k partial slots in the ring.
 template <int D>
-__device__ __forceinline__ void merge_query_warp(int64_t qrow, const int32_t *list, int32_t k,
-                                                 int64_t nb, int32_t full_valid, int lane,
-                                                 const uint16_t *part_o, const float *part_lse,
-                                                 uint16_t *out) {
+__device__ __forceinline__ void merge_query(int64_t qrow, int64_t base, const int32_t *list,
+                                            int32_t k, int64_t nb, int32_t full_valid, int lane,
+                                            uint16_t *part_o, const float *part_lse,
+                                            uint16_t *out) {
     constexpr int E = D / 32;     // channels per lane: 2 or 4
     bool valid = false;
     if (lane < k) {
@@ -78,14 +95,16 @@ __device__ __forceinline__ void merge_query_warp(int64_t qrow, const int32_t *li
             valid = b >= 0 && b < nb;
         }
     }
-    const float lse = valid ? __ldcg(part_lse + qrow * k + lane) : -INFINITY;
+    if (__ballot_sync(0xffffffffu, valid) == 0u) return;   // nothing listed: O stays 0
+    const float lse = valid ? __ldcg(part_lse + base + lane) : -INFINITY;
     uint32_t raw[32][E / 2];
 #pragma unroll
     for (int s = 0; s < 32; ++s) {
         const bool vs = __shfl_sync(0xffffffffu, valid, s);
-        const uint16_t *src = part_o + (qrow * k + s) * D + lane * E;
-        if (E == 2) raw[s][0] = vs ? __ldcg(reinterpret_cast<const unsigned int *>(src)) : 0u;
-        else {
+        const uint16_t *src = part_o + (base + s) * D + lane * E;
+        if (E == 2) {
+            raw[s][0] = vs ? __ldcg(reinterpret_cast<const unsigned int *>(src)) : 0u;
+        } else {
             const uint2 x = vs ? __ldcg(reinterpret_cast<const uint2 *>(src)) : make_uint2(0u, 0u);
             raw[s][0] = x.x;
             raw[s][E / 2 - 1] = x.y;
@@ -113,23 +132,19 @@ __device__ __forceinline__ void merge_query_warp(int64_t qrow, const int32_t *li
         *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * invL, acc[1] * invL),
                                                      pack_bf16x2(acc[E - 2] * invL, acc[E - 1] * invL));
     }
-}
-
-__device__ __forceinline__ int atomic_add_acq_rel(int32_t *p, int32_t v) {
-    int32_t old;
-    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-    return old;
+    // the merged partial rows are dead: drop them from L2 without write-back
+    __syncwarp();
+    if (valid) {
+#pragma unroll
+        for (int line = 0; line < D * 2 / 128; ++line)
+            discard_l2_line(part_o + (base + lane) * D + line * 64);
+    }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const uint16_t *__restrict__ q, const int32_t *__restrict__ list,
-    const int32_t *__restrict__ entries, const int32_t *__restrict__ offsets,
-    const int2 *__restrict__ items, const int32_t *__restrict__ n_items, int64_t n, int64_t nb,
-    int64_t bins_per_head, int32_t k, int32_t full_lists, int32_t item_pairs, float scale_log2,
-    uint16_t *__restrict__ part_o, float *__restrict__ part_lse, int32_t *__restrict__ qcount,
-    uint16_t *__restrict__ out, int32_t *status) {
+    const FineBmArgs a) {
     using S = BmSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -141,10 +156,13 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
     uint64_t *bar_kv = reinterpret_cast<uint64_t *>(smem + S::kTiles);
     uint64_t *bar_mma = bar_kv + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_kv + 2);
+    int32_t *s_item = reinterpret_cast<int32_t *>(bar_kv + 3);    // [1]
+    int32_t *s_ok = s_item + 1;                                     // [1]
 
     const int t = threadIdx.x;
-    const int warp = t >> 5;
-    if (status != nullptr && *reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
+    const int warp = t >> 5, lane = t & 31;
+    int32_t *status = a.status;
+    if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
 
     if (t == 0) {
         tc::mbar_init(bar_kv, 1);
@@ -169,27 +187,77 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
     constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
     const uint32_t aq = tc::smem_u32(sQ), ap = tc::smem_u32(sP);
     const uint32_t ak = tc::smem_u32(sK), av = tc::smem_u32(sV);
-    const int kvalid_all = int(i64min(k, nb));
+    const int32_t k = a.k;
+    const int64_t n = a.n, nb = a.nb, range = a.p.range, nranges = a.p.nranges;
+    const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;
+    const int64_t ring_stride = range * k;       // partial slots per ring entry
+    const int total = *a.w.n_items;
 
     uint32_t kv_phase = 0, mma_phase = 0;
     bool ok = true;
-    const int total = *n_items;
-    for (int it = blockIdx.x; ok && it < total; it += gridDim.x) {
-        const int2 item = items[it];
-        const int64_t hb = item.x;                // bin = (head, query range, block)
-        const int64_t h = hb / bins_per_head;
-        const int64_t b = hb % nb;
-        const int32_t cnt = offsets[hb + 1] - offsets[hb];
-        const int32_t end = min(cnt, item.y + item_pairs);
-        const int32_t *ent = entries + offsets[hb];
+    for (;;) {
+        if (t == 0) *s_item = atomicAdd(a.queue_head, 1);
+        __syncthreads();
+        const int it = *s_item;
+        __syncthreads();                          // s_item may be rewritten below
+        if (it >= total || !ok) break;
+        const int2 item = a.w.items[it];
+
+        if (item.x < 0) {
+            // -------------------------------------------------- merge item
+            const int64_t rg = -int64_t(item.x) - 1;
+            const int64_t h = rg / nranges, rr = rg % nranges;
+            if (t == 0) {
+                const bool got = wait_counter(a.range_done + rg, a.w.range_total[rg], status);
+                __threadfence();
+                *s_ok = got;
+            }
+            __syncthreads();
+            ok = *s_ok != 0;
+            if (ok) {
+                const int64_t i_begin = rr * range + item.y;
+                const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
+                const int64_t slot_base = (rg % kPartialRing) * ring_stride;
+                for (int64_t i = i_begin + warp; i < i_end; i += kThreads / 32)
+                    merge_query<D>(h * n + i, slot_base + (i - rr * range) * k, a.list, k, nb,
+                                   full_valid, lane, a.part_o, a.part_lse, a.out);
+            }
+            __threadfence();
+            __syncthreads();
+            if (t == 0 && ok) atomicAdd(a.merge_done + rg, 1);
+            continue;
+        }
+
+        // ------------------------------------------------------ fine item
+        const int64_t bin = item.x;
+        const int64_t rg = bin / nb;              // range = head * nranges + r
+        const int64_t h = rg / nranges, rr = rg % nranges;
+        const int64_t b = bin % nb;
+        const int32_t *ent = a.w.entries + a.w.offsets[bin];
+        const int32_t cnt = a.w.offsets[bin + 1] - a.w.offsets[bin];
+        const int32_t end = min(cnt, item.y + a.p.item_pairs);
+        const int64_t slot_base = (rg % kPartialRing) * ring_stride;
         if (t == 0) {
-            tc::mbar_arrive_expect_tx(bar_kv, S::kKBytes + S::kVBytes);
+            bool got = true;
+            // the ring entry must have been merged by its previous range
+            if (rg >= kPartialRing)
+                got = wait_counter(a.merge_done + (rg - kPartialRing),
+                                   a.w.range_merges[rg - kPartialRing], status);
+            *s_ok = got;
+            if (got) {
+                tc::mbar_arrive_expect_tx(bar_kv, S::kKBytes + S::kVBytes);
 #pragma unroll
-            for (int sub = 0; sub < S::kSub; ++sub) {
-                tc::tma_load_3d(sK + sub * kB * 128, &tm_k, bar_kv, sub * 64, int32_t(b * kB), int32_t(h));
-                tc::tma_load_3d(sV + sub * kB * 128, &tm_v, bar_kv, sub * 64, int32_t(b * kB), int32_t(h));
+                for (int sub = 0; sub < S::kSub; ++sub) {
+                    tc::tma_load_3d(sK + sub * kB * 128, &tm_k, bar_kv, sub * 64, int32_t(b * kB),
+                                    int32_t(h));
+                    tc::tma_load_3d(sV + sub * kB * 128, &tm_v, bar_kv, sub * 64, int32_t(b * kB),
+                                    int32_t(h));
+                }
             }
         }
+        __syncthreads();
+        ok = *s_ok != 0;
+        if (!ok) break;
         const int64_t keys_valid = n - b * kB;    // >= 1; < 64 only for a ragged last block
         bool first_tile = true;
         for (int32_t p0 = item.y; ok && p0 < end; p0 += kTile) {
@@ -197,9 +265,11 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
             const int32_t p = p0 + t;
             const bool has = p < end;
             const int32_t pid = has ? __ldg(ent + p) : 0;
-            const int64_t qrow = pid / k;
+            const int64_t qrow = pid / k;                       // h * n + i
+            const int64_t slot = pid - qrow * k;
+            const int64_t part = slot_base + (qrow - h * n - rr * range) * k + slot;
             if (has) {
-                const uint16_t *src = q + qrow * D;
+                const uint16_t *src = a.q + qrow * D;
 #pragma unroll
                 for (int c = 0; c < D / 8; ++c) {
                     const int sub = c >> 3, cc = c & 7;
@@ -240,7 +310,7 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
                 float s2[64];
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
-                    s2[j] = j < keys_valid ? __uint_as_float(sv[j >> 5][j & 31]) * scale_log2 : -INFINITY;
+                    s2[j] = j < keys_valid ? __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2 : -INFINITY;
                     m2 = fmaxf(m2, s2[j]);
                 }
 #pragma unroll
@@ -273,47 +343,33 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
             if (ok) ok = tc::mbar_wait(bar_mma, mma_phase, status);
             mma_phase ^= 1;
             tc::tc_fence_after();
-            // 5. partial state of the pair, then the last writer merges
-            {
-                const float inv_l = 1.f / l;
+            // 5. the pair's partial state
+            const float inv_l = 1.f / l;
 #pragma unroll
-                for (int c0 = 0; c0 < D; c0 += 32) {
-                    uint32_t ov[32];
-                    tc::tmem_ld32(tmem_o + lane_off + c0, ov);
-                    tc::tmem_ld_wait();
-                    if (has) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(part_o + int64_t(pid) * D + c0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[v] = make_uint4(
-                                pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l),
-                                pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l),
-                                pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l),
-                                pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l));
-                    }
-                }
-                bool last = false;
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tc::tmem_ld32(tmem_o + lane_off + c0, ov);
+                tc::tmem_ld_wait();
                 if (has) {
-                    part_lse[pid] = m2 + __log2f(l);
-                    // release: this pair's partial is visible before the count;
-                    // acquire: the last writer sees every other slot's partial
-                    const int done = atomic_add_acq_rel(qcount + qrow, 1) + 1;
-                    const int need = full_lists ? kvalid_all : list_valid(list + qrow * k, k, nb);
-                    last = done == need;
-                }
-                unsigned todo = __ballot_sync(0xffffffffu, last);
-                while (todo != 0u) {
-                    const int src_lane = __ffs(todo) - 1;
-                    todo &= todo - 1u;
-                    const int64_t r = __shfl_sync(0xffffffffu, qrow, src_lane);
-                    merge_query_warp<D>(r, list, k, nb, full_lists ? kvalid_all : 0, t & 31, part_o,
-                                        part_lse, out);
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.part_o + part * D + c0);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l));
                 }
             }
+            if (has) a.part_lse[part] = m2 + __log2f(l);
             tc::tc_fence_before();
             ok = __syncthreads_and(ok);   // keeps the loop conditions uniform
         }
         kv_phase ^= 1;
+        // publish: this item's partial states are written
+        __threadfence();
+        __syncthreads();
+        if (t == 0 && ok) atomicAdd(a.range_done + rg, end - item.y);
     }
 
     tc::tc_fence_before();
@@ -369,12 +425,7 @@ cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorM
     const int tmem_limit = int(512 / S::kTmemCols);
     if (per_sm > tmem_limit) per_sm = tmem_limit;
     if (per_sm < 1) per_sm = 1;
-    const int grid = sms * per_sm;
-    kern<<<grid, kThreads, S::kTotal, st>>>(mk, mv, a.q, a.list, a.entries, a.offsets, a.items,
-                                            a.n_items, a.n, a.nb, a.bins_per_head, a.k,
-                                            a.full_lists, a.item_pairs,
-                                            a.scale_log2, a.part_o, a.part_lse, a.qcount, a.out,
-                                            a.status);
+    kern<<<sms * per_sm, kThreads, S::kTotal, st>>>(mk, mv, a);
     return cudaGetLastError();
 }
 

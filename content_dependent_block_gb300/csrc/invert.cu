@@ -13,9 +13,9 @@
 //   count    per bin: how many (query, slot) pairs selected the block;
 //            CTA-local shared-memory histograms, one global atomic per
 //            touched bin and CTA
-//   scan     exclusive prefix over (head, block) -> CSR offsets, plus the
-//            work items (head, block, first pair) of at most kItemPairs
-//            pairs each, in head-major order
+//   scan     exclusive prefix over the bins -> CSR offsets, plus the work
+//            list of the fine stage (fine items per bin, merge items per
+//            range, see scan_kernel)
 //   scatter  writes every pair id p = (h*n + i)*k + s into its block's
 //            range (order inside a range is arbitrary; results do not
 //            depend on it); queries with no valid slot get O = 0 here
@@ -59,68 +59,121 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restri
         if (hist[b] != 0) atomicAdd(counts + bin0 + b, hist[b]);
 }
 
-// One CTA of 1024 threads over the nbh bins (head, query range, block):
-// offsets[nbh + 1], items[...] = {bin, first pair}
-__global__ void __launch_bounds__(1024) scan_kernel(const int32_t *__restrict__ counts,
-                                                    int64_t nbh, int32_t item_pairs,
-                                                    int32_t *__restrict__ offsets,
-                                                    int2 *__restrict__ items,
-                                                    int32_t *__restrict__ n_items) {
-    __shared__ int64_t warp_pairs[32];
-    __shared__ int64_t warp_items[32];
-    const int t = threadIdx.x;
-    const int64_t per = (nbh + 1023) / 1024;
-    const int64_t e0 = i64min(nbh, t * per);
-    const int64_t e1 = i64min(nbh, e0 + per);
-    int64_t my_pairs = 0, my_items = 0;
-    for (int64_t e = e0; e < e1; ++e) {
-        const int64_t c = counts[e];
-        my_pairs += c;
-        my_items += (c + item_pairs - 1) / item_pairs;
-    }
-    // block-wide exclusive scan of (pairs, items)
-    int64_t ip = my_pairs, ii = my_items;
-    const int lane = t & 31, warp = t >> 5;
+// Block-wide exclusive scan of two int64 values per thread (1024 threads).
+__device__ __forceinline__ void block_scan2(int64_t &a, int64_t &b, int64_t *wa, int64_t *wb) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t a0 = a, b0 = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int64_t a = __shfl_up_sync(0xffffffffu, ip, o);
-        const int64_t b = __shfl_up_sync(0xffffffffu, ii, o);
+        const int64_t x = __shfl_up_sync(0xffffffffu, a, o);
+        const int64_t y = __shfl_up_sync(0xffffffffu, b, o);
         if (lane >= o) {
-            ip += a;
-            ii += b;
+            a += x;
+            b += y;
         }
     }
     if (lane == 31) {
-        warp_pairs[warp] = ip;
-        warp_items[warp] = ii;
+        wa[warp] = a;
+        wb[warp] = b;
     }
     __syncthreads();
     if (warp == 0) {
-        int64_t wp = warp_pairs[lane], wi = warp_items[lane];
+        int64_t x = wa[lane], y = wb[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int64_t a = __shfl_up_sync(0xffffffffu, wp, o);
-            const int64_t b = __shfl_up_sync(0xffffffffu, wi, o);
+            const int64_t u = __shfl_up_sync(0xffffffffu, x, o);
+            const int64_t v = __shfl_up_sync(0xffffffffu, y, o);
             if (lane >= o) {
-                wp += a;
-                wi += b;
+                x += u;
+                y += v;
             }
         }
-        warp_pairs[lane] = wp;   // inclusive over warps
-        warp_items[lane] = wi;
+        wa[lane] = x;
+        wb[lane] = y;
     }
     __syncthreads();
-    int64_t pair_off = ip - my_pairs + (warp > 0 ? warp_pairs[warp - 1] : 0);
-    int64_t item_off = ii - my_items + (warp > 0 ? warp_items[warp - 1] : 0);
+    a = a - a0 + (warp > 0 ? wa[warp - 1] : 0);
+    b = b - b0 + (warp > 0 ? wb[warp - 1] : 0);
+    __syncthreads();
+}
+
+// One CTA of 1024 threads.  Builds the CSR offsets over the bins
+// (range-major: bin = range * nb + block, range = head * nranges + r) and
+// the work list of the fine stage: per range its fine items {bin, first
+// pair} (at most item_pairs pairs each), and its merge items {-(range+1),
+// first query} (qm queries each) placed right after the NEXT range's fine
+// items, so that merging range r overlaps the fine work of range r+1.
+__global__ void __launch_bounds__(1024) scan_kernel(
+    const int32_t *__restrict__ counts, int64_t nb, int64_t nr, int64_t nranges, int64_t range,
+    int64_t n, int32_t item_pairs, int32_t qm, int32_t *__restrict__ offsets,
+    int32_t *__restrict__ fitem_off, int32_t *__restrict__ fpre, int32_t *__restrict__ mpre,
+    int32_t *__restrict__ range_total, int32_t *__restrict__ range_merges,
+    int2 *__restrict__ items, int32_t *__restrict__ n_items) {
+    __shared__ int64_t wa[32], wb[32];
+    const int t = threadIdx.x;
+    const int64_t nbins = nr * nb;
+    // 1. bins: pair offsets and fine-item offsets
+    const int64_t per = (nbins + 1023) / 1024;
+    const int64_t e0 = i64min(nbins, t * per), e1 = i64min(nbins, e0 + per);
+    int64_t pairs = 0, fitems = 0;
     for (int64_t e = e0; e < e1; ++e) {
         const int64_t c = counts[e];
-        offsets[e] = int32_t(pair_off);
-        for (int64_t f = 0; f < c; f += item_pairs) items[item_off++] = make_int2(int(e), int(f));
-        pair_off += c;
+        pairs += c;
+        fitems += (c + item_pairs - 1) / item_pairs;
+    }
+    int64_t poff = pairs, foff = fitems;
+    block_scan2(poff, foff, wa, wb);
+    for (int64_t e = e0; e < e1; ++e) {
+        const int64_t c = counts[e];
+        offsets[e] = int32_t(poff);
+        fitem_off[e] = int32_t(foff);
+        poff += c;
+        foff += (c + item_pairs - 1) / item_pairs;
     }
     if (t == 1023) {
-        offsets[nbh] = int32_t(pair_off);
-        *n_items = int32_t(item_off);
+        offsets[nbins] = int32_t(poff);
+        fitem_off[nbins] = int32_t(foff);
+    }
+    __syncthreads();
+    // 2. ranges: pair totals, fine-item and merge-item prefixes
+    const int64_t rper = (nr + 1023) / 1024;
+    const int64_t r0 = i64min(nr, t * rper), r1 = i64min(nr, r0 + rper);
+    int64_t f_sum = 0, m_sum = 0;
+    for (int64_t r = r0; r < r1; ++r) {
+        const int64_t rr = r % nranges;
+        const int64_t queries = i64min(range, n - rr * range);
+        const int64_t m = (queries + qm - 1) / qm;
+        range_total[r] = offsets[(r + 1) * nb] - offsets[r * nb];
+        range_merges[r] = int32_t(m);
+        f_sum += fitem_off[(r + 1) * nb] - fitem_off[r * nb];
+        m_sum += m;
+    }
+    int64_t fo = f_sum, mo = m_sum;
+    block_scan2(fo, mo, wa, wb);
+    for (int64_t r = r0; r < r1; ++r) {
+        fpre[r] = int32_t(fo);
+        mpre[r] = int32_t(mo);
+        fo += fitem_off[(r + 1) * nb] - fitem_off[r * nb];
+        mo += range_merges[r];
+    }
+    if (t == 1023) {
+        fpre[nr] = int32_t(fo);
+        fpre[nr + 1] = int32_t(fo);
+        mpre[nr] = int32_t(mo);
+        *n_items = int32_t(fo + mo);
+    }
+    __syncthreads();
+    // 3. the work list
+    for (int64_t e = e0; e < e1; ++e) {
+        const int64_t r = e / nb;
+        const int64_t c = counts[e];
+        int64_t pos = fitem_off[e] + (r >= 1 ? mpre[r - 1] : 0);
+        for (int64_t f = 0; f < c; f += item_pairs) items[pos++] = make_int2(int(e), int(f));
+    }
+    for (int64_t r = r0; r < r1; ++r) {
+        int64_t pos = fpre[i64min(r + 2, nr)] + mpre[r];
+        for (int64_t j = 0; j < range_merges[r]; ++j)
+            items[pos++] = make_int2(int(-(r + 1)), int(j * qm));
     }
 }
 
@@ -178,39 +231,42 @@ int64_t invert_query_range(int64_t n, int64_t nb, int32_t k) {
     return r;
 }
 
-int64_t invert_bins(int64_t bh, int64_t n, int64_t nb, int32_t k) {
-    const int64_t r = invert_query_range(n, nb, k);
-    return bh * ((n + r - 1) / r) * nb;
-}
-
-size_t invert_items_capacity(int64_t bh, int64_t n, int64_t nb, int32_t k, int32_t item_pairs) {
-    return size_t(invert_bins(bh, n, nb, k)) + size_t((bh * n * k + item_pairs - 1) / item_pairs);
+InvertPlan invert_plan(int64_t bh, int64_t n, int64_t nb, int32_t k) {
+    InvertPlan p;
+    p.range = invert_query_range(n, nb, k);
+    p.nranges = (n + p.range - 1) / p.range;
+    p.nr = bh * p.nranges;
+    p.nbins = p.nr * nb;
+    p.item_pairs = kFineBmItemPairs;
+    p.qm = kMergeQueries;
+    p.items_cap = p.nbins + (bh * n * k + p.item_pairs - 1) / p.item_pairs +
+                  p.nr * ((p.range + p.qm - 1) / p.qm);
+    return p;
 }
 
 cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
-                          int32_t item_pairs, int32_t *counts, int32_t *cursors,
-                          int32_t *offsets, int2 *items, int32_t *n_items, int32_t *entries,
-                          uint16_t *out_bf16, int32_t d, int32_t *status, cudaStream_t st) {
+                          const InvertPlan &p, const InvertBuffers &w, uint16_t *out_bf16,
+                          int32_t d, int32_t *status, cudaStream_t st) {
     const dim3 grid(unsigned((n + kQueriesPerCta - 1) / kQueriesPerCta), unsigned(bh));
     const size_t smem1 = size_t(nb) * sizeof(int32_t);
-    if (smem1 > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(smem1));
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(scatter_kernel<uint16_t>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * smem1));
-        if (e != cudaSuccess) return e;
-    } else if (2 * smem1 > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(scatter_kernel<uint16_t>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * smem1));
-        if (e != cudaSuccess) return e;
-    }
-    const int64_t range = invert_query_range(n, nb, k);
-    const int64_t nranges = (n + range - 1) / range;
-    count_kernel<<<grid, kThreads, smem1, st>>>(list, n, nb, k, range, nranges, counts, status);
-    scan_kernel<<<1, 1024, 0, st>>>(counts, bh * nranges * nb, item_pairs, offsets, items, n_items);
-    scatter_kernel<uint16_t><<<grid, kThreads, 2 * smem1, st>>>(list, n, nb, k, range, nranges,
-                                                                offsets, cursors, entries, out_bf16, d);
+    cudaError_t e = cudaSuccess;
+    if (smem1 > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(smem1))) != cudaSuccess)
+        return e;
+    if (2 * smem1 > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(scatter_kernel<uint16_t>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * smem1))) !=
+            cudaSuccess)
+        return e;
+    count_kernel<<<grid, kThreads, smem1, st>>>(list, n, nb, k, p.range, p.nranges, w.counts,
+                                               status);
+    scan_kernel<<<1, 1024, 0, st>>>(w.counts, nb, p.nr, p.nranges, p.range, n, p.item_pairs, p.qm,
+                                    w.offsets, w.fitem_off, w.fpre, w.mpre, w.range_total,
+                                    w.range_merges, w.items, w.n_items);
+    scatter_kernel<uint16_t><<<grid, kThreads, 2 * smem1, st>>>(list, n, nb, k, p.range,
+                                                                p.nranges, w.offsets, w.cursors,
+                                                                w.entries, out_bf16, d);
     return cudaGetLastError();
 }
 
