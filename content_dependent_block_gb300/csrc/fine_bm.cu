@@ -77,72 +77,105 @@ __device__ __forceinline__ void discard_l2_line(const void *p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
-// Merge query row `qrow` (flat h*n + i): lane s reads slot s's lse; lane l
-// owns D/32 channels; all of the row's partial values are requested before
-// any is used.  `base` indexes the query's k partial slots in the ring.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Merge up to four queries per warp: the warp splits into four 8-lane
+// groups, one query each; lane gl of a group owns channels [gl*D/8,
+// (gl+1)*D/8).  Slot lse values are spread over the group's lanes; every
+// partial row of a chunk of slots is requested before any is used.
+// `qrow` / `base` are the group's query row (flat h*n + i) and the index of
+// its k partial slots in the ring; `active` false for a group with no query.
 template <int D>
-__device__ __forceinline__ void merge_query(int64_t qrow, int64_t base, const int32_t *list,
-                                            int32_t k, int64_t nb, int32_t full_valid, int lane,
-                                            uint16_t *part_o, const float *part_lse,
-                                            uint16_t *out) {
-    constexpr int E = D / 32;     // channels per lane: 2 or 4
-    bool valid = false;
-    if (lane < k) {
-        if (full_valid > 0) {
-            valid = lane < full_valid;
-        } else {
-            const int32_t b = __ldg(list + qrow * k + lane);
-            valid = b >= 0 && b < nb;
+__device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t base,
+                                            const int32_t *list, int32_t k, int64_t nb,
+                                            int32_t full_valid, int lane, uint16_t *part_o,
+                                            const float *part_lse, uint16_t *out) {
+    constexpr int C = D / 8;                   // channels per lane: 8 or 16
+    constexpr int V = C / 8;                   // uint4 per partial row chunk: 1 or 2
+    constexpr int CH = D == 64 ? 16 : 8;       // slots per load chunk
+    const int gl = lane & 7;
+    const int gbase = lane & ~7;
+    bool vs[4];
+    float lse[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int s = gl + 8 * j;
+        bool v = active && s < k;
+        if (v && full_valid == 0) {
+            const int32_t b = __ldg(list + qrow * k + s);
+            v = b >= 0 && b < nb;
+        } else if (v) {
+            v = s < full_valid;
+        }
+        vs[j] = v;
+        lse[j] = v ? __ldcg(part_lse + base + s) : -INFINITY;
+    }
+    float M = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float w[4], L = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w[j] = vs[j] ? ex2(lse[j] - M) : 0.f;
+        L += w[j];
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < 32; c0 += CH) {
+        if (c0 >= k) break;
+        uint4 x[CH][V];
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+            const int s = c0 + u;
+            const bool v = __shfl_sync(0xffffffffu, vs[s >> 3], gbase | (s & 7));
+            const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (base + s) * D + gl * C);
+#pragma unroll
+            for (int e = 0; e < V; ++e) x[u][e] = v ? __ldcg(src + e) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < CH; ++u) {
+            const int s = c0 + u;
+            const float ws = __shfl_sync(0xffffffffu, w[s >> 3], gbase | (s & 7));
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const uint32_t xw[4] = {x[u][e].x, x[u][e].y, x[u][e].z, x[u][e].w};
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    acc[8 * e + 2 * h2] = fmaf(ws, bf16_low_half(xw[h2]), acc[8 * e + 2 * h2]);
+                    acc[8 * e + 2 * h2 + 1] = fmaf(ws, bf16_high_half(xw[h2]), acc[8 * e + 2 * h2 + 1]);
+                }
+            }
         }
     }
-    if (__ballot_sync(0xffffffffu, valid) == 0u) return;   // nothing listed: O stays 0
-    const float lse = valid ? __ldcg(part_lse + base + lane) : -INFINITY;
-    uint32_t raw[32][E / 2];
+    if (!active || L == 0.f) return;           // nothing listed: O stays 0
+    const float invL = 1.f / L;
+    uint4 *dst = reinterpret_cast<uint4 *>(out + qrow * D + gl * C);
 #pragma unroll
-    for (int s = 0; s < 32; ++s) {
-        const bool vs = __shfl_sync(0xffffffffu, valid, s);
-        const uint16_t *src = part_o + (base + s) * D + lane * E;
-        if (E == 2) {
-            raw[s][0] = vs ? __ldcg(reinterpret_cast<const unsigned int *>(src)) : 0u;
-        } else {
-            const uint2 x = vs ? __ldcg(reinterpret_cast<const uint2 *>(src)) : make_uint2(0u, 0u);
-            raw[s][0] = x.x;
-            raw[s][E / 2 - 1] = x.y;
-        }
-    }
-    const float M = warp_max(lse);
-    const float w = valid ? exp2f(lse - M) : 0.f;
-    const float invL = 1.f / warp_sum(w);
-    float acc[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-#pragma unroll
-    for (int s = 0; s < 32; ++s) {
-        const float ws = __shfl_sync(0xffffffffu, w, s);
-#pragma unroll
-        for (int e2 = 0; e2 < E / 2; ++e2) {
-            acc[2 * e2] = fmaf(ws, bf16_low_half(raw[s][e2]), acc[2 * e2]);
-            acc[2 * e2 + 1] = fmaf(ws, bf16_high_half(raw[s][e2]), acc[2 * e2 + 1]);
-        }
-    }
-    uint16_t *dst = out + qrow * D + lane * E;
-    if (E == 2) {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * invL, acc[1] * invL);
-    } else {
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(acc[0] * invL, acc[1] * invL),
-                                                     pack_bf16x2(acc[E - 2] * invL, acc[E - 1] * invL));
-    }
+    for (int e = 0; e < V; ++e)
+        dst[e] = make_uint4(pack_bf16x2(acc[8 * e + 0] * invL, acc[8 * e + 1] * invL),
+                            pack_bf16x2(acc[8 * e + 2] * invL, acc[8 * e + 3] * invL),
+                            pack_bf16x2(acc[8 * e + 4] * invL, acc[8 * e + 5] * invL),
+                            pack_bf16x2(acc[8 * e + 6] * invL, acc[8 * e + 7] * invL));
     // the merged partial rows are dead: drop them from L2 without write-back
-    __syncwarp();
-    if (valid) {
 #pragma unroll
-        for (int line = 0; line < D * 2 / 128; ++line)
-            discard_l2_line(part_o + (base + lane) * D + line * 64);
-    }
+    for (int j = 0; j < 4; ++j)
+        if (vs[j]) {
+#pragma unroll
+            for (int line = 0; line < D * 2 / 128; ++line)
+                discard_l2_line(part_o + (base + gl + 8 * j) * D + line * 64);
+        }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) fine_bm_kernel(
+__global__ void __launch_bounds__(kThreads, D == 64 ? 4 : 2) fine_bm_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const FineBmArgs a) {
     using S = BmSmem<D>;
@@ -218,9 +251,14 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
                 const int64_t i_begin = rr * range + item.y;
                 const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
                 const int64_t slot_base = (rg % kPartialRing) * ring_stride;
-                for (int64_t i = i_begin + warp; i < i_end; i += kThreads / 32)
-                    merge_query<D>(h * n + i, slot_base + (i - rr * range) * k, a.list, k, nb,
-                                   full_valid, lane, a.part_o, a.part_lse, a.out);
+                // 16 queries per pass: 4 warps x 4 groups of 8 lanes
+                for (int64_t i0 = i_begin; i0 < i_end; i0 += 16) {
+                    const int64_t i = i0 + warp * 4 + (lane >> 3);
+                    const bool act = i < i_end;
+                    const int64_t ic = act ? i : i_begin;
+                    merge_group<D>(act, h * n + ic, slot_base + (ic - rr * range) * k, a.list, k,
+                                   nb, full_valid, lane, a.part_o, a.part_lse, a.out);
+                }
             }
             __threadfence();
             __syncthreads();
@@ -309,13 +347,19 @@ __global__ void __launch_bounds__(kThreads) fine_bm_kernel(
                 tc::tmem_ld_wait();
                 float s2[64];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    s2[j] = j < keys_valid ? __uint_as_float(sv[j >> 5][j & 31]) * a.scale_log2 : -INFINITY;
-                    m2 = fmaxf(m2, s2[j]);
+                for (int j = 0; j < 64; ++j) s2[j] = __uint_as_float(sv[j >> 5][j & 31]);
+                if (keys_valid < 64) {                    // ragged last block only
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (j >= keys_valid) s2[j] = -INFINITY;
                 }
+                float mraw = s2[0];
+#pragma unroll
+                for (int j = 1; j < 64; ++j) mraw = fmaxf(mraw, s2[j]);
+                m2 = mraw * a.scale_log2;                 // scale > 0 keeps the argmax
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
-                    s2[j] = exp2f(s2[j] - m2);
+                    s2[j] = ex2(fmaf(s2[j], a.scale_log2, -m2));
                     l += s2[j];
                 }
 #pragma unroll
@@ -420,10 +464,16 @@ cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorM
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
         return e;
-    // resident CTAs per SM: shared memory (+1 KB reserved per CTA) and TMEM
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    // resident CTAs per SM: shared memory (+1 KB reserved per CTA), TMEM and
+    // registers (allocated per warp in units of 256)
     int per_sm = smem_sm / (S::kTotal + 1024);
     const int tmem_limit = int(512 / S::kTmemCols);
+    const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;
+    const int reg_limit = 65536 / (warp_regs * (kThreads / 32));
     if (per_sm > tmem_limit) per_sm = tmem_limit;
+    if (per_sm > reg_limit) per_sm = reg_limit;
     if (per_sm < 1) per_sm = 1;
     kern<<<sms * per_sm, kThreads, S::kTotal, st>>>(mk, mv, a);
     return cudaGetLastError();
