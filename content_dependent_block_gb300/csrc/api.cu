@@ -125,11 +125,11 @@ cudaError_t run_coarse(const bsa_shape &s, const void *q, const float *kbar, con
 // Workspace of the block-major fine stage over per-query lists [bh][n][k].
 struct BmLayout {
     bsa::InvertPlan plan;
-    size_t zero = 0, zero_bytes = 0;     // counts, cursors, queue head, range counters
-    size_t counts = 0, cursors = 0, queue_head = 0, range_done = 0, merge_done = 0;
+    size_t zero = 0, zero_bytes = 0;     // counts, cursors, queue heads, range counters
+    size_t counts = 0, cursors = 0, fine_head = 0, merge_head = 0, range_done = 0, merge_done = 0;
     size_t offsets = 0, fitem_off = 0, fpre = 0, mpre = 0, range_total = 0, range_merges = 0;
-    size_t n_items = 0, items = 0, entries = 0, part_o = 0, part_lse = 0;
-    size_t total = 0;
+    size_t n_fine = 0, n_merge = 0, fine_items = 0, merge_items = 0, entries = 0;
+    size_t part_o = 0, part_lse = 0, total = 0;
 };
 
 BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
@@ -137,7 +137,7 @@ BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     const int64_t nb = ceil_div(s.n, kb);
     L.plan = bsa::invert_plan(s.bh, s.n, nb, k);
     const size_t nbins = size_t(L.plan.nbins), nr = size_t(L.plan.nr);
-    const size_t ring_slots = size_t(bsa::kPartialRing) * size_t(L.plan.range) * size_t(k);
+    const size_t ring_slots = size_t(bsa::kPartialRing) * size_t(L.plan.range) * size_t(L.plan.kpad);
     size_t off = base;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -147,7 +147,8 @@ BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     L.zero = off;
     L.counts = take(nbins * 4);
     L.cursors = take(nbins * 4);
-    L.queue_head = take(4);
+    L.fine_head = take(4);
+    L.merge_head = take(4);
     L.range_done = take(nr * 4);
     L.merge_done = take(nr * 4);
     L.zero_bytes = off - L.zero;
@@ -158,8 +159,10 @@ BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     L.mpre = take((nr + 1) * 4);
     L.range_total = take(nr * 4);
     L.range_merges = take(nr * 4);
-    L.n_items = take(4);
-    L.items = take(size_t(L.plan.items_cap) * sizeof(int2));
+    L.n_fine = take(4);
+    L.n_merge = take(4);
+    L.fine_items = take(size_t(L.plan.fine_cap) * sizeof(int2));
+    L.merge_items = take(size_t(L.plan.merge_cap) * sizeof(int2));
     L.entries = take(size_t(s.bh) * s.n * k * 4);
     off = round_up(off, 256);
     L.part_o = take(ring_slots * s.d * 2);
@@ -191,8 +194,10 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     w.mpre = reinterpret_cast<int32_t *>(ws + L.mpre);
     w.range_total = reinterpret_cast<int32_t *>(ws + L.range_total);
     w.range_merges = reinterpret_cast<int32_t *>(ws + L.range_merges);
-    w.items = reinterpret_cast<int2 *>(ws + L.items);
-    w.n_items = reinterpret_cast<int32_t *>(ws + L.n_items);
+    w.fine_items = reinterpret_cast<int2 *>(ws + L.fine_items);
+    w.merge_items = reinterpret_cast<int2 *>(ws + L.merge_items);
+    w.n_fine = reinterpret_cast<int32_t *>(ws + L.n_fine);
+    w.n_merge = reinterpret_cast<int32_t *>(ws + L.n_merge);
     w.entries = reinterpret_cast<int32_t *>(ws + L.entries);
     e = bsa::launch_invert(list, s.bh, s.n, nb, topk, L.plan, w, static_cast<uint16_t *>(out), s.d,
                            status, st);
@@ -204,7 +209,8 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     a.list = list;
     a.w = w;
     a.p = L.plan;
-    a.queue_head = reinterpret_cast<int32_t *>(ws + L.queue_head);
+    a.fine_head = reinterpret_cast<int32_t *>(ws + L.fine_head);
+    a.merge_head = reinterpret_cast<int32_t *>(ws + L.merge_head);
     a.range_done = reinterpret_cast<int32_t *>(ws + L.range_done);
     a.merge_done = reinterpret_cast<int32_t *>(ws + L.merge_done);
     a.bh = s.bh;

@@ -61,8 +61,9 @@ constexpr int32_t kPartialRing = 4;         // query ranges whose partials coexi
 
 // Bins are (head, query range of `range` queries, key block).
 struct InvertPlan {
-    int64_t range = 0, nranges = 0, nr = 0, nbins = 0, items_cap = 0;
+    int64_t range = 0, nranges = 0, nr = 0, nbins = 0, fine_cap = 0, merge_cap = 0;
     int32_t item_pairs = 0, qm = 0;
+    int32_t kpad = 0;       // partial slots per query in the ring (k rounded up to 4)
 };
 InvertPlan invert_plan(int64_t bh, int64_t n, int64_t nb, int32_t k);
 
@@ -75,8 +76,10 @@ struct InvertBuffers {
     int32_t *mpre;          // [nr + 1]
     int32_t *range_total;   // [nr] pairs per range
     int32_t *range_merges;  // [nr] merge items per range
-    int2 *items;            // [items_cap]
-    int32_t *n_items;
+    int2 *fine_items;       // [fine_cap]  {bin, first pair}
+    int2 *merge_items;      // [merge_cap] {range, first query}
+    int32_t *n_fine;
+    int32_t *n_merge;
     int32_t *entries;       // [bh * n * k]
 };
 // count + scan + scatter launches
@@ -91,15 +94,16 @@ struct FineBmArgs {
     const int32_t *list;          // [bh][n][k]
     InvertBuffers w;
     InvertPlan p;
-    int32_t *queue_head;          // zeroed
+    int32_t *fine_head;           // zeroed queue heads
+    int32_t *merge_head;
     int32_t *range_done;          // [nr] zeroed: pairs with partials written
     int32_t *merge_done;          // [nr] zeroed: merge items finished
     int64_t bh, n, nb;
     int32_t d, k;
     int32_t full_lists;           // every row holds min(k, nb) valid ids, first
     float scale_log2;
-    uint16_t *part_o;             // [ring][range * k][d] bf16
-    float *part_lse;              // [ring][range * k]
+    uint16_t *part_o;             // [ring][range * kpad][d] bf16
+    float *part_lse;              // [ring][range * kpad]
     uint16_t *out;
     int32_t *status;
 };

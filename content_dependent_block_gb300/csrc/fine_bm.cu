@@ -4,26 +4,34 @@
 // accumulator acc merged block by block).
 //
 // Schedule.  The per-query lists are inverted (invert.cu) into bins
-// (head, query range, key block), each listing the (query, slot) pairs
-// that selected the block.  A persistent grid pulls work items from one
-// queue (an atomic counter) in the order the scan kernel laid out:
-//   fine items   one bin and up to 512 of its pairs.  The CTA loads K_b and
-//                V_b once (TMA, 128-byte swizzle); per tile of 128 pairs it
-//                gathers the query rows (cp.async), S = Q_g . K_b^T
-//                (tcgen05, M = 128, N = 64, fp32 in TMEM), per row
-//                m = max s, p = exp2(s - m), l = sum p, P -> shared memory
-//                (bf16), O = P . V_b (tcgen05, N = d), and stores the pair's
-//                partial state o = O / l (bf16) and lse = m + log2 l.
-//   merge items  256 queries of a range whose fine items are all done: the
-//                k partial states of each query are merged in slot order
-//                (online-softmax merge of (m, l, acc)) into O, and the
-//                merged partial lines are discarded from L2 so they are
-//                never written back to memory.
-// Merge items of range r sit after the fine items of range r + 1, so every
-// wait is on work taken from the queue earlier (no deadlock), and partial
-// states live in a ring of kPartialRing ranges (bounded, L2-sized memory).
-// Results do not depend on scheduling: partial states are per pair and the
-// merge reads them in slot order.
+// (head, query range, key block), each listing the (query, slot) pairs that
+// selected the block.  One persistent CTA per SM runs five warp roles that
+// hand work to each other through mbarrier rings in shared memory:
+//
+//   producer  (warp 0)      takes fine items (one bin, <= 512 pairs) from a
+//                           global queue; loads K_b, V_b by TMA (128-byte
+//                           swizzle, double-buffered per item) and gathers the
+//                           128 query rows of each tile with cp.async into a
+//                           ring of Q stages; publishes per-tile info
+//   MMA       (warp 1)      S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
+//                           one of two TMEM score buffers, then O[j] = P . V_b
+//                           (N = d, V MN-major) into one of two TMEM outputs;
+//                           tile g's S is issued before tile g-1's P.V
+//   softmax   (warps 2-5)   one thread per row: m = max s, p = exp2(s - m),
+//                           l = sum p; P (bf16) to shared memory, (m, l) aside
+//   epilogue  (warps 6-9)   reads O, stores the pair's partial state
+//                           o = O / l (bf16) and lse = m + log2 l into a ring
+//                           of query ranges, counts the range's finished pairs
+//   merge     (warps 10-13) takes merge items (256 queries of one range) from a
+//                           second queue once the range's pairs are all done
+//                           and merges each query's k partial states in slot
+//                           order (the online-softmax merge of (m, l, acc))
+//
+// Partial states of a range live in ring entry (range mod kPartialRing); a
+// fine item of range r waits until range r - kPartialRing is merged.  Every
+// wait is on work taken from a queue earlier, so the schedule cannot
+// deadlock, and every wait is bounded.  Results do not depend on scheduling:
+// partial states are per pair and merged in slot order.
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -36,19 +44,54 @@ namespace bsa {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 128;
-constexpr int kB = 64;                  // key block handled by this kernel
+constexpr int kB = 64;                   // key block handled by this kernel
+constexpr int kNT = 8;                   // tile-info ring
+constexpr int kWarps = 14;
+constexpr int kThreads = kWarps * 32;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 6, kWarpMerge = 10;
+constexpr uint32_t kBarEpi = 1, kBarMerge = 2;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct TileInfo {
+    int32_t bin, p0, count, item, last, rg, end, pad;
+};
 
 template <int D>
-struct BmSmem {
+struct Cfg {
     static constexpr int kSub = D / 64;
-    static constexpr int kQBytes = kSub * kTile * 128;   // gathered Q   [128][D]
-    static constexpr int kPBytes = kTile * 128;          // P (bf16)     [128][64]
-    static constexpr int kKBytes = kSub * kB * 128;      // K_b          [64][D]
-    static constexpr int kVBytes = kSub * kB * 128;      // V_b          [64][D]
-    static constexpr int kTiles = kQBytes + kPBytes + kKBytes + kVBytes;
-    static constexpr int kTotal = kTiles + 1024 + 64;
-    static constexpr uint32_t kTmemCols = (kB + D) <= 128 ? 128 : 256;
+    static constexpr int kNQ = D == 64 ? 4 : 3;            // Q stages
+    static constexpr int kLag = kNQ - 2;                   // gathers left unpublished
+    static constexpr int kQBytes = kSub * kTile * 128;
+    static constexpr int kPBytes = kTile * 128;
+    static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
+    static constexpr int oQ = 0;
+    static constexpr int oP = oQ + kNQ * kQBytes;
+    static constexpr int oK = oP + 2 * kPBytes;
+    static constexpr int oV = oK + 2 * kKBytes;
+    static constexpr int oML = oV + 2 * kKBytes;           // float2 [2][128]
+    static constexpr int oPid = oML + 2 * kTile * 8;       // int32  [kNT][128]
+    static constexpr int oTi = oPid + kNT * kTile * 4;     // TileInfo [kNT]
+    static constexpr int oBar = oTi + kNT * 32;
+    enum {
+        bQFull = 0,
+        bQFree = bQFull + kNQ,
+        bKvFull = bQFree + kNQ,
+        bKvFree = bKvFull + 2,
+        bSFull = bKvFree + 2,
+        bSFree = bSFull + 2,
+        bPFull = bSFree + 2,
+        bPFree = bPFull + 2,
+        bOFull = bPFree + 2,
+        bOFree = bOFull + 2,
+        bMlFree = bOFree + 2,
+        bTiFull = bMlFree + 2,
+        bTiFree = bTiFull + kNT,
+        bCount = bTiFree + kNT
+    };
+    static constexpr int oMisc = oBar + bCount * 8;
+    static constexpr int kTotal = oMisc + 64 + 1024;
+    static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
+    static constexpr uint32_t cO = 2 * kB;                 // O[j] at cO + j*D; S[j] at j*64
 };
 
 __device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
@@ -58,12 +101,12 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
 }
 
 // Bounded wait until *p >= target (acquire).  False on timeout, or when
-// another CTA already reported one.
+// another wait in the grid already timed out.
 __device__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status) {
     if (ld_acquire(p) >= target) return true;
     const uint64_t t0 = tc::global_ns();
     for (;;) {
-        __nanosleep(128);
+        __nanosleep(64);
         if (ld_acquire(p) >= target) return true;
         if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return false;
         if (tc::global_ns() - t0 > tc::kWaitLimitNs) {
@@ -73,26 +116,19 @@ __device__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status) 
     }
 }
 
-__device__ __forceinline__ void discard_l2_line(const void *p) {
-    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
-}
-
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
-// Merge up to four queries per warp: the warp splits into four 8-lane
-// groups, one query each; lane gl of a group owns channels [gl*D/8,
-// (gl+1)*D/8).  Slot lse values are spread over the group's lanes; every
-// partial row of a chunk of slots is requested before any is used.
-// `qrow` / `base` are the group's query row (flat h*n + i) and the index of
-// its k partial slots in the ring; `active` false for a group with no query.
+// Merge up to four queries per warp: four 8-lane groups, one query each;
+// lane gl of a group owns channels [gl*D/8, (gl+1)*D/8).  `base` indexes the
+// query's partial slots in the ring; `active` false for an idle group.
 template <int D>
 __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t base,
                                             const int32_t *list, int32_t k, int64_t nb,
-                                            int32_t full_valid, int lane, uint16_t *part_o,
+                                            int32_t full_valid, int lane, const uint16_t *part_o,
                                             const float *part_lse, uint16_t *out) {
     constexpr int C = D / 8;                   // channels per lane: 8 or 16
     constexpr int V = C / 8;                   // uint4 per partial row chunk: 1 or 2
@@ -116,7 +152,7 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
     }
     float M = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     float w[4], L = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -124,7 +160,7 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
         L += w[j];
     }
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(kFull, L, o);
     float acc[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) acc[c] = 0.f;
@@ -135,7 +171,7 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
 #pragma unroll
         for (int u = 0; u < CH; ++u) {
             const int s = c0 + u;
-            const bool v = __shfl_sync(0xffffffffu, vs[s >> 3], gbase | (s & 7));
+            const bool v = __shfl_sync(kFull, vs[s >> 3], gbase | (s & 7));
             const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (base + s) * D + gl * C);
 #pragma unroll
             for (int e = 0; e < V; ++e) x[u][e] = v ? __ldcg(src + e) : make_uint4(0u, 0u, 0u, 0u);
@@ -143,7 +179,7 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
 #pragma unroll
         for (int u = 0; u < CH; ++u) {
             const int s = c0 + u;
-            const float ws = __shfl_sync(0xffffffffu, w[s >> 3], gbase | (s & 7));
+            const float ws = __shfl_sync(kFull, w[s >> 3], gbase | (s & 7));
 #pragma unroll
             for (int e = 0; e < V; ++e) {
                 const uint32_t xw[4] = {x[u][e].x, x[u][e].y, x[u][e].z, x[u][e].w};
@@ -164,235 +200,357 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
                             pack_bf16x2(acc[8 * e + 2] * invL, acc[8 * e + 3] * invL),
                             pack_bf16x2(acc[8 * e + 4] * invL, acc[8 * e + 5] * invL),
                             pack_bf16x2(acc[8 * e + 6] * invL, acc[8 * e + 7] * invL));
-    // the merged partial rows are dead: drop them from L2 without write-back
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-        if (vs[j]) {
-#pragma unroll
-            for (int line = 0; line < D * 2 / 128; ++line)
-                discard_l2_line(part_o + (base + gl + 8 * j) * D + line * 64);
-        }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, D == 64 ? 4 : 2) fine_bm_kernel(
+__global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const FineBmArgs a) {
-    using S = BmSmem<D>;
+    using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sQ = smem;
-    uint8_t *sP = sQ + S::kQBytes;
-    uint8_t *sK = sP + S::kPBytes;
-    uint8_t *sV = sK + S::kKBytes;
-    uint64_t *bar_kv = reinterpret_cast<uint64_t *>(smem + S::kTiles);
-    uint64_t *bar_mma = bar_kv + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_kv + 2);
-    int32_t *s_item = reinterpret_cast<int32_t *>(bar_kv + 3);    // [1]
-    int32_t *s_ok = s_item + 1;                                     // [1]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::oBar);
+    TileInfo *ti = reinterpret_cast<TileInfo *>(sm + C::oTi);
+    int32_t *pids = reinterpret_cast<int32_t *>(sm + C::oPid);
+    float2 *ml = reinterpret_cast<float2 *>(sm + C::oML);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::oMisc);
+    int32_t *s_merge = reinterpret_cast<int32_t *>(sm + C::oMisc + 16);   // [2]
 
-    const int t = threadIdx.x;
-    const int warp = t >> 5, lane = t & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = a.status;
     if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
 
-    if (t == 0) {
-        tc::mbar_init(bar_kv, 1);
-        tc::mbar_init(bar_mma, 1);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNQ; ++i) {
+            tc::mbar_init(bars + C::bQFull + i, 32);
+            tc::mbar_init(bars + C::bQFree + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bars + C::bKvFull + i, 1);
+            tc::mbar_init(bars + C::bKvFree + i, 1);
+            tc::mbar_init(bars + C::bSFull + i, 1);
+            tc::mbar_init(bars + C::bSFree + i, kTile);
+            tc::mbar_init(bars + C::bPFull + i, kTile);
+            tc::mbar_init(bars + C::bPFree + i, 1);
+            tc::mbar_init(bars + C::bOFull + i, 1);
+            tc::mbar_init(bars + C::bOFree + i, kTile);
+            tc::mbar_init(bars + C::bMlFree + i, kTile);
+        }
+        for (int i = 0; i < kNT; ++i) {
+            tc::mbar_init(bars + C::bTiFull + i, 32);
+            tc::mbar_init(bars + C::bTiFree + i, 1);
+        }
         tc::fence_barrier_init();
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
     }
-    if (warp == 0) {
-        tc::tmem_alloc(tmem_slot, S::kTmemCols);
+    if (warp == kWarpMma) {
+        tc::tmem_alloc(tmem_slot, C::kTmemCols);
         tc::tmem_relinquish();
     }
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tmem_s = tmem;                 // S: columns [0, 64)
-    const uint32_t tmem_o = tmem + kB;            // O: columns [64, 64 + D)
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
 
-    constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
-    constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
-    const uint32_t aq = tc::smem_u32(sQ), ap = tc::smem_u32(sP);
-    const uint32_t ak = tc::smem_u32(sK), av = tc::smem_u32(sV);
     const int32_t k = a.k;
     const int64_t n = a.n, nb = a.nb, range = a.p.range, nranges = a.p.nranges;
-    const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;
-    const int64_t ring_stride = range * k;       // partial slots per ring entry
-    const int total = *a.w.n_items;
+    const int64_t kpad = a.p.kpad;
+    const int64_t ring_stride = range * kpad;
 
-    uint32_t kv_phase = 0, mma_phase = 0;
-    bool ok = true;
-    for (;;) {
-        if (t == 0) *s_item = atomicAdd(a.queue_head, 1);
-        __syncthreads();
-        const int it = *s_item;
-        __syncthreads();                          // s_item may be rewritten below
-        if (it >= total || !ok) break;
-        const int2 item = a.w.items[it];
-
-        if (item.x < 0) {
-            // -------------------------------------------------- merge item
-            const int64_t rg = -int64_t(item.x) - 1;
-            const int64_t h = rg / nranges, rr = rg % nranges;
-            if (t == 0) {
-                const bool got = wait_counter(a.range_done + rg, a.w.range_total[rg], status);
-                __threadfence();
-                *s_ok = got;
-            }
-            __syncthreads();
-            ok = *s_ok != 0;
-            if (ok) {
-                const int64_t i_begin = rr * range + item.y;
-                const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
-                const int64_t slot_base = (rg % kPartialRing) * ring_stride;
-                // 16 queries per pass: 4 warps x 4 groups of 8 lanes
-                for (int64_t i0 = i_begin; i0 < i_end; i0 += 16) {
-                    const int64_t i = i0 + warp * 4 + (lane >> 3);
-                    const bool act = i < i_end;
-                    const int64_t ic = act ? i : i_begin;
-                    merge_group<D>(act, h * n + ic, slot_base + (ic - rr * range) * k, a.list, k,
-                                   nb, full_valid, lane, a.part_o, a.part_lse, a.out);
-                }
-            }
-            __threadfence();
-            __syncthreads();
-            if (t == 0 && ok) atomicAdd(a.merge_done + rg, 1);
-            continue;
-        }
-
-        // ------------------------------------------------------ fine item
-        const int64_t bin = item.x;
-        const int64_t rg = bin / nb;              // range = head * nranges + r
-        const int64_t h = rg / nranges, rr = rg % nranges;
-        const int64_t b = bin % nb;
-        const int32_t *ent = a.w.entries + a.w.offsets[bin];
-        const int32_t cnt = a.w.offsets[bin + 1] - a.w.offsets[bin];
-        const int32_t end = min(cnt, item.y + a.p.item_pairs);
-        const int64_t slot_base = (rg % kPartialRing) * ring_stride;
-        if (t == 0) {
-            bool got = true;
-            // the ring entry must have been merged by its previous range
-            if (rg >= kPartialRing)
-                got = wait_counter(a.merge_done + (rg - kPartialRing),
-                                   a.w.range_merges[rg - kPartialRing], status);
-            *s_ok = got;
-            if (got) {
-                tc::mbar_arrive_expect_tx(bar_kv, S::kKBytes + S::kVBytes);
-#pragma unroll
-                for (int sub = 0; sub < S::kSub; ++sub) {
-                    tc::tma_load_3d(sK + sub * kB * 128, &tm_k, bar_kv, sub * 64, int32_t(b * kB),
-                                    int32_t(h));
-                    tc::tma_load_3d(sV + sub * kB * 128, &tm_v, bar_kv, sub * 64, int32_t(b * kB),
-                                    int32_t(h));
-                }
-            }
-        }
-        __syncthreads();
-        ok = *s_ok != 0;
-        if (!ok) break;
-        const int64_t keys_valid = n - b * kB;    // >= 1; < 64 only for a ragged last block
-        bool first_tile = true;
-        for (int32_t p0 = item.y; ok && p0 < end; p0 += kTile) {
-            // 1. gather the tile's query rows
-            const int32_t p = p0 + t;
-            const bool has = p < end;
-            const int32_t pid = has ? __ldg(ent + p) : 0;
-            const int64_t qrow = pid / k;                       // h * n + i
-            const int64_t slot = pid - qrow * k;
-            const int64_t part = slot_base + (qrow - h * n - rr * range) * k + slot;
-            if (has) {
-                const uint16_t *src = a.q + qrow * D;
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    const int sub = c >> 3, cc = c & 7;
-                    tc::cp_async16(sQ + sub * kTile * 128 + t * 128 + ((cc ^ (t & 7)) << 4), src + c * 8);
-                }
-            }
-            tc::cp_async_wait_all();
+    if (warp == kWarpProducer) {
+        // ------------------------------------------------------- producer
+        const int n_fine = *a.w.n_fine;
+        int g = 0, item_idx = 0, pend = 0;
+        bool ok = true;
+        for (;;) {
+            int it = 0;
+            if (lane == 0) it = atomicAdd(a.fine_head, 1);
+            it = __shfl_sync(kFull, it, 0);
+            bool done = it >= n_fine || !ok;
+            // every issued gather is published before anything that may wait
+            // on other CTAs (merges of an earlier range need these tiles)
+            tc::cp_async_wait_pending<0>();
             tc::fence_proxy_async_smem();
-            __syncthreads();
-            // 2. S = Q . K_b^T
-            if (t == 0) {
-                if (first_tile) ok = tc::mbar_wait(bar_kv, kv_phase, status);
-                tc::tc_fence_after();
-                if (ok) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
-                        const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
-                        tc::mma_bf16(tmem_s, tc::smem_desc_sw128(aq + off_q, 1024),
-                                     tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+            for (; pend > 0; --pend) tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
+            int64_t bin = 0, rg = 0, h = 0, b = 0;
+            int32_t first = 0, end = 0;
+            const int32_t *ent = nullptr;
+            if (!done) {
+                const int2 item = a.w.fine_items[it];
+                bin = item.x;
+                first = item.y;
+                rg = bin / nb;
+                h = rg / nranges;
+                b = bin % nb;
+                const int32_t off = a.w.offsets[bin];
+                end = min(a.w.offsets[bin + 1] - off, first + a.p.item_pairs);
+                ent = a.w.entries + off;
+                if (rg >= kPartialRing) {
+                    int got = 1;
+                    if (lane == 0)
+                        got = wait_counter(a.merge_done + (rg - kPartialRing),
+                                           a.w.range_merges[rg - kPartialRing], status);
+                    got = __shfl_sync(kFull, got, 0);
+                    if (!got) {
+                        ok = false;
+                        done = true;
                     }
-                    tc::mma_commit(bar_mma);
                 }
             }
-            first_tile = false;
-            ok = __syncthreads_and(ok);
-            if (!ok) break;
-            ok = tc::mbar_wait(bar_mma, mma_phase, status);
-            mma_phase ^= 1;
-            tc::tc_fence_after();
-            // 3. softmax of the row (scores in base-2 units)
-            float m2 = -INFINITY, l = 0.f;
-            {
-                uint32_t sv[2][32];
-                tc::tmem_ld32(tmem_s + lane_off, sv[0]);
-                tc::tmem_ld32(tmem_s + lane_off + 32, sv[1]);
-                tc::tmem_ld_wait();
-                float s2[64];
+            if (done) {
+                const int slot = g % kNT;
+                bool w = true;
+                if (g >= kNT) w = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
+                w = __all_sync(kFull, w);
+                if (w && lane == 0) ti[slot].end = 1;
+                __syncwarp();
+                if (w) tc::mbar_arrive(bars + C::bTiFull + slot);
+                break;
+            }
+            const int ib = item_idx & 1;
+            int got = 1;
+            if (lane == 0) {
+                if (item_idx >= 2)
+                    got = tc::mbar_wait(bars + C::bKvFree + ib, ((item_idx >> 1) - 1) & 1, status);
+                if (got) {
+                    tc::mbar_arrive_expect_tx(bars + C::bKvFull + ib, 2 * C::kKBytes);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) s2[j] = __uint_as_float(sv[j >> 5][j & 31]);
-                if (keys_valid < 64) {                    // ragged last block only
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (j >= keys_valid) s2[j] = -INFINITY;
-                }
-                float mraw = s2[0];
-#pragma unroll
-                for (int j = 1; j < 64; ++j) mraw = fmaxf(mraw, s2[j]);
-                m2 = mraw * a.scale_log2;                 // scale > 0 keeps the argmax
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    s2[j] = ex2(fmaf(s2[j], a.scale_log2, -m2));
-                    l += s2[j];
-                }
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = make_uint4(pack_bf16x2(s2[8 * c + 0], s2[8 * c + 1]),
-                                               pack_bf16x2(s2[8 * c + 2], s2[8 * c + 3]),
-                                               pack_bf16x2(s2[8 * c + 4], s2[8 * c + 5]),
-                                               pack_bf16x2(s2[8 * c + 6], s2[8 * c + 7]));
-                    *reinterpret_cast<uint4 *>(sP + t * 128 + ((c ^ (t & 7)) << 4)) = v;
+                    for (int sub = 0; sub < C::kSub; ++sub) {
+                        tc::tma_load_3d(sm + C::oK + ib * C::kKBytes + sub * kB * 128, &tm_k,
+                                        bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
+                        tc::tma_load_3d(sm + C::oV + ib * C::kKBytes + sub * kB * 128, &tm_v,
+                                        bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
+                    }
                 }
             }
-            tc::fence_proxy_async_smem();
-            tc::tc_fence_before();
-            __syncthreads();
-            // 4. O = P . V_b
-            if (t == 0 && ok) {
+            if (!__shfl_sync(kFull, got, 0)) {
+                ok = false;
+                continue;                         // publishes the end marker
+            }
+            // the item's pair ids: at most 4 tiles x 4 rows per lane
+            int32_t my_pid[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int32_t p = first + (e >> 2) * kTile + lane + 32 * (e & 3);
+                my_pid[e] = p < end ? __ldg(ent + p) : 0;
+            }
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) {
+                const int32_t p0 = first + tt * kTile;
+                if (p0 >= end || !ok) break;
+                const int s = g % C::kNQ, slot = g % kNT;
+                if (g >= C::kNQ) ok = tc::mbar_wait(bars + C::bQFree + s, ((g / C::kNQ) - 1) & 1, status);
+                if (ok && g >= kNT) ok = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
+                ok = __all_sync(kFull, ok);
+                if (!ok) break;
+                const int cnt = min(kTile, end - p0);
+                uint8_t *sQ = sm + C::oQ + s * C::kQBytes;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int r = lane + 32 * qq;
+                    if (r < cnt) {
+                        const int32_t pid = my_pid[tt * 4 + qq];
+                        pids[slot * kTile + r] = pid;
+                        const uint16_t *src = a.q + int64_t(pid / k) * D;
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c)
+                            tc::cp_async16(sQ + (c >> 3) * kTile * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4),
+                                           src + c * 8);
+                    }
+                }
+                tc::cp_async_commit();
+                if (lane == 0) {
+                    TileInfo x;
+                    x.bin = int32_t(bin);
+                    x.p0 = p0;
+                    x.count = cnt;
+                    x.item = item_idx;
+                    x.last = p0 + kTile >= end;
+                    x.rg = int32_t(rg);
+                    x.end = 0;
+                    x.pad = 0;
+                    ti[slot] = x;
+                }
+                __syncwarp();
+                tc::mbar_arrive(bars + C::bTiFull + slot);
+                ++g;
+                ++pend;
+                if (pend > C::kLag) {
+                    // the oldest gather has landed: make it visible to the MMA
+                    tc::cp_async_wait_pending<C::kLag>();
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
+                    --pend;
+                }
+            }
+            ++item_idx;
+        }
+        tc::cp_async_wait_pending<0>();
+        tc::fence_proxy_async_smem();
+        for (; pend > 0; --pend) tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
+            int g = 0, cur_item = -1;
+            int pg = -1, pib = 0;
+            bool plast = false, ok = true;
+            auto issue_pv = [&]() {
+                const int pj = pg & 1;
+                bool w = tc::mbar_wait(bars + C::bPFull + pj, (pg >> 1) & 1, status);
+                if (w && pg >= 2) w = tc::mbar_wait(bars + C::bOFree + pj, ((pg >> 1) - 1) & 1, status);
+                if (!w) return false;
                 tc::tc_fence_after();
+                const uint32_t ap = tc::smem_u32(sm + C::oP + pj * C::kPBytes);
+                const uint32_t av = tc::smem_u32(sm + C::oV + pib * C::kKBytes);
 #pragma unroll
                 for (int kk = 0; kk < kB / 16; ++kk)
-                    tc::mma_bf16(tmem_o, tc::smem_desc_sw128(ap + kk * 32, 1024),
+                    tc::mma_bf16(tmem + C::cO + uint32_t(pj * D), tc::smem_desc_sw128(ap + kk * 32, 1024),
                                  tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
                                  kk > 0);
-                tc::mma_commit(bar_mma);
+                tc::mma_commit(bars + C::bOFull + pj);
+                tc::mma_commit(bars + C::bPFree + pj);
+                if (plast) tc::mma_commit(bars + C::bKvFree + pib);
+                return true;
+            };
+            for (;;) {
+                const int slot = g % kNT;
+                if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) {
+                    ok = false;
+                    break;
+                }
+                const int32_t x_end = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
+                if (x_end) break;
+                const int32_t x_item = reinterpret_cast<volatile TileInfo *>(ti + slot)->item;
+                const int32_t x_last = reinterpret_cast<volatile TileInfo *>(ti + slot)->last;
+                const int s = g % C::kNQ, j = g & 1, ib = x_item & 1;
+                bool w = true;
+                if (x_item != cur_item) {
+                    cur_item = x_item;
+                    w = tc::mbar_wait(bars + C::bKvFull + ib, (x_item >> 1) & 1, status);
+                }
+                if (w) w = tc::mbar_wait(bars + C::bQFull + s, (g / C::kNQ) & 1, status);
+                if (w && g >= 2) w = tc::mbar_wait(bars + C::bSFree + j, ((g >> 1) - 1) & 1, status);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t aq = tc::smem_u32(sm + C::oQ + s * C::kQBytes);
+                const uint32_t ak = tc::smem_u32(sm + C::oK + ib * C::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
+                    const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
+                    tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
+                                 tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+                }
+                tc::mma_commit(bars + C::bSFull + j);
+                tc::mma_commit(bars + C::bQFree + s);
+                if (pg >= 0 && !issue_pv()) {
+                    ok = false;
+                    break;
+                }
+                pg = g;
+                pib = ib;
+                plast = x_last != 0;
+                ++g;
             }
-            if (ok) ok = tc::mbar_wait(bar_mma, mma_phase, status);
-            mma_phase ^= 1;
+            if (ok && pg >= 0) issue_pv();
+        }
+        __syncwarp();
+    } else if (warp < kWarpEpi) {
+        // -------------------------------------------------------- softmax
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        for (int g = 0;; ++g) {
+            const int slot = g % kNT, j = g & 1;
+            if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
+            const int32_t end_flag = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
+            if (end_flag) break;
+            const int64_t bin = reinterpret_cast<volatile TileInfo *>(ti + slot)->bin;
+            if (!tc::mbar_wait(bars + C::bSFull + j, (g >> 1) & 1, status)) break;
             tc::tc_fence_after();
-            // 5. the pair's partial state
-            const float inv_l = 1.f / l;
+            uint32_t sv[2][32];
+            tc::tmem_ld32(tmem + uint32_t(j * kB) + lane_off, sv[0]);
+            tc::tmem_ld32(tmem + uint32_t(j * kB + 32) + lane_off, sv[1]);
+            tc::tmem_ld_wait();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bars + C::bSFree + j);
+            const int64_t keys_valid = n - (bin % nb) * kB;
+            float s2[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) s2[c] = __uint_as_float(sv[c >> 5][c & 31]);
+            if (keys_valid < 64) {                    // ragged last block only
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c >= keys_valid) s2[c] = -INFINITY;
+            }
+            float mraw = s2[0];
+#pragma unroll
+            for (int c = 1; c < 64; ++c) mraw = fmaxf(mraw, s2[c]);
+            const float m2 = mraw * a.scale_log2;     // scale > 0 keeps the argmax
+            float l = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                s2[c] = ex2(fmaf(s2[c], a.scale_log2, -m2));
+                l += s2[c];
+            }
+            bool w = true;
+            if (g >= 2) {
+                w = tc::mbar_wait(bars + C::bPFree + j, ((g >> 1) - 1) & 1, status);
+                if (w) w = tc::mbar_wait(bars + C::bMlFree + j, ((g >> 1) - 1) & 1, status);
+            }
+            if (!w) break;
+            uint8_t *sP = sm + C::oP + j * C::kPBytes;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 v = make_uint4(pack_bf16x2(s2[8 * c + 0], s2[8 * c + 1]),
+                                           pack_bf16x2(s2[8 * c + 2], s2[8 * c + 3]),
+                                           pack_bf16x2(s2[8 * c + 4], s2[8 * c + 5]),
+                                           pack_bf16x2(s2[8 * c + 6], s2[8 * c + 7]));
+                *reinterpret_cast<uint4 *>(sP + row * 128 + ((c ^ (row & 7)) << 4)) = v;
+            }
+            ml[j * kTile + row] = make_float2(m2, l);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(bars + C::bPFull + j);
+        }
+    } else if (warp < kWarpMerge) {
+        // ------------------------------------------------------- epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int et = (warp - kWarpEpi) * 32 + lane;
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        for (int g = 0;; ++g) {
+            const int slot = g % kNT, j = g & 1;
+            if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
+            const int32_t x_end = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
+            if (x_end) break;
+            const int32_t x_count = reinterpret_cast<volatile TileInfo *>(ti + slot)->count;
+            const int32_t x_rg = reinterpret_cast<volatile TileInfo *>(ti + slot)->rg;
+            if (!tc::mbar_wait(bars + C::bOFull + j, (g >> 1) & 1, status)) break;
+            if (!tc::mbar_wait(bars + C::bPFull + j, (g >> 1) & 1, status)) break;
+            tc::tc_fence_after();
+            const float2 mlv = ml[j * kTile + row];
+            tc::mbar_arrive(bars + C::bMlFree + j);
+            const bool has = row < x_count;
+            int64_t part = 0;
+            if (has) {
+                const int32_t pid = pids[slot * kTile + row];
+                const int64_t qrow = pid / k;
+                const int64_t s = pid - qrow * k;
+                const int64_t h = x_rg / nranges, rr = x_rg % nranges;
+                part = (x_rg % kPartialRing) * ring_stride + (qrow - h * n - rr * range) * kpad + s;
+            }
+            const float inv_l = 1.f / mlv.y;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
                 uint32_t ov[32];
-                tc::tmem_ld32(tmem_o + lane_off + c0, ov);
+                tc::tmem_ld32(tmem + C::cO + uint32_t(j * D + c0) + lane_off, ov);
                 tc::tmem_ld_wait();
                 if (has) {
                     uint4 *dst = reinterpret_cast<uint4 *>(a.part_o + part * D + c0);
@@ -405,22 +563,60 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 4 : 2) fine_bm_kernel(
                             pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l));
                 }
             }
-            if (has) a.part_lse[part] = m2 + __log2f(l);
             tc::tc_fence_before();
-            ok = __syncthreads_and(ok);   // keeps the loop conditions uniform
+            tc::mbar_arrive(bars + C::bOFree + j);
+            if (has) a.part_lse[part] = mlv.x + __log2f(mlv.y);
+            __threadfence();
+            tc::named_bar_sync(kBarEpi, 128);
+            if (et == 0) {
+                atomicAdd(a.range_done + x_rg, x_count);
+                tc::mbar_arrive(bars + C::bTiFree + slot);
+            }
         }
-        kv_phase ^= 1;
-        // publish: this item's partial states are written
-        __threadfence();
-        __syncthreads();
-        if (t == 0 && ok) atomicAdd(a.range_done + rg, end - item.y);
+    } else {
+        // ---------------------------------------------------------- merge
+        const int mt = (warp - kWarpMerge) * 32 + lane;
+        const int mw = warp - kWarpMerge;
+        const int n_merge = *a.w.n_merge;
+        const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;
+        for (;;) {
+            if (mt == 0) s_merge[0] = atomicAdd(a.merge_head, 1);
+            tc::named_bar_sync(kBarMerge, 128);
+            const int it = s_merge[0];
+            tc::named_bar_sync(kBarMerge, 128);
+            if (it >= n_merge) break;
+            const int2 item = a.w.merge_items[it];
+            const int64_t rg = item.x;
+            if (mt == 0) {
+                const bool got = wait_counter(a.range_done + rg, a.w.range_total[rg], status);
+                __threadfence();
+                s_merge[1] = got;
+            }
+            tc::named_bar_sync(kBarMerge, 128);
+            if (!s_merge[1]) break;
+            const int64_t h = rg / nranges, rr = rg % nranges;
+            const int64_t i_begin = rr * range + item.y;
+            const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
+            const int64_t slot_base = (rg % kPartialRing) * ring_stride;
+            // 16 queries per pass: 4 warps x 4 groups of 8 lanes
+            for (int64_t i0 = i_begin; i0 < i_end; i0 += 16) {
+                const int64_t i = i0 + mw * 4 + (lane >> 3);
+                const bool act = i < i_end;
+                const int64_t ic = act ? i : i_begin;
+                merge_group<D>(act, h * n + ic, slot_base + (ic - rr * range) * kpad, a.list, k, nb,
+                               full_valid, lane, a.part_o, a.part_lse, a.out);
+            }
+            __threadfence();
+            tc::named_bar_sync(kBarMerge, 128);
+            if (mt == 0) atomicAdd(a.merge_done + rg, 1);
+        }
     }
 
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kWarpMma) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, S::kTmemCols);
+        tc::tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
@@ -452,30 +648,14 @@ bool make_rows_map(CUtensorMap *m, const void *base, int64_t bh, int64_t n, int 
 template <int D>
 cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorMap &mv,
                      cudaStream_t st) {
-    using S = BmSmem<D>;
-    auto kern = fine_bm_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kTotal);
+    using C = Cfg<D>;
+    auto kern = fine_ws_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal);
     if (e != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
-        return e;
-    int dev = 0, sms = 0, smem_sm = 0;
+    int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
-        return e;
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    // resident CTAs per SM: shared memory (+1 KB reserved per CTA), TMEM and
-    // registers (allocated per warp in units of 256)
-    int per_sm = smem_sm / (S::kTotal + 1024);
-    const int tmem_limit = int(512 / S::kTmemCols);
-    const int warp_regs = (fa.numRegs * 32 + 255) / 256 * 256;
-    const int reg_limit = 65536 / (warp_regs * (kThreads / 32));
-    if (per_sm > tmem_limit) per_sm = tmem_limit;
-    if (per_sm > reg_limit) per_sm = reg_limit;
-    if (per_sm < 1) per_sm = 1;
-    kern<<<sms * per_sm, kThreads, S::kTotal, st>>>(mk, mv, a);
+    kern<<<sms, kThreads, C::kTotal, st>>>(mk, mv, a);   // one CTA per SM
     return cudaGetLastError();
 }
 

@@ -99,16 +99,16 @@ __device__ __forceinline__ void block_scan2(int64_t &a, int64_t &b, int64_t *wa,
 
 // One CTA of 1024 threads.  Builds the CSR offsets over the bins
 // (range-major: bin = range * nb + block, range = head * nranges + r) and
-// the work list of the fine stage: per range its fine items {bin, first
-// pair} (at most item_pairs pairs each), and its merge items {-(range+1),
-// first query} (qm queries each) placed right after the NEXT range's fine
-// items, so that merging range r overlaps the fine work of range r+1.
+// the two work lists of the fine stage: fine items {bin, first pair} (at
+// most item_pairs pairs each) in bin order, and merge items {range, first
+// query} (qm queries each) in range order.
 __global__ void __launch_bounds__(1024) scan_kernel(
     const int32_t *__restrict__ counts, int64_t nb, int64_t nr, int64_t nranges, int64_t range,
     int64_t n, int32_t item_pairs, int32_t qm, int32_t *__restrict__ offsets,
     int32_t *__restrict__ fitem_off, int32_t *__restrict__ fpre, int32_t *__restrict__ mpre,
     int32_t *__restrict__ range_total, int32_t *__restrict__ range_merges,
-    int2 *__restrict__ items, int32_t *__restrict__ n_items) {
+    int2 *__restrict__ fine_items, int2 *__restrict__ merge_items, int32_t *__restrict__ n_fine,
+    int32_t *__restrict__ n_merge) {
     __shared__ int64_t wa[32], wb[32];
     const int t = threadIdx.x;
     const int64_t nbins = nr * nb;
@@ -160,20 +160,20 @@ __global__ void __launch_bounds__(1024) scan_kernel(
         fpre[nr] = int32_t(fo);
         fpre[nr + 1] = int32_t(fo);
         mpre[nr] = int32_t(mo);
-        *n_items = int32_t(fo + mo);
+        *n_fine = int32_t(fo);
+        *n_merge = int32_t(mo);
     }
     __syncthreads();
-    // 3. the work list
+    // 3. the work lists: fine items in bin order, merge items in range order
     for (int64_t e = e0; e < e1; ++e) {
-        const int64_t r = e / nb;
         const int64_t c = counts[e];
-        int64_t pos = fitem_off[e] + (r >= 1 ? mpre[r - 1] : 0);
-        for (int64_t f = 0; f < c; f += item_pairs) items[pos++] = make_int2(int(e), int(f));
+        int64_t pos = fitem_off[e];
+        for (int64_t f = 0; f < c; f += item_pairs) fine_items[pos++] = make_int2(int(e), int(f));
     }
     for (int64_t r = r0; r < r1; ++r) {
-        int64_t pos = fpre[i64min(r + 2, nr)] + mpre[r];
+        int64_t pos = mpre[r];
         for (int64_t j = 0; j < range_merges[r]; ++j)
-            items[pos++] = make_int2(int(-(r + 1)), int(j * qm));
+            merge_items[pos++] = make_int2(int(r), int(j * qm));
     }
 }
 
@@ -239,8 +239,9 @@ InvertPlan invert_plan(int64_t bh, int64_t n, int64_t nb, int32_t k) {
     p.nbins = p.nr * nb;
     p.item_pairs = kFineBmItemPairs;
     p.qm = kMergeQueries;
-    p.items_cap = p.nbins + (bh * n * k + p.item_pairs - 1) / p.item_pairs +
-                  p.nr * ((p.range + p.qm - 1) / p.qm);
+    p.fine_cap = p.nbins + (bh * n * k + p.item_pairs - 1) / p.item_pairs;
+    p.merge_cap = p.nr * ((p.range + p.qm - 1) / p.qm);
+    p.kpad = (k + 3) / 4 * 4;
     return p;
 }
 
@@ -263,7 +264,8 @@ cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb
                                                status);
     scan_kernel<<<1, 1024, 0, st>>>(w.counts, nb, p.nr, p.nranges, p.range, n, p.item_pairs, p.qm,
                                     w.offsets, w.fitem_off, w.fpre, w.mpre, w.range_total,
-                                    w.range_merges, w.items, w.n_items);
+                                    w.range_merges, w.fine_items, w.merge_items, w.n_fine,
+                                    w.n_merge);
     scatter_kernel<uint16_t><<<grid, kThreads, 2 * smem1, st>>>(list, n, nb, k, p.range,
                                                                 p.nranges, w.offsets, w.cursors,
                                                                 w.entries, out_bf16, d);

@@ -71,17 +71,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
+// Bounded wait for the phase with the given parity to complete.  Gives up
+// after kWaitLimitNs, or as soon as another wait in the grid has (the status
+// word then already holds BSA_ERR_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
-            report_status(status, kStatusTimeout);
-            return false;
+        if ((spin & 255u) == 0) {
+            if (status != nullptr && *reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout)
+                return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                report_status(status, kStatusTimeout);
+                return false;
+            }
         }
     }
+}
+
+// Named barrier among `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ----------------------------------------------------------------- TMA
@@ -165,6 +176,14 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N committed groups of this thread are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
