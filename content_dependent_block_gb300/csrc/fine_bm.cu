@@ -8,8 +8,10 @@
 // selected the block.  One persistent CTA per SM runs five warp roles that
 // hand work to each other through mbarrier rings in shared memory:
 //
-//   producer  (warp 0)      takes fine items (one bin, <= 512 pairs) from a
-//                           global queue; loads K_b, V_b by TMA (128-byte
+//   prefetch  (warp 14)     takes fine items (one bin, <= 512 pairs) from a
+//                           global queue and stages each item's descriptor
+//                           and pair ids in a shared-memory ring
+//   producer  (warp 0)      per staged item: loads K_b, V_b by TMA (128-byte
 //                           swizzle, double-buffered per item) and gathers the
 //                           128 query rows of each tile with cp.async into a
 //                           ring of Q stages; publishes per-tile info
@@ -46,14 +48,22 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kB = 64;                   // key block handled by this kernel
 constexpr int kNT = 8;                   // tile-info ring
-constexpr int kWarps = 14;
+constexpr int kNI = 4;                   // staged fine-item ring
+constexpr int kItemMax = 512;            // pairs per fine item (kFineBmItemPairs)
+constexpr int kWarps = 15;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 6, kWarpMerge = 10;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 6, kWarpMerge = 10, kWarpFetch = 14;
 constexpr uint32_t kBarEpi = 1, kBarMerge = 2;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TileInfo {
     int32_t bin, p0, count, item, last, rg, end, pad;
+};
+
+// A fine item staged by the prefetcher: descriptor plus all its pair ids.
+struct StagedItem {
+    int32_t bin, first, end, rg, h, b, valid, pad;
+    int32_t pid[kItemMax];
 };
 
 template <int D>
@@ -71,7 +81,8 @@ struct Cfg {
     static constexpr int oML = oV + 2 * kKBytes;           // float2 [2][128]
     static constexpr int oPid = oML + 2 * kTile * 8;       // int32  [kNT][128]
     static constexpr int oTi = oPid + kNT * kTile * 4;     // TileInfo [kNT]
-    static constexpr int oBar = oTi + kNT * 32;
+    static constexpr int oItem = oTi + kNT * 32;           // StagedItem [kNI]
+    static constexpr int oBar = oItem + kNI * int(sizeof(StagedItem));
     enum {
         bQFull = 0,
         bQFree = bQFull + kNQ,
@@ -86,7 +97,9 @@ struct Cfg {
         bMlFree = bOFree + 2,
         bTiFull = bMlFree + 2,
         bTiFree = bTiFull + kNT,
-        bCount = bTiFree + kNT
+        bItFull = bTiFree + kNT,
+        bItFree = bItFull + kNI,
+        bCount = bItFree + kNI
     };
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
@@ -212,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::oBar);
     TileInfo *ti = reinterpret_cast<TileInfo *>(sm + C::oTi);
+    StagedItem *items = reinterpret_cast<StagedItem *>(sm + C::oItem);
     int32_t *pids = reinterpret_cast<int32_t *>(sm + C::oPid);
     float2 *ml = reinterpret_cast<float2 *>(sm + C::oML);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::oMisc);
@@ -241,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::mbar_init(bars + C::bTiFull + i, 32);
             tc::mbar_init(bars + C::bTiFree + i, 1);
         }
+        for (int i = 0; i < kNI; ++i) {
+            tc::mbar_init(bars + C::bItFull + i, 32);
+            tc::mbar_init(bars + C::bItFree + i, 32);
+        }
         tc::fence_barrier_init();
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
@@ -259,47 +277,92 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
     const int64_t kpad = a.p.kpad;
     const int64_t ring_stride = range * kpad;
 
-    if (warp == kWarpProducer) {
-        // ------------------------------------------------------- producer
+    if (warp == kWarpFetch) {
+        // ----------------------------------------------------- prefetcher
+        // dequeues fine items and stages descriptor + pair ids in shared memory
         const int n_fine = *a.w.n_fine;
-        int g = 0, item_idx = 0, pend = 0;
-        bool ok = true;
-        for (;;) {
+        for (int u = 0;; ++u) {
+            const int slot = u % kNI;
+            if (u >= kNI && !tc::mbar_wait(bars + C::bItFree + slot, ((u / kNI) - 1) & 1, status)) break;
             int it = 0;
             if (lane == 0) it = atomicAdd(a.fine_head, 1);
             it = __shfl_sync(kFull, it, 0);
-            bool done = it >= n_fine || !ok;
-            // every issued gather is published before anything that may wait
-            // on other CTAs (merges of an earlier range need these tiles)
+            StagedItem *si = items + slot;
+            const bool valid = it < n_fine;
+            if (valid) {
+                const int2 item = a.w.fine_items[it];
+                const int64_t bin = item.x;
+                const int32_t off = a.w.offsets[bin];
+                const int32_t end = min(a.w.offsets[bin + 1] - off, item.y + a.p.item_pairs);
+                const int32_t *ent = a.w.entries + off;
+                int32_t v[kItemMax / 32];
+#pragma unroll
+                for (int e = 0; e < kItemMax / 32; ++e) {
+                    const int32_t p = item.y + e * 32 + lane;
+                    v[e] = p < end ? __ldg(ent + p) : 0;
+                }
+#pragma unroll
+                for (int e = 0; e < kItemMax / 32; ++e) si->pid[e * 32 + lane] = v[e];
+                if (lane == 0) {
+                    const int64_t rg = bin / nb;
+                    si->bin = int32_t(bin);
+                    si->first = item.y;
+                    si->end = end;
+                    si->rg = int32_t(rg);
+                    si->h = int32_t(rg / nranges);
+                    si->b = int32_t(bin % nb);
+                }
+            }
+            if (lane == 0) si->valid = valid ? 1 : 0;
+            __syncwarp();
+            tc::mbar_arrive(bars + C::bItFull + slot);
+            if (!valid) break;
+        }
+    } else if (warp == kWarpProducer) {
+        // ------------------------------------------------------- producer
+        int g = 0, item_idx = 0, pend = 0;
+        bool ok = true;
+        // publish every issued gather (needed before any wait that another
+        // role or CTA can only satisfy by consuming those tiles)
+        auto flush = [&]() {
             tc::cp_async_wait_pending<0>();
             tc::fence_proxy_async_smem();
             for (; pend > 0; --pend) tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
+        };
+        for (int u = 0;; ++u) {
+            const int islot = u % kNI;
+            if (!__all_sync(kFull, tc::mbar_try_wait(bars + C::bItFull + islot, (u / kNI) & 1))) {
+                flush();
+                if (!tc::mbar_wait(bars + C::bItFull + islot, (u / kNI) & 1, status)) ok = false;
+            }
+            ok = __all_sync(kFull, ok);
+            const StagedItem *si = items + islot;
+            bool done = !ok || !si->valid;
             int64_t bin = 0, rg = 0, h = 0, b = 0;
             int32_t first = 0, end = 0;
-            const int32_t *ent = nullptr;
             if (!done) {
-                const int2 item = a.w.fine_items[it];
-                bin = item.x;
-                first = item.y;
-                rg = bin / nb;
-                h = rg / nranges;
-                b = bin % nb;
-                const int32_t off = a.w.offsets[bin];
-                end = min(a.w.offsets[bin + 1] - off, first + a.p.item_pairs);
-                ent = a.w.entries + off;
+                bin = si->bin;
+                first = si->first;
+                end = si->end;
+                rg = si->rg;
+                h = si->h;
+                b = si->b;
                 if (rg >= kPartialRing) {
-                    int got = 1;
-                    if (lane == 0)
-                        got = wait_counter(a.merge_done + (rg - kPartialRing),
-                                           a.w.range_merges[rg - kPartialRing], status);
-                    got = __shfl_sync(kFull, got, 0);
-                    if (!got) {
-                        ok = false;
-                        done = true;
+                    const int32_t *cnt = a.merge_done + (rg - kPartialRing);
+                    const int32_t need = a.w.range_merges[rg - kPartialRing];
+                    if (__shfl_sync(kFull, lane == 0 ? ld_acquire(cnt) : 0, 0) < need) {
+                        flush();
+                        int got = 1;
+                        if (lane == 0) got = wait_counter(cnt, need, status);
+                        if (!__shfl_sync(kFull, got, 0)) {
+                            ok = false;
+                            done = true;
+                        }
                     }
                 }
             }
             if (done) {
+                flush();
                 const int slot = g % kNT;
                 bool w = true;
                 if (g >= kNT) w = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
@@ -310,36 +373,27 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 break;
             }
             const int ib = item_idx & 1;
-            int got = 1;
-            if (lane == 0) {
-                if (item_idx >= 2)
-                    got = tc::mbar_wait(bars + C::bKvFree + ib, ((item_idx >> 1) - 1) & 1, status);
-                if (got) {
-                    tc::mbar_arrive_expect_tx(bars + C::bKvFull + ib, 2 * C::kKBytes);
-#pragma unroll
-                    for (int sub = 0; sub < C::kSub; ++sub) {
-                        tc::tma_load_3d(sm + C::oK + ib * C::kKBytes + sub * kB * 128, &tm_k,
-                                        bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
-                        tc::tma_load_3d(sm + C::oV + ib * C::kKBytes + sub * kB * 128, &tm_v,
-                                        bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
-                    }
+            if (item_idx >= 2 &&
+                !__all_sync(kFull, tc::mbar_try_wait(bars + C::bKvFree + ib, ((item_idx >> 1) - 1) & 1))) {
+                flush();
+                ok = tc::mbar_wait(bars + C::bKvFree + ib, ((item_idx >> 1) - 1) & 1, status);
+                ok = __all_sync(kFull, ok);
+                if (!ok) {
+                    tc::mbar_arrive(bars + C::bItFree + islot);
+                    continue;                     // publishes the end marker
                 }
             }
-            if (!__shfl_sync(kFull, got, 0)) {
-                ok = false;
-                continue;                         // publishes the end marker
-            }
-            // the item's pair ids: at most 4 tiles x 4 rows per lane
-            int32_t my_pid[16];
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(bars + C::bKvFull + ib, 2 * C::kKBytes);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int32_t p = first + (e >> 2) * kTile + lane + 32 * (e & 3);
-                my_pid[e] = p < end ? __ldg(ent + p) : 0;
+                for (int sub = 0; sub < C::kSub; ++sub) {
+                    tc::tma_load_3d(sm + C::oK + ib * C::kKBytes + sub * kB * 128, &tm_k,
+                                    bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
+                    tc::tma_load_3d(sm + C::oV + ib * C::kKBytes + sub * kB * 128, &tm_v,
+                                    bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
+                }
             }
-#pragma unroll
-            for (int tt = 0; tt < 4; ++tt) {
-                const int32_t p0 = first + tt * kTile;
-                if (p0 >= end || !ok) break;
+            for (int32_t p0 = first; ok && p0 < end; p0 += kTile) {
                 const int s = g % C::kNQ, slot = g % kNT;
                 if (g >= C::kNQ) ok = tc::mbar_wait(bars + C::bQFree + s, ((g / C::kNQ) - 1) & 1, status);
                 if (ok && g >= kNT) ok = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
@@ -351,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 for (int qq = 0; qq < 4; ++qq) {
                     const int r = lane + 32 * qq;
                     if (r < cnt) {
-                        const int32_t pid = my_pid[tt * 4 + qq];
+                        const int32_t pid = si->pid[p0 - first + r];
                         pids[slot * kTile + r] = pid;
                         const uint16_t *src = a.q + int64_t(pid / k) * D;
 #pragma unroll
@@ -385,11 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     --pend;
                 }
             }
+            __syncwarp();
+            tc::mbar_arrive(bars + C::bItFree + islot);
             ++item_idx;
         }
-        tc::cp_async_wait_pending<0>();
-        tc::fence_proxy_async_smem();
-        for (; pend > 0; --pend) tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
+        flush();
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
