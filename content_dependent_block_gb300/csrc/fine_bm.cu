@@ -472,9 +472,21 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             };
             for (;;) {
                 const int slot = g % kNT;
-                if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) {
-                    ok = false;
-                    break;
+                if (!tc::mbar_try_wait(bars + C::bTiFull + slot, (g / kNT) & 1)) {
+                    // no next tile yet: never keep a tile's P.V back while
+                    // waiting (the producer may be waiting on merges that
+                    // need that tile's partial states)
+                    if (pg >= 0) {
+                        if (!issue_pv()) {
+                            ok = false;
+                            break;
+                        }
+                        pg = -1;
+                    }
+                    if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 const int32_t x_end = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
                 if (x_end) break;
