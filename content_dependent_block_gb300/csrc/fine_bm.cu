@@ -13,8 +13,9 @@
 //                           and pair ids in a shared-memory ring
 //   producer  (warp 0)      per staged item: loads K_b, V_b by TMA (128-byte
 //                           swizzle, double-buffered per item) and gathers the
-//                           128 query rows of each tile with cp.async into a
-//                           ring of Q stages; publishes per-tile info
+//                           128 query rows of each tile with TMA gather4 (four
+//                           rows per instruction) into a ring of Q stages;
+//                           publishes per-tile info
 //   MMA       (warp 1)      S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
 //                           one of two TMEM score buffers, then O[j] = P . V_b
 //                           (N = d, V MN-major) into one of two TMEM outputs;
@@ -70,16 +71,16 @@ template <int D>
 struct Cfg {
     static constexpr int kSub = D / 64;
     static constexpr int kNQ = D == 64 ? 4 : 3;            // Q stages
-    static constexpr int kLag = kNQ - 2;                   // gathers left unpublished
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kPBytes = kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int oQ = 0;
     static constexpr int oP = oQ + kNQ * kQBytes;
+    static constexpr int kNKV = D == 64 ? 4 : 2;           // K/V buffers (items in flight)
     static constexpr int oK = oP + 2 * kPBytes;
-    static constexpr int oV = oK + 2 * kKBytes;
-    static constexpr int oML = oV + 2 * kKBytes;           // float2 [2][128]
-    static constexpr int oPid = oML + 2 * kTile * 8;       // int32  [kNT][128]
+    static constexpr int oV = oK + kNKV * kKBytes;
+    static constexpr int oML = oV + kNKV * kKBytes;        // float2 [kNT][128]
+    static constexpr int oPid = oML + kNT * kTile * 8;     // int32  [kNT][128]
     static constexpr int oTi = oPid + kNT * kTile * 4;     // TileInfo [kNT]
     static constexpr int oItem = oTi + kNT * 32;           // StagedItem [kNI]
     static constexpr int oBar = oItem + kNI * int(sizeof(StagedItem));
@@ -87,15 +88,15 @@ struct Cfg {
         bQFull = 0,
         bQFree = bQFull + kNQ,
         bKvFull = bQFree + kNQ,
-        bKvFree = bKvFull + 2,
-        bSFull = bKvFree + 2,
+        bKvFree = bKvFull + kNKV,
+        bSFull = bKvFree + kNKV,
         bSFree = bSFull + 2,
         bPFull = bSFree + 2,
         bPFree = bPFull + 2,
         bOFull = bPFree + 2,
         bOFree = bOFull + 2,
-        bMlFree = bOFree + 2,
-        bTiFull = bMlFree + 2,
+        bMlFull = bOFree + 2,
+        bTiFull = bMlFull + kNT,
         bTiFree = bTiFull + kNT,
         bItFull = bTiFree + kNT,
         bItFree = bItFull + kNI,
@@ -129,6 +130,10 @@ __device__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status) 
     }
 }
 
+__device__ __forceinline__ void red_add_release(int32_t *p, int32_t v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -149,7 +154,6 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
     const int gl = lane & 7;
     const int gbase = lane & ~7;
     bool vs[4];
-    float lse[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int s = gl + 8 * j;
@@ -161,25 +165,16 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
             v = s < full_valid;
         }
         vs[j] = v;
-        lse[j] = v ? __ldcg(part_lse + base + s) : -INFINITY;
     }
-    float M = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    float w[4], L = 0.f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        w[j] = vs[j] ? ex2(lse[j] - M) : 0.f;
-        L += w[j];
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(kFull, L, o);
     float acc[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) acc[c] = 0.f;
+    float M = -INFINITY, L = 0.f;
+    float w[4];
 #pragma unroll
     for (int c0 = 0; c0 < 32; c0 += CH) {
         if (c0 >= k) break;
+        // every load of this chunk (and the slot lse values) in flight at once
         uint4 x[CH][V];
 #pragma unroll
         for (int u = 0; u < CH; ++u) {
@@ -188,6 +183,21 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
             const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (base + s) * D + gl * C);
 #pragma unroll
             for (int e = 0; e < V; ++e) x[u][e] = v ? __ldcg(src + e) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (c0 == 0) {
+            float lse[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) lse[j] = vs[j] ? __ldcg(part_lse + base + gl + 8 * j) : -INFINITY;
+            M = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w[j] = vs[j] ? ex2(lse[j] - M) : 0.f;
+                L += w[j];
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(kFull, L, o);
         }
 #pragma unroll
         for (int u = 0; u < CH; ++u) {
@@ -217,8 +227,8 @@ __device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t b
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const FineBmArgs a) {
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const FineBmArgs a) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -237,20 +247,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNQ; ++i) {
-            tc::mbar_init(bars + C::bQFull + i, 32);
+            tc::mbar_init(bars + C::bQFull + i, 1);
             tc::mbar_init(bars + C::bQFree + i, 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::kNKV; ++i) {
             tc::mbar_init(bars + C::bKvFull + i, 1);
             tc::mbar_init(bars + C::bKvFree + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bars + C::bSFull + i, 1);
             tc::mbar_init(bars + C::bSFree + i, kTile);
             tc::mbar_init(bars + C::bPFull + i, kTile);
             tc::mbar_init(bars + C::bPFree + i, 1);
             tc::mbar_init(bars + C::bOFull + i, 1);
             tc::mbar_init(bars + C::bOFree + i, kTile);
-            tc::mbar_init(bars + C::bMlFree + i, kTile);
         }
+        for (int i = 0; i < kNT; ++i) tc::mbar_init(bars + C::bMlFull + i, kTile);
         for (int i = 0; i < kNT; ++i) {
             tc::mbar_init(bars + C::bTiFull + i, 32);
             tc::mbar_init(bars + C::bTiFree + i, 1);
@@ -260,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::mbar_init(bars + C::bItFree + i, 32);
         }
         tc::fence_barrier_init();
+        tc::prefetch_tensormap(&tm_q);
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
     }
@@ -320,21 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         }
     } else if (warp == kWarpProducer) {
         // ------------------------------------------------------- producer
-        int g = 0, item_idx = 0, pend = 0;
+        int g = 0, item_idx = 0;
         bool ok = true;
-        // publish every issued gather (needed before any wait that another
-        // role or CTA can only satisfy by consuming those tiles)
-        auto flush = [&]() {
-            tc::cp_async_wait_pending<0>();
-            tc::fence_proxy_async_smem();
-            for (; pend > 0; --pend) tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
-        };
         for (int u = 0;; ++u) {
             const int islot = u % kNI;
-            if (!__all_sync(kFull, tc::mbar_try_wait(bars + C::bItFull + islot, (u / kNI) & 1))) {
-                flush();
-                if (!tc::mbar_wait(bars + C::bItFull + islot, (u / kNI) & 1, status)) ok = false;
-            }
+            if (!tc::mbar_wait(bars + C::bItFull + islot, (u / kNI) & 1, status)) ok = false;
             ok = __all_sync(kFull, ok);
             const StagedItem *si = items + islot;
             bool done = !ok || !si->valid;
@@ -348,21 +351,18 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 h = si->h;
                 b = si->b;
                 if (rg >= kPartialRing) {
-                    const int32_t *cnt = a.merge_done + (rg - kPartialRing);
-                    const int32_t need = a.w.range_merges[rg - kPartialRing];
-                    if (__shfl_sync(kFull, lane == 0 ? ld_acquire(cnt) : 0, 0) < need) {
-                        flush();
-                        int got = 1;
-                        if (lane == 0) got = wait_counter(cnt, need, status);
-                        if (!__shfl_sync(kFull, got, 0)) {
-                            ok = false;
-                            done = true;
-                        }
+                    // the ring entry must have been merged by its previous range
+                    int got = 1;
+                    if (lane == 0)
+                        got = wait_counter(a.merge_done + (rg - kPartialRing),
+                                           a.w.range_merges[rg - kPartialRing], status);
+                    if (!__shfl_sync(kFull, got, 0)) {
+                        ok = false;
+                        done = true;
                     }
                 }
             }
             if (done) {
-                flush();
                 const int slot = g % kNT;
                 bool w = true;
                 if (g >= kNT) w = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
@@ -372,11 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 if (w) tc::mbar_arrive(bars + C::bTiFull + slot);
                 break;
             }
-            const int ib = item_idx & 1;
-            if (item_idx >= 2 &&
-                !__all_sync(kFull, tc::mbar_try_wait(bars + C::bKvFree + ib, ((item_idx >> 1) - 1) & 1))) {
-                flush();
-                ok = tc::mbar_wait(bars + C::bKvFree + ib, ((item_idx >> 1) - 1) & 1, status);
+            const int ib = item_idx % C::kNKV;
+            if (item_idx >= C::kNKV) {
+                ok = tc::mbar_wait(bars + C::bKvFree + ib, ((item_idx / C::kNKV) - 1) & 1, status);
                 ok = __all_sync(kFull, ok);
                 if (!ok) {
                     tc::mbar_arrive(bars + C::bItFree + islot);
@@ -400,21 +398,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 ok = __all_sync(kFull, ok);
                 if (!ok) break;
                 const int cnt = min(kTile, end - p0);
+                // lane l gathers rows 4l .. 4l+3 (padding rows repeat row 0)
+                int32_t qr[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 4 * lane + e;
+                    const int32_t pid = si->pid[p0 - first + (r < cnt ? r : 0)];
+                    if (r < cnt) pids[slot * kTile + r] = pid;
+                    qr[e] = pid / k;                        // flat query row h*n + i
+                }
+                if (lane == 0) tc::mbar_arrive_expect_tx(bars + C::bQFull + s, C::kQBytes);
+                __syncwarp();
                 uint8_t *sQ = sm + C::oQ + s * C::kQBytes;
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const int r = lane + 32 * qq;
-                    if (r < cnt) {
-                        const int32_t pid = si->pid[p0 - first + r];
-                        pids[slot * kTile + r] = pid;
-                        const uint16_t *src = a.q + int64_t(pid / k) * D;
-#pragma unroll
-                        for (int c = 0; c < D / 8; ++c)
-                            tc::cp_async16(sQ + (c >> 3) * kTile * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4),
-                                           src + c * 8);
-                    }
-                }
-                tc::cp_async_commit();
+                for (int sub = 0; sub < C::kSub; ++sub)
+                    tc::tma_gather4(sQ + sub * kTile * 128 + lane * 4 * 128, &tm_q, bars + C::bQFull + s,
+                                    sub * 64, qr[0], qr[1], qr[2], qr[3]);
                 if (lane == 0) {
                     TileInfo x;
                     x.bin = int32_t(bin);
@@ -430,102 +429,101 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 __syncwarp();
                 tc::mbar_arrive(bars + C::bTiFull + slot);
                 ++g;
-                ++pend;
-                if (pend > C::kLag) {
-                    // the oldest gather has landed: make it visible to the MMA
-                    tc::cp_async_wait_pending<C::kLag>();
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bars + C::bQFull + (g - pend) % C::kNQ);
-                    --pend;
-                }
             }
             __syncwarp();
             tc::mbar_arrive(bars + C::bItFree + islot);
             ++item_idx;
         }
-        flush();
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
+        // One thread, run as an event loop: issue whichever is ready first,
+        // the S of the next tile or the P.V of the oldest tile whose P is in
+        // shared memory (both in tile order), so no P.V is ever held back.
         if (lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
-            int g = 0, cur_item = -1;
-            int pg = -1, pib = 0;
-            bool plast = false, ok = true;
-            auto issue_pv = [&]() {
-                const int pj = pg & 1;
-                bool w = tc::mbar_wait(bars + C::bPFull + pj, (pg >> 1) & 1, status);
-                if (w && pg >= 2) w = tc::mbar_wait(bars + C::bOFree + pj, ((pg >> 1) - 1) & 1, status);
-                if (!w) return false;
-                tc::tc_fence_after();
-                const uint32_t ap = tc::smem_u32(sm + C::oP + pj * C::kPBytes);
-                const uint32_t av = tc::smem_u32(sm + C::oV + pib * C::kKBytes);
+            int g1 = 0, g2 = 0;                   // next tile for S, next tile for P.V
+            int cur_item = -1, x_item = 0, x_last = 0;
+            int t_ib[4] = {0, 0, 0, 0}, t_last[4] = {0, 0, 0, 0};
+            bool end_seen = false, have_info = false;
+            uint64_t idle_since = 0;
+            for (uint32_t spin = 0;; ++spin) {
+                bool progressed = false;
+                if (g2 < g1) {
+                    const int j = g2 & 1;
+                    if (tc::mbar_try_wait(bars + C::bPFull + j, (g2 >> 1) & 1) &&
+                        (g2 < 2 || tc::mbar_try_wait(bars + C::bOFree + j, ((g2 >> 1) - 1) & 1))) {
+                        tc::tc_fence_after();
+                        const int ib = t_ib[g2 & 3];
+                        const uint32_t ap = tc::smem_u32(sm + C::oP + j * C::kPBytes);
+                        const uint32_t av = tc::smem_u32(sm + C::oV + ib * C::kKBytes);
 #pragma unroll
-                for (int kk = 0; kk < kB / 16; ++kk)
-                    tc::mma_bf16(tmem + C::cO + uint32_t(pj * D), tc::smem_desc_sw128(ap + kk * 32, 1024),
-                                 tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
-                                 kk > 0);
-                tc::mma_commit(bars + C::bOFull + pj);
-                tc::mma_commit(bars + C::bPFree + pj);
-                if (plast) tc::mma_commit(bars + C::bKvFree + pib);
-                return true;
-            };
-            for (;;) {
-                const int slot = g % kNT;
-                if (!tc::mbar_try_wait(bars + C::bTiFull + slot, (g / kNT) & 1)) {
-                    // no next tile yet: never keep a tile's P.V back while
-                    // waiting (the producer may be waiting on merges that
-                    // need that tile's partial states)
-                    if (pg >= 0) {
-                        if (!issue_pv()) {
-                            ok = false;
-                            break;
-                        }
-                        pg = -1;
+                        for (int kk = 0; kk < kB / 16; ++kk)
+                            tc::mma_bf16(tmem + C::cO + uint32_t(j * D), tc::smem_desc_sw128(ap + kk * 32, 1024),
+                                         tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
+                                         kk > 0);
+                        tc::mma_commit(bars + C::bOFull + j);
+                        tc::mma_commit(bars + C::bPFree + j);
+                        if (t_last[g2 & 3]) tc::mma_commit(bars + C::bKvFree + ib);
+                        ++g2;
+                        progressed = true;
                     }
-                    if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) {
-                        ok = false;
+                }
+                if (!end_seen && g1 - g2 < 3) {
+                    const int slot = g1 % kNT;
+                    if (!have_info && tc::mbar_try_wait(bars + C::bTiFull + slot, (g1 / kNT) & 1)) {
+                        const volatile TileInfo *xi = ti + slot;
+                        if (xi->end) {
+                            end_seen = true;
+                        } else {
+                            have_info = true;
+                            x_item = xi->item;
+                            x_last = xi->last;
+                        }
+                        progressed = true;
+                    }
+                    if (have_info) {
+                        const int s = g1 % C::kNQ, j = g1 & 1, ib = x_item % C::kNKV;
+                        bool ready = x_item == cur_item ||
+                                     tc::mbar_try_wait(bars + C::bKvFull + ib, (x_item / C::kNKV) & 1);
+                        ready = ready && tc::mbar_try_wait(bars + C::bQFull + s, (g1 / C::kNQ) & 1);
+                        ready = ready && (g1 < 2 || tc::mbar_try_wait(bars + C::bSFree + j, ((g1 >> 1) - 1) & 1));
+                        if (ready) {
+                            cur_item = x_item;
+                            tc::tc_fence_after();
+                            const uint32_t aq = tc::smem_u32(sm + C::oQ + s * C::kQBytes);
+                            const uint32_t ak = tc::smem_u32(sm + C::oK + ib * C::kKBytes);
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
+                                const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
+                                tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
+                                             tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+                            }
+                            tc::mma_commit(bars + C::bSFull + j);
+                            tc::mma_commit(bars + C::bQFree + s);
+                            t_ib[g1 & 3] = ib;
+                            t_last[g1 & 3] = x_last;
+                            ++g1;
+                            have_info = false;
+                            progressed = true;
+                        }
+                    }
+                }
+                if (end_seen && g2 == g1) break;
+                if (progressed) {
+                    idle_since = 0;
+                } else if ((spin & 63u) == 0) {
+                    if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) break;
+                    const uint64_t now = tc::global_ns();
+                    if (idle_since == 0) {
+                        idle_since = now;
+                    } else if (now - idle_since > tc::kWaitLimitNs) {
+                        report_status(status, kStatusTimeout);
                         break;
                     }
                 }
-                const int32_t x_end = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
-                if (x_end) break;
-                const int32_t x_item = reinterpret_cast<volatile TileInfo *>(ti + slot)->item;
-                const int32_t x_last = reinterpret_cast<volatile TileInfo *>(ti + slot)->last;
-                const int s = g % C::kNQ, j = g & 1, ib = x_item & 1;
-                bool w = true;
-                if (x_item != cur_item) {
-                    cur_item = x_item;
-                    w = tc::mbar_wait(bars + C::bKvFull + ib, (x_item >> 1) & 1, status);
-                }
-                if (w) w = tc::mbar_wait(bars + C::bQFull + s, (g / C::kNQ) & 1, status);
-                if (w && g >= 2) w = tc::mbar_wait(bars + C::bSFree + j, ((g >> 1) - 1) & 1, status);
-                if (!w) {
-                    ok = false;
-                    break;
-                }
-                tc::tc_fence_after();
-                const uint32_t aq = tc::smem_u32(sm + C::oQ + s * C::kQBytes);
-                const uint32_t ak = tc::smem_u32(sm + C::oK + ib * C::kKBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
-                    const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
-                    tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
-                                 tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
-                }
-                tc::mma_commit(bars + C::bSFull + j);
-                tc::mma_commit(bars + C::bQFree + s);
-                if (pg >= 0 && !issue_pv()) {
-                    ok = false;
-                    break;
-                }
-                pg = g;
-                pib = ib;
-                plast = x_last != 0;
-                ++g;
             }
-            if (ok && pg >= 0) issue_pv();
         }
         __syncwarp();
     } else if (warp < kWarpEpi) {
@@ -566,12 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 s2[c] = ex2(fmaf(s2[c], a.scale_log2, -m2));
                 l += s2[c];
             }
-            bool w = true;
-            if (g >= 2) {
-                w = tc::mbar_wait(bars + C::bPFree + j, ((g >> 1) - 1) & 1, status);
-                if (w) w = tc::mbar_wait(bars + C::bMlFree + j, ((g >> 1) - 1) & 1, status);
-            }
-            if (!w) break;
+            // (m, l) live with the tile slot, which the producer reuses only
+            // after this tile's epilogue is done
+            ml[slot * kTile + row] = make_float2(m2, l);
+            tc::mbar_arrive(bars + C::bMlFull + slot);
+            if (g >= 2 && !tc::mbar_wait(bars + C::bPFree + j, ((g >> 1) - 1) & 1, status)) break;
             uint8_t *sP = sm + C::oP + j * C::kPBytes;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -581,7 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                                            pack_bf16x2(s2[8 * c + 6], s2[8 * c + 7]));
                 *reinterpret_cast<uint4 *>(sP + row * 128 + ((c ^ (row & 7)) << 4)) = v;
             }
-            ml[j * kTile + row] = make_float2(m2, l);
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(bars + C::bPFull + j);
         }
@@ -599,10 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const int32_t x_count = reinterpret_cast<volatile TileInfo *>(ti + slot)->count;
             const int32_t x_rg = reinterpret_cast<volatile TileInfo *>(ti + slot)->rg;
             if (!tc::mbar_wait(bars + C::bOFull + j, (g >> 1) & 1, status)) break;
-            if (!tc::mbar_wait(bars + C::bPFull + j, (g >> 1) & 1, status)) break;
+            if (!tc::mbar_wait(bars + C::bMlFull + slot, (g / kNT) & 1, status)) break;
             tc::tc_fence_after();
-            const float2 mlv = ml[j * kTile + row];
-            tc::mbar_arrive(bars + C::bMlFree + j);
+            const float2 mlv = ml[slot * kTile + row];
             const bool has = row < x_count;
             int64_t part = 0;
             if (has) {
@@ -632,10 +627,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::tc_fence_before();
             tc::mbar_arrive(bars + C::bOFree + j);
             if (has) a.part_lse[part] = mlv.x + __log2f(mlv.y);
-            __threadfence();
+            // the group's partial stores happen before one release-add
             tc::named_bar_sync(kBarEpi, 128);
             if (et == 0) {
-                atomicAdd(a.range_done + x_rg, x_count);
+                red_add_release(a.range_done + x_rg, x_count);
                 tc::mbar_arrive(bars + C::bTiFree + slot);
             }
         }
@@ -711,9 +706,22 @@ bool make_rows_map(CUtensorMap *m, const void *base, int64_t bh, int64_t n, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][d] bf16 viewed as 2-D, box 64 x 1 (one row per gathered row).
+bool make_gather_map(CUtensorMap *m, const void *base, int64_t rows, int d) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(d) * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
-cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorMap &mv,
-                     cudaStream_t st) {
+cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, cudaStream_t st) {
     using C = Cfg<D>;
     auto kern = fine_ws_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal);
@@ -721,7 +729,7 @@ cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorM
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    kern<<<sms, kThreads, C::kTotal, st>>>(mk, mv, a);   // one CTA per SM
+    kern<<<sms, kThreads, C::kTotal, st>>>(mq, mk, mv, a);   // one CTA per SM
     return cudaGetLastError();
 }
 
@@ -732,11 +740,12 @@ bool fine_bm_supported(int32_t d, int32_t key_block) {
 }
 
 cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st) {
-    CUtensorMap mk, mv;
-    if (!make_rows_map(&mk, a.k_ptr, a.bh, a.n, a.d, kB) || !make_rows_map(&mv, a.v_ptr, a.bh, a.n, a.d, kB))
+    CUtensorMap mq, mk, mv;
+    if (!make_gather_map(&mq, a.q, a.bh * a.n, a.d) ||
+        !make_rows_map(&mk, a.k_ptr, a.bh, a.n, a.d, kB) || !make_rows_map(&mv, a.v_ptr, a.bh, a.n, a.d, kB))
         return cudaErrorInvalidValue;
-    if (a.d == 64) return launch_d<64>(a, mk, mv, st);
-    return launch_d<128>(a, mk, mv, st);
+    if (a.d == 64) return launch_d<64>(a, mq, mk, mv, st);
+    return launch_d<128>(a, mq, mk, mv, st);
 }
 
 }  // namespace bsa
