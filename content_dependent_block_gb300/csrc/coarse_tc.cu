@@ -76,8 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
     uint32_t key_mask, int32_t *__restrict__ idx, int32_t *status) {
     using S = CoarseSmem<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = tc::align_smem_1024(smem_raw);
     uint8_t *sQ = smem;
     uint8_t *sK = smem + S::kQBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kTiles);

@@ -5,30 +5,33 @@
 //
 // Schedule.  The per-query lists are inverted (invert.cu) into bins
 // (head, query range, key block), each listing the (query, slot) pairs that
-// selected the block.  One persistent CTA per SM runs five warp roles that
+// selected the block.  One persistent CTA per SM runs six warp roles that
 // hand work to each other through mbarrier rings in shared memory:
 //
-//   prefetch  (warp 14)     takes fine items (one bin, <= 512 pairs) from a
+//   prefetch  (warp 13)     takes fine items (one bin, <= 512 pairs) from a
 //                           global queue and stages each item's descriptor
 //                           and pair ids in a shared-memory ring
-//   producer  (warp 0)      per staged item: loads K_b, V_b by TMA (128-byte
-//                           swizzle, double-buffered per item) and gathers the
-//                           128 query rows of each tile with TMA gather4 (four
-//                           rows per instruction) into a ring of Q stages;
-//                           publishes per-tile info
-//   MMA       (warp 1)      S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
+//   gather    (warps 0-3)   per staged item: loads K_b, V_b by TMA (128-byte
+//                           swizzle, one buffer per item in flight); per tile
+//                           of 128 pairs, 128 threads copy the query rows
+//                           with cp.async straight into the swizzled operand
+//                           layout, and publish a tile once the next one is
+//                           in flight (or before any wait that may block)
+//   MMA       (warp 12)     S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
 //                           one of two TMEM score buffers, then O[j] = P . V_b
 //                           (N = d, V MN-major) into one of two TMEM outputs;
-//                           tile g's S is issued before tile g-1's P.V
-//   softmax   (warps 2-5)   one thread per row: m = max s, p = exp2(s - m),
+//                           an event loop that issues whichever is ready
+//   softmax   (warps 4-7)   one thread per row: m = max s, p = exp2(s - m),
 //                           l = sum p; P (bf16) to shared memory, (m, l) aside
-//   epilogue  (warps 6-9)   reads O, stores the pair's partial state
+//   epilogue  (warps 8-11)  reads O, stores the pair's partial state
 //                           o = O / l (bf16) and lse = m + log2 l into a ring
 //                           of query ranges, counts the range's finished pairs
-//   merge     (warps 10-13) takes merge items (256 queries of one range) from a
-//                           second queue once the range's pairs are all done
-//                           and merges each query's k partial states in slot
-//                           order (the online-softmax merge of (m, l, acc))
+//   merge     (warps 14-15) each takes merge items (256 queries of one range)
+//                           from a second queue once the range's pairs are all
+//                           done, pulls the queries' partial states into
+//                           shared-memory stages with bulk copies and merges
+//                           each query's k states in slot order (the
+//                           online-softmax merge of (m, l, acc))
 //
 // Partial states of a range live in ring entry (range mod kPartialRing); a
 // fine item of range r waits until range r - kPartialRing is merged.  Every
@@ -49,12 +52,15 @@ namespace {
 constexpr int kTile = 128;
 constexpr int kB = 64;                   // key block handled by this kernel
 constexpr int kNT = 8;                   // tile-info ring
-constexpr int kNI = 4;                   // staged fine-item ring
+constexpr int kNI = 2;                   // staged fine-item ring
 constexpr int kItemMax = 512;            // pairs per fine item (kFineBmItemPairs)
-constexpr int kWarps = 15;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpEpi = 6, kWarpMerge = 10, kWarpFetch = 14;
-constexpr uint32_t kBarEpi = 1, kBarMerge = 2;
+constexpr int kWarpSoftmax = 4, kWarpEpi = 8, kWarpMma = 12, kWarpFetch = 13, kWarpMerge = 14;
+constexpr int kGather = 128;             // gather threads (warps 0-3)
+constexpr int kMergeWarps = 2;
+constexpr int kStageBytes = 17408;       // one merge stage: >= 2 queries at d = 128, k = 32
+constexpr uint32_t kBarEpi = 1;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct TileInfo {
@@ -70,16 +76,19 @@ struct StagedItem {
 template <int D>
 struct Cfg {
     static constexpr int kSub = D / 64;
-    static constexpr int kNQ = D == 64 ? 4 : 3;            // Q stages
+    static constexpr int kNQ = D == 64 ? 3 : 2;            // Q stages
+    static constexpr int kNKV = D == 64 ? 3 : 2;           // K/V buffers (items in flight)
+    static constexpr int kMS = D == 64 ? 2 : 1;            // merge stages per merge warp
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kPBytes = kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int oQ = 0;
     static constexpr int oP = oQ + kNQ * kQBytes;
-    static constexpr int kNKV = D == 64 ? 4 : 2;           // K/V buffers (items in flight)
     static constexpr int oK = oP + 2 * kPBytes;
     static constexpr int oV = oK + kNKV * kKBytes;
-    static constexpr int oML = oV + kNKV * kKBytes;        // float2 [kNT][128]
+    static constexpr int oMs = oV + kNKV * kKBytes;        // merge stages
+    static constexpr int oEpi = oMs + kMergeWarps * kMS * kStageBytes;  // 4 warps x 32 rows x 64 B
+    static constexpr int oML = oEpi + 4 * 2048;            // float2 [kNT][128]
     static constexpr int oPid = oML + kNT * kTile * 8;     // int32  [kNT][128]
     static constexpr int oTi = oPid + kNT * kTile * 4;     // TileInfo [kNT]
     static constexpr int oItem = oTi + kNT * 32;           // StagedItem [kNI]
@@ -100,13 +109,16 @@ struct Cfg {
         bTiFree = bTiFull + kNT,
         bItFull = bTiFree + kNT,
         bItFree = bItFull + kNI,
-        bCount = bItFree + kNI
+        bMsFull = bItFree + kNI,
+        bCount = bMsFull + kMergeWarps * kMS
     };
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
     static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
     static constexpr uint32_t cO = 2 * kB;                 // O[j] at cO + j*D; S[j] at j*64
 };
+static_assert(Cfg<64>::kTotal <= 227 * 1024, "shared memory (d = 64)");
+static_assert(Cfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
 
 __device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
     int32_t v;
@@ -140,106 +152,97 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Merge up to four queries per warp: four 8-lane groups, one query each;
-// lane gl of a group owns channels [gl*D/8, (gl+1)*D/8).  `base` indexes the
-// query's partial slots in the ring; `active` false for an idle group.
+// Merge one query's partial states from a shared-memory stage.  The query
+// is owned by a group of LPQ = D/16 lanes; lane gl owns channels
+// [16 gl, 16 gl + 16), read as two 16-byte chunks per slot.  `po` points at
+// this lane's channels of slot 0 (slots D channels apart), `pl` at the
+// query's lse values, `vm` has bit s set for every listed slot s.  Slot s's
+// lse is read by lane s mod LPQ and the weights exp2(lse - max) are shared
+// by shuffles.  Neighbouring queries read their two chunks in opposite
+// order, so that a quarter warp touches all 32 banks once.  The slot loop
+// is rolled (four slots per trip) to keep the code small.  Returns false
+// when nothing is listed; else acc holds the merged channels.
 template <int D>
-__device__ __forceinline__ void merge_group(bool active, int64_t qrow, int64_t base,
-                                            const int32_t *list, int32_t k, int64_t nb,
-                                            int32_t full_valid, int lane, const uint16_t *part_o,
-                                            const float *part_lse, uint16_t *out) {
-    constexpr int C = D / 8;                   // channels per lane: 8 or 16
-    constexpr int V = C / 8;                   // uint4 per partial row chunk: 1 or 2
-    constexpr int CH = D == 64 ? 16 : 8;       // slots per load chunk
-    const int gl = lane & 7;
-    const int gbase = lane & ~7;
-    bool vs[4];
+__device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pl, uint32_t vm, int k,
+                                            int lane, float (&acc)[16]) {
+    constexpr int LPQ = D / 16;
+    constexpr int SPL = 32 / LPQ;              // slots per lane (k <= 32)
+    const int gl = lane % LPQ, gbase = lane - gl;
+    const int c0 = (lane / LPQ) & 1;           // chunk read first
+    float w[SPL];
+    float M = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int s = gl + 8 * j;
-        bool v = active && s < k;
-        if (v && full_valid == 0) {
-            const int32_t b = __ldg(list + qrow * k + s);
-            v = b >= 0 && b < nb;
-        } else if (v) {
-            v = s < full_valid;
-        }
-        vs[j] = v;
+    for (int t = 0; t < SPL; ++t) {
+        const int s = gl + LPQ * t;
+        w[t] = ((vm >> s) & 1u) ? pl[s] : -INFINITY;
+        M = fmaxf(M, w[t]);
     }
-    float acc[C];
 #pragma unroll
-    for (int c = 0; c < C; ++c) acc[c] = 0.f;
-    float M = -INFINITY, L = 0.f;
-    float w[4];
+    for (int o = 1; o < LPQ; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+    float L = 0.f;
 #pragma unroll
-    for (int c0 = 0; c0 < 32; c0 += CH) {
-        if (c0 >= k) break;
-        // every load of this chunk (and the slot lse values) in flight at once
-        uint4 x[CH][V];
+    for (int t = 0; t < SPL; ++t) {
+        const int s = gl + LPQ * t;
+        w[t] = ((vm >> s) & 1u) ? ex2(w[t] - M) : 0.f;
+        L += w[t];
+    }
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-            const int s = c0 + u;
-            const bool v = __shfl_sync(kFull, vs[s >> 3], gbase | (s & 7));
-            const uint4 *src = reinterpret_cast<const uint4 *>(part_o + (base + s) * D + gl * C);
+    for (int o = 1; o < LPQ; o <<= 1) L += __shfl_xor_sync(kFull, L, o);
+    float a0[8], a1[8];                        // chunk c0, chunk 1 - c0
 #pragma unroll
-            for (int e = 0; e < V; ++e) x[u][e] = v ? __ldcg(src + e) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (c0 == 0) {
-            float lse[4];
+    for (int c = 0; c < 8; ++c) a0[c] = a1[c] = 0.f;
+#pragma unroll 1
+    for (int s0 = 0; s0 < k; s0 += 4) {
+        const int u0 = s0 % LPQ;               // w[0] holds slots gl + s0 - u0 .. of the group
+        float ws[4];
+        uint4 x[4][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) lse[j] = vs[j] ? __ldcg(part_lse + base + gl + 8 * j) : -INFINITY;
-            M = fmaxf(fmaxf(lse[0], lse[1]), fmaxf(lse[2], lse[3]));
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                w[j] = vs[j] ? ex2(lse[j] - M) : 0.f;
-                L += w[j];
-            }
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) L += __shfl_xor_sync(kFull, L, o);
+        for (int u = 0; u < 4; ++u) {
+            ws[u] = __shfl_sync(kFull, w[0], gbase + u0 + u);
+            const uint16_t *src = po + (s0 + u) * D;
+            x[u][0] = ws[u] != 0.f ? *reinterpret_cast<const uint4 *>(src + c0 * 8) : make_uint4(0u, 0u, 0u, 0u);
+            x[u][1] = ws[u] != 0.f ? *reinterpret_cast<const uint4 *>(src + (1 - c0) * 8) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < CH; ++u) {
-            const int s = c0 + u;
-            const float ws = __shfl_sync(kFull, w[s >> 3], gbase | (s & 7));
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t xa[4] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w};
+            const uint32_t xb[4] = {x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const uint32_t xw[4] = {x[u][e].x, x[u][e].y, x[u][e].z, x[u][e].w};
-#pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    acc[8 * e + 2 * h2] = fmaf(ws, bf16_low_half(xw[h2]), acc[8 * e + 2 * h2]);
-                    acc[8 * e + 2 * h2 + 1] = fmaf(ws, bf16_high_half(xw[h2]), acc[8 * e + 2 * h2 + 1]);
-                }
+            for (int h2 = 0; h2 < 4; ++h2) {
+                a0[2 * h2] = fmaf(ws[u], bf16_low_half(xa[h2]), a0[2 * h2]);
+                a0[2 * h2 + 1] = fmaf(ws[u], bf16_high_half(xa[h2]), a0[2 * h2 + 1]);
+                a1[2 * h2] = fmaf(ws[u], bf16_low_half(xb[h2]), a1[2 * h2]);
+                a1[2 * h2 + 1] = fmaf(ws[u], bf16_high_half(xb[h2]), a1[2 * h2 + 1]);
             }
         }
+        if (u0 + 4 == LPQ) {                   // this lane's next slot group
+#pragma unroll
+            for (int t = 0; t + 1 < SPL; ++t) w[t] = w[t + 1];
+        }
     }
-    if (!active || L == 0.f) return;           // nothing listed: O stays 0
+    if (L == 0.f) return false;
     const float invL = 1.f / L;
-    uint4 *dst = reinterpret_cast<uint4 *>(out + qrow * D + gl * C);
 #pragma unroll
-    for (int e = 0; e < V; ++e)
-        dst[e] = make_uint4(pack_bf16x2(acc[8 * e + 0] * invL, acc[8 * e + 1] * invL),
-                            pack_bf16x2(acc[8 * e + 2] * invL, acc[8 * e + 3] * invL),
-                            pack_bf16x2(acc[8 * e + 4] * invL, acc[8 * e + 5] * invL),
-                            pack_bf16x2(acc[8 * e + 6] * invL, acc[8 * e + 7] * invL));
+    for (int c = 0; c < 8; ++c) {
+        acc[c] = (c0 == 0 ? a0[c] : a1[c]) * invL;
+        acc[8 + c] = (c0 == 0 ? a1[c] : a0[c]) * invL;
+    }
+    return true;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const FineBmArgs a) {
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const FineBmArgs a) {
     using C = Cfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sm = tc::align_smem_1024(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::oBar);
     TileInfo *ti = reinterpret_cast<TileInfo *>(sm + C::oTi);
     StagedItem *items = reinterpret_cast<StagedItem *>(sm + C::oItem);
     int32_t *pids = reinterpret_cast<int32_t *>(sm + C::oPid);
     float2 *ml = reinterpret_cast<float2 *>(sm + C::oML);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::oMisc);
-    int32_t *s_merge = reinterpret_cast<int32_t *>(sm + C::oMisc + 16);   // [2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = a.status;
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNQ; ++i) {
-            tc::mbar_init(bars + C::bQFull + i, 1);
+            tc::mbar_init(bars + C::bQFull + i, kGather);
             tc::mbar_init(bars + C::bQFree + i, 1);
         }
         for (int i = 0; i < C::kNKV; ++i) {
@@ -264,15 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         }
         for (int i = 0; i < kNT; ++i) tc::mbar_init(bars + C::bMlFull + i, kTile);
         for (int i = 0; i < kNT; ++i) {
-            tc::mbar_init(bars + C::bTiFull + i, 32);
+            tc::mbar_init(bars + C::bTiFull + i, kGather);
             tc::mbar_init(bars + C::bTiFree + i, 1);
         }
         for (int i = 0; i < kNI; ++i) {
             tc::mbar_init(bars + C::bItFull + i, 32);
-            tc::mbar_init(bars + C::bItFree + i, 32);
+            tc::mbar_init(bars + C::bItFree + i, kGather);
         }
+        for (int i = 0; i < kMergeWarps * C::kMS; ++i) tc::mbar_init(bars + C::bMsFull + i, 1);
         tc::fence_barrier_init();
-        tc::prefetch_tensormap(&tm_q);
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
     }
@@ -331,130 +334,160 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::mbar_arrive(bars + C::bItFull + slot);
             if (!valid) break;
         }
-    } else if (warp == kWarpProducer) {
-        // ------------------------------------------------------- producer
-        int g = 0, item_idx = 0;
+    } else if (warp < kWarpSoftmax) {
+        // --------------------------------------------------------- gather
+        // Thread gt owns pair row gt of each tile (its pid and query row);
+        // for the copies, lane l of warp gw moves 16-byte chunk (l & 7) of
+        // rows gw*32 + 4*i + (l >> 3), i < 8, taking the query row from the
+        // owning lane.  A tile's copies are published (wait, proxy fence,
+        // arrive) once kLag later tiles are in flight, or before any wait
+        // that may block.
+        constexpr int kLag = C::kNQ - 1;
+        const int gw = warp, gt = threadIdx.x;
+        const int chunk = lane & 7, rsub = lane >> 3;
+        int g = 0, item_idx = 0, npend = 0;      // tiles g - npend .. g - 1 unpublished
         bool ok = true;
+        auto flush = [&]() {
+            if (npend > 0) {
+                tc::cp_async_wait_pending<0>();
+                tc::fence_proxy_async_smem();
+                for (int t = g - npend; t < g; ++t) tc::mbar_arrive(bars + C::bQFull + t % C::kNQ);
+                npend = 0;
+            }
+        };
+        auto wait = [&](uint64_t *bar, uint32_t par) -> bool {
+            if (__all_sync(kFull, tc::mbar_test_wait(bar, par))) return true;
+            flush();
+            return __all_sync(kFull, tc::mbar_wait(bar, par, status));
+        };
         for (int u = 0;; ++u) {
             const int islot = u % kNI;
-            if (!tc::mbar_wait(bars + C::bItFull + islot, (u / kNI) & 1, status)) ok = false;
-            ok = __all_sync(kFull, ok);
+            if (!wait(bars + C::bItFull + islot, (u / kNI) & 1)) {
+                ok = false;
+                break;
+            }
             const StagedItem *si = items + islot;
-            bool done = !ok || !si->valid;
-            int64_t bin = 0, rg = 0, h = 0, b = 0;
-            int32_t first = 0, end = 0;
-            if (!done) {
-                bin = si->bin;
-                first = si->first;
-                end = si->end;
-                rg = si->rg;
-                h = si->h;
-                b = si->b;
+            if (!si->valid) break;
+            const int32_t first = si->first, end = si->end, bin = si->bin, rg = si->rg;
+            if (gw == 0) {
                 if (rg >= kPartialRing) {
                     // the ring entry must have been merged by its previous range
+                    flush();
                     int got = 1;
                     if (lane == 0)
                         got = wait_counter(a.merge_done + (rg - kPartialRing),
                                            a.w.range_merges[rg - kPartialRing], status);
                     if (!__shfl_sync(kFull, got, 0)) {
                         ok = false;
-                        done = true;
+                        break;
+                    }
+                }
+                const int ib = item_idx % C::kNKV;
+                if (item_idx >= C::kNKV && !wait(bars + C::bKvFree + ib, ((item_idx / C::kNKV) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const int32_t h = si->h, b = si->b;
+                    tc::mbar_arrive_expect_tx(bars + C::bKvFull + ib, 2 * C::kKBytes);
+#pragma unroll
+                    for (int sub = 0; sub < C::kSub; ++sub) {
+                        tc::tma_load_3d(sm + C::oK + ib * C::kKBytes + sub * kB * 128, &tm_k,
+                                        bars + C::bKvFull + ib, sub * 64, b * kB, h);
+                        tc::tma_load_3d(sm + C::oV + ib * C::kKBytes + sub * kB * 128, &tm_v,
+                                        bars + C::bKvFull + ib, sub * 64, b * kB, h);
                     }
                 }
             }
-            if (done) {
-                const int slot = g % kNT;
-                bool w = true;
-                if (g >= kNT) w = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
-                w = __all_sync(kFull, w);
-                if (w && lane == 0) ti[slot].end = 1;
-                __syncwarp();
-                if (w) tc::mbar_arrive(bars + C::bTiFull + slot);
-                break;
-            }
-            const int ib = item_idx % C::kNKV;
-            if (item_idx >= C::kNKV) {
-                ok = tc::mbar_wait(bars + C::bKvFree + ib, ((item_idx / C::kNKV) - 1) & 1, status);
-                ok = __all_sync(kFull, ok);
-                if (!ok) {
-                    tc::mbar_arrive(bars + C::bItFree + islot);
-                    continue;                     // publishes the end marker
-                }
-            }
-            if (lane == 0) {
-                tc::mbar_arrive_expect_tx(bars + C::bKvFull + ib, 2 * C::kKBytes);
-#pragma unroll
-                for (int sub = 0; sub < C::kSub; ++sub) {
-                    tc::tma_load_3d(sm + C::oK + ib * C::kKBytes + sub * kB * 128, &tm_k,
-                                    bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
-                    tc::tma_load_3d(sm + C::oV + ib * C::kKBytes + sub * kB * 128, &tm_v,
-                                    bars + C::bKvFull + ib, sub * 64, int32_t(b * kB), int32_t(h));
-                }
-            }
-            for (int32_t p0 = first; ok && p0 < end; p0 += kTile) {
+            for (int32_t p0 = first; p0 < end; p0 += kTile) {
                 const int s = g % C::kNQ, slot = g % kNT;
-                if (g >= C::kNQ) ok = tc::mbar_wait(bars + C::bQFree + s, ((g / C::kNQ) - 1) & 1, status);
-                if (ok && g >= kNT) ok = tc::mbar_wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1, status);
-                ok = __all_sync(kFull, ok);
-                if (!ok) break;
-                const int cnt = min(kTile, end - p0);
-                // lane l gathers rows 4l .. 4l+3 (padding rows repeat row 0)
-                int32_t qr[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = 4 * lane + e;
-                    const int32_t pid = si->pid[p0 - first + (r < cnt ? r : 0)];
-                    if (r < cnt) pids[slot * kTile + r] = pid;
-                    qr[e] = pid / k;                        // flat query row h*n + i
+                if (g >= C::kNQ && !wait(bars + C::bQFree + s, ((g / C::kNQ) - 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                if (lane == 0) tc::mbar_arrive_expect_tx(bars + C::bQFull + s, C::kQBytes);
-                __syncwarp();
+                if (g >= kNT && !wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int cnt = min(kTile, end - p0);
+                const int32_t *pp = si->pid + (p0 - first);
+                const int32_t my_pid = pp[gt < cnt ? gt : 0];
+                if (gt < cnt) pids[slot * kTile + gt] = my_pid;
+                const int32_t my_q = my_pid / k;             // flat query row h*n + i
                 uint8_t *sQ = sm + C::oQ + s * C::kQBytes;
 #pragma unroll
-                for (int sub = 0; sub < C::kSub; ++sub)
-                    tc::tma_gather4(sQ + sub * kTile * 128 + lane * 4 * 128, &tm_q, bars + C::bQFull + s,
-                                    sub * 64, qr[0], qr[1], qr[2], qr[3]);
-                if (lane == 0) {
+                for (int i = 0; i < 8; ++i) {
+                    const int rl = i * 4 + rsub, r = gw * 32 + rl;
+                    const int64_t qrow = __shfl_sync(kFull, my_q, rl);
+                    const uint16_t *src = a.q + qrow * D + chunk * 8;
+                    uint8_t *dst = sQ + r * 128 + ((chunk ^ (r & 7)) << 4);
+#pragma unroll
+                    for (int sub = 0; sub < C::kSub; ++sub)   // rows past the pairs read as zeros
+                        tc::cp_async16_zfill(dst + sub * kTile * 128, src + sub * 64, r < cnt);
+                }
+                tc::cp_async_commit();
+                if (npend == kLag) {
+                    tc::cp_async_wait_pending<kLag>();
+                    tc::fence_proxy_async_smem();
+                    tc::mbar_arrive(bars + C::bQFull + (g - kLag) % C::kNQ);
+                    --npend;
+                }
+                ++npend;
+                if (gt == 0) {
                     TileInfo x;
-                    x.bin = int32_t(bin);
+                    x.bin = bin;
                     x.p0 = p0;
                     x.count = cnt;
                     x.item = item_idx;
                     x.last = p0 + kTile >= end;
-                    x.rg = int32_t(rg);
+                    x.rg = rg;
                     x.end = 0;
                     x.pad = 0;
                     ti[slot] = x;
                 }
-                __syncwarp();
                 tc::mbar_arrive(bars + C::bTiFull + slot);
                 ++g;
             }
-            __syncwarp();
+            if (!ok) break;
             tc::mbar_arrive(bars + C::bItFree + islot);
             ++item_idx;
         }
+        flush();
+        if (ok) {
+            // end marker for the consumers
+            const int slot = g % kNT;
+            if (g < kNT || wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1)) {
+                if (gt == 0) ti[slot].end = 1;
+                tc::mbar_arrive(bars + C::bTiFull + slot);
+            }
+        }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA
-        // One thread, run as an event loop: issue whichever is ready first,
-        // the S of the next tile or the P.V of the oldest tile whose P is in
-        // shared memory (both in tile order), so no P.V is ever held back.
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
-            int g1 = 0, g2 = 0;                   // next tile for S, next tile for P.V
-            int cur_item = -1, x_item = 0, x_last = 0;
-            int t_ib[4] = {0, 0, 0, 0}, t_last[4] = {0, 0, 0, 0};
-            bool end_seen = false, have_info = false;
-            uint64_t idle_since = 0;
-            for (uint32_t spin = 0;; ++spin) {
-                bool progressed = false;
-                if (g2 < g1) {
-                    const int j = g2 & 1;
-                    if (tc::mbar_try_wait(bars + C::bPFull + j, (g2 >> 1) & 1) &&
-                        (g2 < 2 || tc::mbar_try_wait(bars + C::bOFree + j, ((g2 >> 1) - 1) & 1))) {
-                        tc::tc_fence_after();
-                        const int ib = t_ib[g2 & 3];
+        // The whole warp runs an event loop with warp-uniform state (barrier
+        // probes are made by lane 0 and broadcast) and one elected lane
+        // issues: the S of the next tile or the P.V of the oldest tile whose
+        // P is in shared memory, whichever is ready first (both in tile
+        // order), so no P.V is ever held back.  Keeping the issuing code
+        // warp-uniform lets the MMAs issue back to back.
+        constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
+        constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
+        int g1 = 0, g2 = 0;                       // next tile for S, next tile for P.V
+        int cur_item = -1, x_item = 0, x_last = 0;
+        int t_ib[4] = {0, 0, 0, 0}, t_last[4] = {0, 0, 0, 0};
+        bool end_seen = false, have_info = false;
+        uint64_t idle_since = 0;
+        auto probe = [&](uint64_t *bar, uint32_t par) -> bool {
+            return __shfl_sync(kFull, lane == 0 ? int(tc::mbar_test_wait(bar, par)) : 0, 0) != 0;
+        };
+        for (uint32_t spin = 0;; ++spin) {
+            bool progressed = false;
+            if (g2 < g1) {
+                const int j = g2 & 1;
+                if (probe(bars + C::bPFull + j, (g2 >> 1) & 1) &&
+                    (g2 < 2 || probe(bars + C::bOFree + j, ((g2 >> 1) - 1) & 1))) {
+                    tc::tc_fence_after();
+                    const int ib = t_ib[g2 & 3];
+                    if (tc::elect_one()) {
                         const uint32_t ap = tc::smem_u32(sm + C::oP + j * C::kPBytes);
                         const uint32_t av = tc::smem_u32(sm + C::oV + ib * C::kKBytes);
 #pragma unroll
@@ -465,32 +498,34 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                         tc::mma_commit(bars + C::bOFull + j);
                         tc::mma_commit(bars + C::bPFree + j);
                         if (t_last[g2 & 3]) tc::mma_commit(bars + C::bKvFree + ib);
-                        ++g2;
-                        progressed = true;
                     }
+                    __syncwarp();
+                    ++g2;
+                    progressed = true;
                 }
-                if (!end_seen && g1 - g2 < 3) {
-                    const int slot = g1 % kNT;
-                    if (!have_info && tc::mbar_try_wait(bars + C::bTiFull + slot, (g1 / kNT) & 1)) {
-                        const volatile TileInfo *xi = ti + slot;
-                        if (xi->end) {
-                            end_seen = true;
-                        } else {
-                            have_info = true;
-                            x_item = xi->item;
-                            x_last = xi->last;
-                        }
-                        progressed = true;
+            }
+            if (!end_seen && g1 - g2 < 3) {
+                const int slot = g1 % kNT;
+                if (!have_info && probe(bars + C::bTiFull + slot, (g1 / kNT) & 1)) {
+                    const volatile TileInfo *xi = ti + slot;
+                    if (xi->end) {
+                        end_seen = true;
+                    } else {
+                        have_info = true;
+                        x_item = xi->item;
+                        x_last = xi->last;
                     }
-                    if (have_info) {
-                        const int s = g1 % C::kNQ, j = g1 & 1, ib = x_item % C::kNKV;
-                        bool ready = x_item == cur_item ||
-                                     tc::mbar_try_wait(bars + C::bKvFull + ib, (x_item / C::kNKV) & 1);
-                        ready = ready && tc::mbar_try_wait(bars + C::bQFull + s, (g1 / C::kNQ) & 1);
-                        ready = ready && (g1 < 2 || tc::mbar_try_wait(bars + C::bSFree + j, ((g1 >> 1) - 1) & 1));
-                        if (ready) {
-                            cur_item = x_item;
-                            tc::tc_fence_after();
+                    progressed = true;
+                }
+                if (have_info) {
+                    const int s = g1 % C::kNQ, j = g1 & 1, ib = x_item % C::kNKV;
+                    bool ready = x_item == cur_item || probe(bars + C::bKvFull + ib, (x_item / C::kNKV) & 1);
+                    ready = ready && probe(bars + C::bQFull + s, (g1 / C::kNQ) & 1);
+                    ready = ready && (g1 < 2 || probe(bars + C::bSFree + j, ((g1 >> 1) - 1) & 1));
+                    if (ready) {
+                        cur_item = x_item;
+                        tc::tc_fence_after();
+                        if (tc::elect_one()) {
                             const uint32_t aq = tc::smem_u32(sm + C::oQ + s * C::kQBytes);
                             const uint32_t ak = tc::smem_u32(sm + C::oK + ib * C::kKBytes);
 #pragma unroll
@@ -502,32 +537,36 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                             }
                             tc::mma_commit(bars + C::bSFull + j);
                             tc::mma_commit(bars + C::bQFree + s);
-                            t_ib[g1 & 3] = ib;
-                            t_last[g1 & 3] = x_last;
-                            ++g1;
-                            have_info = false;
-                            progressed = true;
                         }
+                        __syncwarp();
+                        t_ib[g1 & 3] = ib;
+                        t_last[g1 & 3] = x_last;
+                        ++g1;
+                        have_info = false;
+                        progressed = true;
                     }
                 }
-                if (end_seen && g2 == g1) break;
-                if (progressed) {
-                    idle_since = 0;
-                } else if ((spin & 63u) == 0) {
-                    if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) break;
-                    const uint64_t now = tc::global_ns();
-                    if (idle_since == 0) {
-                        idle_since = now;
-                    } else if (now - idle_since > tc::kWaitLimitNs) {
-                        report_status(status, kStatusTimeout);
-                        break;
-                    }
+            }
+            if (end_seen && g2 == g1) break;
+            if (progressed) {
+                idle_since = 0;
+            } else if ((spin & 63u) == 0) {
+                if (__shfl_sync(kFull, *reinterpret_cast<volatile int32_t *>(status), 0) == kStatusTimeout) break;
+                const uint64_t now = __shfl_sync(kFull, tc::global_ns(), 0);
+                if (idle_since == 0) {
+                    idle_since = now;
+                } else if (now - idle_since > tc::kWaitLimitNs) {
+                    if (lane == 0) report_status(status, kStatusTimeout);
+                    break;
                 }
             }
         }
         __syncwarp();
     } else if (warp < kWarpEpi) {
         // -------------------------------------------------------- softmax
+        // One thread per score row, in two passes over the row in TMEM (32
+        // columns at a time, rolled loops to keep the code small): the row
+        // max, then p = exp2(s * scale - m) written to P as bf16.
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
@@ -539,54 +578,70 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const int64_t bin = reinterpret_cast<volatile TileInfo *>(ti + slot)->bin;
             if (!tc::mbar_wait(bars + C::bSFull + j, (g >> 1) & 1, status)) break;
             tc::tc_fence_after();
-            uint32_t sv[2][32];
-            tc::tmem_ld32(tmem + uint32_t(j * kB) + lane_off, sv[0]);
-            tc::tmem_ld32(tmem + uint32_t(j * kB + 32) + lane_off, sv[1]);
-            tc::tmem_ld_wait();
-            tc::tc_fence_before();
-            tc::mbar_arrive(bars + C::bSFree + j);
-            const int64_t keys_valid = n - (bin % nb) * kB;
-            float s2[64];
+            const int keys_valid = int(i64min(64, n - (bin % nb) * kB));   // < 64: ragged last block
+            float mraw = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t sv[32];
+                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                tc::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 64; ++c) s2[c] = __uint_as_float(sv[c >> 5][c & 31]);
-            if (keys_valid < 64) {                    // ragged last block only
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c >= keys_valid) s2[c] = -INFINITY;
+                for (int c = 0; c < 32; ++c)
+                    if (c0 + c < keys_valid) mraw = fmaxf(mraw, __uint_as_float(sv[c]));
             }
-            float mraw = s2[0];
-#pragma unroll
-            for (int c = 1; c < 64; ++c) mraw = fmaxf(mraw, s2[c]);
             const float m2 = mraw * a.scale_log2;     // scale > 0 keeps the argmax
             float l = 0.f;
+            bool ok = true;
+            uint8_t *sP = sm + C::oP + j * C::kPBytes + row * 128;
+#pragma unroll 1
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                uint32_t sv[32];
+                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                tc::tmem_ld_wait();
+                if (c0 == 32) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(bars + C::bSFree + j);
+                }
+                uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                s2[c] = ex2(fmaf(s2[c], a.scale_log2, -m2));
-                l += s2[c];
+                for (int c = 0; c < 32; c += 2) {
+                    const float p0 = c0 + c < keys_valid ? ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -m2)) : 0.f;
+                    const float p1 = c0 + c + 1 < keys_valid ? ex2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, -m2)) : 0.f;
+                    l += p0 + p1;
+                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                if (c0 == 0 && g >= 2 && !tc::mbar_wait(bars + C::bPFree + j, ((g >> 1) - 1) & 1, status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = (c0 >> 3) + c;          // 16-byte chunk of the 128-byte row
+                    *reinterpret_cast<uint4 *>(sP + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
             }
-            // (m, l) live with the tile slot, which the producer reuses only
-            // after this tile's epilogue is done
+            if (!ok) break;
+            // (m, l) live with the tile slot, which the gather group reuses
+            // only after this tile's epilogue is done
             ml[slot * kTile + row] = make_float2(m2, l);
             tc::mbar_arrive(bars + C::bMlFull + slot);
-            if (g >= 2 && !tc::mbar_wait(bars + C::bPFree + j, ((g >> 1) - 1) & 1, status)) break;
-            uint8_t *sP = sm + C::oP + j * C::kPBytes;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 v = make_uint4(pack_bf16x2(s2[8 * c + 0], s2[8 * c + 1]),
-                                           pack_bf16x2(s2[8 * c + 2], s2[8 * c + 3]),
-                                           pack_bf16x2(s2[8 * c + 4], s2[8 * c + 5]),
-                                           pack_bf16x2(s2[8 * c + 6], s2[8 * c + 7]));
-                *reinterpret_cast<uint4 *>(sP + row * 128 + ((c ^ (row & 7)) << 4)) = v;
-            }
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(bars + C::bPFull + j);
         }
-    } else if (warp < kWarpMerge) {
+    } else if (warp < kWarpMma) {
         // ------------------------------------------------------- epilogue
+        // Thread `row` owns one pair: o = O / l (bf16) and lse = m + log2 l.
+        // O is read from TMEM 64 columns at a time (the buffer is released
+        // after the last read); each 32-column chunk goes through a small
+        // swizzled shared buffer so that every store instruction writes 64
+        // contiguous bytes of 8 rows instead of 16 bytes of 32 rows.
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int et = (warp - kWarpEpi) * 32 + lane;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        uint8_t *eb = sm + C::oEpi + (warp - kWarpEpi) * 2048;
+        const int srow = lane >> 2, spiece = lane & 3;      // store phase: rows 8i + srow
         for (int g = 0;; ++g) {
             const int slot = g % kNT, j = g & 1;
             if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
@@ -607,25 +662,47 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 const int64_t h = x_rg / nranges, rr = x_rg % nranges;
                 part = (x_rg % kPartialRing) * ring_stride + (qrow - h * n - rr * range) * kpad + s;
             }
+            int64_t sp[4];                                    // part of rows 8i + srow
+            bool sh[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                sp[i] = __shfl_sync(kFull, part, 8 * i + srow);
+                sh[i] = quad * 32 + 8 * i + srow < x_count;
+            }
             const float inv_l = 1.f / mlv.y;
-#pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                uint32_t ov[32];
-                tc::tmem_ld32(tmem + C::cO + uint32_t(j * D + c0) + lane_off, ov);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 64) {
+                uint32_t ov[2][32];
+                tc::tmem_ld32(tmem + C::cO + uint32_t(j * D + c0) + lane_off, ov[0]);
+                tc::tmem_ld32(tmem + C::cO + uint32_t(j * D + c0 + 32) + lane_off, ov[1]);
                 tc::tmem_ld_wait();
-                if (has) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.part_o + part * D + c0);
+                if (c0 + 64 == D) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(bars + C::bOFree + j);
+                }
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(
-                            pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l),
-                            pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l),
-                            pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l),
-                            pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l));
+                for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 val = make_uint4(
+                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 0]) * inv_l, __uint_as_float(ov[hf][8 * v + 1]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 2]) * inv_l, __uint_as_float(ov[hf][8 * v + 3]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 4]) * inv_l, __uint_as_float(ov[hf][8 * v + 5]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 6]) * inv_l, __uint_as_float(ov[hf][8 * v + 7]) * inv_l));
+                        *reinterpret_cast<uint4 *>(eb + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 8 * i + srow;
+                        const uint4 val =
+                            *reinterpret_cast<const uint4 *>(eb + r * 64 + ((spiece ^ ((r >> 1) & 3)) << 4));
+                        if (sh[i])
+                            *reinterpret_cast<uint4 *>(a.part_o + sp[i] * D + c0 + hf * 32 + spiece * 8) = val;
+                    }
+                    __syncwarp();
                 }
             }
-            tc::tc_fence_before();
-            tc::mbar_arrive(bars + C::bOFree + j);
             if (has) a.part_lse[part] = mlv.x + __log2f(mlv.y);
             // the group's partial stores happen before one release-add
             tc::named_bar_sync(kBarEpi, 128);
@@ -634,42 +711,98 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 tc::mbar_arrive(bars + C::bTiFree + slot);
             }
         }
-    } else {
+    } else if (warp >= kWarpMerge) {
         // ---------------------------------------------------------- merge
-        const int mt = (warp - kWarpMerge) * 32 + lane;
+        // Each merge warp runs on its own: it takes a merge item, waits for
+        // the range's pairs, then streams the item's queries through its
+        // shared-memory stages (one bulk copy for the partial o block and one
+        // for the lse values of up to qs consecutive queries).  A group of
+        // D/16 lanes merges one query, each lane owning 16 channels.
+        constexpr int LPQ = D / 16;                  // lanes per query
+        constexpr int QP = 32 / LPQ;                 // queries per pass
         const int mw = warp - kWarpMerge;
+        const int gq = lane / LPQ, gl = lane % LPQ;
         const int n_merge = *a.w.n_merge;
         const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;
+        const uint32_t full_mask = full_valid >= 32 ? kFull : ((1u << full_valid) - 1u);
+        const int64_t per_q = kpad * D * 2 + kpad * 4;
+        const int qs = int(kStageBytes / per_q);                  // queries per stage (>= 2)
+        const int64_t o_cap = int64_t(qs) * kpad * D * 2;         // lse offset within a stage
+        uint8_t *stage0 = sm + C::oMs + mw * C::kMS * kStageBytes;
+        uint64_t *msbar = bars + C::bMsFull + mw * C::kMS;
+        uint32_t sc = 0;                                          // stages used so far
         for (;;) {
-            if (mt == 0) s_merge[0] = atomicAdd(a.merge_head, 1);
-            tc::named_bar_sync(kBarMerge, 128);
-            const int it = s_merge[0];
-            tc::named_bar_sync(kBarMerge, 128);
+            int it = 0;
+            if (lane == 0) it = atomicAdd(a.merge_head, 1);
+            it = __shfl_sync(kFull, it, 0);
             if (it >= n_merge) break;
             const int2 item = a.w.merge_items[it];
             const int64_t rg = item.x;
-            if (mt == 0) {
-                const bool got = wait_counter(a.range_done + rg, a.w.range_total[rg], status);
-                __threadfence();
-                s_merge[1] = got;
+            int got = 1;
+            if (lane == 0) {
+                got = wait_counter(a.range_done + rg, a.w.range_total[rg], status);
+                tc::fence_proxy_async_global();      // partials were written by generic stores
             }
-            tc::named_bar_sync(kBarMerge, 128);
-            if (!s_merge[1]) break;
+            if (!__shfl_sync(kFull, got, 0)) break;
             const int64_t h = rg / nranges, rr = rg % nranges;
             const int64_t i_begin = rr * range + item.y;
             const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
-            const int64_t slot_base = (rg % kPartialRing) * ring_stride;
-            // 16 queries per pass: 4 warps x 4 groups of 8 lanes
-            for (int64_t i0 = i_begin; i0 < i_end; i0 += 16) {
-                const int64_t i = i0 + mw * 4 + (lane >> 3);
-                const bool act = i < i_end;
-                const int64_t ic = act ? i : i_begin;
-                merge_group<D>(act, h * n + ic, slot_base + (ic - rr * range) * kpad, a.list, k, nb,
-                               full_valid, lane, a.part_o, a.part_lse, a.out);
+            const int nq = int(i_end - i_begin);
+            const int nch = (nq + qs - 1) / qs;
+            const int64_t slot0 = (rg % kPartialRing) * ring_stride + (i_begin - rr * range) * kpad;
+            auto issue = [&](int c) {                // lane 0: chunk c into its stage
+                const uint32_t b = (sc + uint32_t(c)) % C::kMS;
+                const int qn = min(qs, nq - c * qs);
+                const uint32_t bo = uint32_t(qn * kpad * D * 2), bl = uint32_t(qn * kpad * 4);
+                const int64_t sl = slot0 + int64_t(c) * qs * kpad;
+                uint8_t *st = stage0 + b * kStageBytes;
+                tc::mbar_arrive_expect_tx(msbar + b, bo + bl);
+                tc::bulk_g2s(st, a.part_o + sl * D, bo, msbar + b);
+                tc::bulk_g2s(st + o_cap, a.part_lse + sl, bl, msbar + b);
+            };
+            if (lane == 0)
+                for (int c = 0; c < min(C::kMS, nch); ++c) issue(c);
+            bool ok = true;
+            for (int c = 0; c < nch; ++c) {
+                const uint32_t u = sc + uint32_t(c), b = u % C::kMS;
+                const int q0 = c * qs, qn = min(qs, nq - q0);
+                const uint8_t *st = stage0 + b * kStageBytes;
+                if (!tc::mbar_wait(msbar + b, (u / C::kMS) & 1, status)) {
+                    ok = false;
+                    break;
+                }
+                for (int q = 0; q < qn; q += QP) {
+                    const int jq = q + gq;                // groups past qn read nothing
+                    const bool act = jq < qn;
+                    const int64_t qrow = h * n + i_begin + q0 + (act ? jq : 0);
+                    uint32_t vm = act ? full_mask : 0u;
+                    if (full_valid == 0) {
+                        // lists with padding: a slot counts only if its id is a block
+                        vm = 0u;
+                        for (int s = gl; act && s < k; s += LPQ) {
+                            const int32_t bb = __ldg(a.list + qrow * k + s);
+                            if (bb >= 0 && bb < nb) vm |= 1u << s;
+                        }
+#pragma unroll
+                        for (int o = 1; o < LPQ; o <<= 1) vm |= __shfl_xor_sync(kFull, vm, o);
+                    }
+                    float acc[16];
+                    const uint16_t *po = reinterpret_cast<const uint16_t *>(st) + jq * kpad * D + gl * 16;
+                    const float *pl = reinterpret_cast<const float *>(st + o_cap) + jq * kpad;
+                    if (merge_query<D>(po, pl, vm, k, lane, acc)) {   // nothing listed: O stays 0
+                        uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow * D + gl * 16);
+                        dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                            pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                        dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                            pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+                    }
+                }
+                __syncwarp();                             // stage read by every lane
+                if (lane == 0 && c + C::kMS < nch) issue(c + C::kMS);
             }
-            __threadfence();
-            tc::named_bar_sync(kBarMerge, 128);
-            if (mt == 0) atomicAdd(a.merge_done + rg, 1);
+            if (!ok) break;
+            sc += uint32_t(nch);
+            if (lane == 0) red_add_release(a.merge_done + rg, 1);
         }
     }
 
@@ -706,22 +839,9 @@ bool make_rows_map(CUtensorMap *m, const void *base, int64_t bh, int64_t n, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows][d] bf16 viewed as 2-D, box 64 x 1 (one row per gathered row).
-bool make_gather_map(CUtensorMap *m, const void *base, int64_t rows, int d) {
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    cuuint64_t dims[2] = {cuuint64_t(d), cuuint64_t(rows)};
-    cuuint64_t strides[1] = {cuuint64_t(d) * 2};
-    cuuint32_t box[2] = {64, 1};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D>
-cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, cudaStream_t st) {
+cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorMap &mv,
+                     cudaStream_t st) {
     using C = Cfg<D>;
     auto kern = fine_ws_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal);
@@ -729,7 +849,7 @@ cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mq, const CUtensorM
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    kern<<<sms, kThreads, C::kTotal, st>>>(mq, mk, mv, a);   // one CTA per SM
+    kern<<<sms, kThreads, C::kTotal, st>>>(mk, mv, a);   // one CTA per SM
     return cudaGetLastError();
 }
 
@@ -740,12 +860,12 @@ bool fine_bm_supported(int32_t d, int32_t key_block) {
 }
 
 cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st) {
-    CUtensorMap mq, mk, mv;
-    if (!make_gather_map(&mq, a.q, a.bh * a.n, a.d) ||
-        !make_rows_map(&mk, a.k_ptr, a.bh, a.n, a.d, kB) || !make_rows_map(&mv, a.v_ptr, a.bh, a.n, a.d, kB))
+    if (a.k < 1 || a.k > 32) return cudaErrorInvalidValue;   // slot masks are 32 bits wide
+    CUtensorMap mk, mv;
+    if (!make_rows_map(&mk, a.k_ptr, a.bh, a.n, a.d, kB) || !make_rows_map(&mv, a.v_ptr, a.bh, a.n, a.d, kB))
         return cudaErrorInvalidValue;
-    if (a.d == 64) return launch_d<64>(a, mq, mk, mv, st);
-    return launch_d<128>(a, mq, mk, mv, st);
+    if (a.d == 64) return launch_d<64>(a, mk, mv, st);
+    return launch_d<128>(a, mk, mv, st);
 }
 
 }  // namespace bsa
