@@ -80,7 +80,7 @@ struct InvertBuffers {
     int2 *merge_items;      // [merge_cap] {range, first query}
     int32_t *n_fine;
     int32_t *n_merge;
-    int32_t *entries;       // [bh * n * k]
+    int32_t *entries;       // [bh * n * k] pair ids (flat query row << 5) | slot, by bin
 };
 // count + scan + scatter launches
 cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,

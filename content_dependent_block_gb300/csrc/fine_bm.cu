@@ -63,13 +63,17 @@ constexpr int kStageBytes = 17408;       // one merge stage: >= 2 queries at d =
 constexpr uint32_t kBarEpi = 1;
 constexpr unsigned kFull = 0xffffffffu;
 
+// Per-tile constants, computed once by the gather group: keys in the block
+// (kv < 64 only for a ragged last block), flat row of the range's first
+// query (qbase) and the range's offset in the partial-state ring (roff).
 struct TileInfo {
-    int32_t bin, p0, count, item, last, rg, end, pad;
+    int32_t bin, p0, count, item, last, rg, end, kv, qbase, roff, pad0, pad1;
 };
 
-// A fine item staged by the prefetcher: descriptor plus all its pair ids.
+// A fine item staged by the prefetcher: descriptor plus all its pair ids
+// ((flat query row << 5) | slot).
 struct StagedItem {
-    int32_t bin, first, end, rg, h, b, valid, pad;
+    int32_t bin, first, end, rg, h, b, valid, kv, qbase, roff, pad0, pad1;
     int32_t pid[kItemMax];
 };
 
@@ -91,7 +95,7 @@ struct Cfg {
     static constexpr int oML = oEpi + 4 * 2048;            // float2 [kNT][128]
     static constexpr int oPid = oML + kNT * kTile * 8;     // int32  [kNT][128]
     static constexpr int oTi = oPid + kNT * kTile * 4;     // TileInfo [kNT]
-    static constexpr int oItem = oTi + kNT * 32;           // StagedItem [kNI]
+    static constexpr int oItem = oTi + kNT * int(sizeof(TileInfo));   // StagedItem [kNI]
     static constexpr int oBar = oItem + kNI * int(sizeof(StagedItem));
     enum {
         bQFull = 0,
@@ -320,13 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
 #pragma unroll
                 for (int e = 0; e < kItemMax / 32; ++e) si->pid[e * 32 + lane] = v[e];
                 if (lane == 0) {
-                    const int64_t rg = bin / nb;
+                    const int64_t rg = bin / nb, b = bin - rg * nb;
+                    const int64_t h = rg / nranges, rr = rg - h * nranges;
                     si->bin = int32_t(bin);
                     si->first = item.y;
                     si->end = end;
                     si->rg = int32_t(rg);
-                    si->h = int32_t(rg / nranges);
-                    si->b = int32_t(bin % nb);
+                    si->h = int32_t(h);
+                    si->b = int32_t(b);
+                    si->kv = int32_t(i64min(kB, n - b * kB));
+                    si->qbase = int32_t(h * n + rr * range);
+                    si->roff = int32_t((rg % kPartialRing) * ring_stride);
                 }
             }
             if (lane == 0) si->valid = valid ? 1 : 0;
@@ -369,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const StagedItem *si = items + islot;
             if (!si->valid) break;
             const int32_t first = si->first, end = si->end, bin = si->bin, rg = si->rg;
+            const int32_t kv = si->kv, qbase = si->qbase, roff = si->roff;
             if (gw == 0) {
                 if (rg >= kPartialRing) {
                     // the ring entry must have been merged by its previous range
@@ -413,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 const int32_t *pp = si->pid + (p0 - first);
                 const int32_t my_pid = pp[gt < cnt ? gt : 0];
                 if (gt < cnt) pids[slot * kTile + gt] = my_pid;
-                const int32_t my_q = my_pid / k;             // flat query row h*n + i
+                const int32_t my_q = my_pid >> 5;            // flat query row h*n + i
                 uint8_t *sQ = sm + C::oQ + s * C::kQBytes;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -442,7 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     x.last = p0 + kTile >= end;
                     x.rg = rg;
                     x.end = 0;
-                    x.pad = 0;
+                    x.kv = kv;
+                    x.qbase = qbase;
+                    x.roff = roff;
+                    x.pad0 = x.pad1 = 0;
                     ti[slot] = x;
                 }
                 tc::mbar_arrive(bars + C::bTiFull + slot);
@@ -575,10 +587,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
             const int32_t end_flag = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
             if (end_flag) break;
-            const int64_t bin = reinterpret_cast<volatile TileInfo *>(ti + slot)->bin;
+            const int keys_valid = reinterpret_cast<volatile TileInfo *>(ti + slot)->kv;   // < 64: ragged
             if (!tc::mbar_wait(bars + C::bSFull + j, (g >> 1) & 1, status)) break;
             tc::tc_fence_after();
-            const int keys_valid = int(i64min(64, n - (bin % nb) * kB));   // < 64: ragged last block
             float mraw = -INFINITY;
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -649,20 +660,19 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (x_end) break;
             const int32_t x_count = reinterpret_cast<volatile TileInfo *>(ti + slot)->count;
             const int32_t x_rg = reinterpret_cast<volatile TileInfo *>(ti + slot)->rg;
+            const int32_t x_qbase = reinterpret_cast<volatile TileInfo *>(ti + slot)->qbase;
+            const int32_t x_roff = reinterpret_cast<volatile TileInfo *>(ti + slot)->roff;
             if (!tc::mbar_wait(bars + C::bOFull + j, (g >> 1) & 1, status)) break;
             if (!tc::mbar_wait(bars + C::bMlFull + slot, (g / kNT) & 1, status)) break;
             tc::tc_fence_after();
             const float2 mlv = ml[slot * kTile + row];
             const bool has = row < x_count;
-            int64_t part = 0;
+            int32_t part = 0;                               // < kPartialRing * range * kpad
             if (has) {
                 const int32_t pid = pids[slot * kTile + row];
-                const int64_t qrow = pid / k;
-                const int64_t s = pid - qrow * k;
-                const int64_t h = x_rg / nranges, rr = x_rg % nranges;
-                part = (x_rg % kPartialRing) * ring_stride + (qrow - h * n - rr * range) * kpad + s;
+                part = x_roff + ((pid >> 5) - x_qbase) * int32_t(kpad) + (pid & 31);
             }
-            int64_t sp[4];                                    // part of rows 8i + srow
+            int32_t sp[4];                                    // part of rows 8i + srow
             bool sh[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -698,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                         const uint4 val =
                             *reinterpret_cast<const uint4 *>(eb + r * 64 + ((spiece ^ ((r >> 1) & 3)) << 4));
                         if (sh[i])
-                            *reinterpret_cast<uint4 *>(a.part_o + sp[i] * D + c0 + hf * 32 + spiece * 8) = val;
+                            *reinterpret_cast<uint4 *>(a.part_o + int64_t(sp[i]) * D + c0 + hf * 32 + spiece * 8) = val;
                     }
                     __syncwarp();
                 }

@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
         const int32_t b = __ldg(lh + e);
         if (valid_block(b, nb)) {
             const int32_t r = atomicAdd(&hist[b], 1);
-            entries[base[b] + r] = int32_t(h * n * k + e);
+            const int64_t i = e / k;
+            entries[base[b] + r] = int32_t(((h * n + i) << 5) | (e - i * k));
         }
     }
     // queries whose list admits nothing: their output is zero
