@@ -57,6 +57,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-forwards", type=int, default=0, metavar="N",
+                   help="run N untimed forwards of the workload and exit (a fixed launch "
+                        "sequence for profilers: 6 kernels per forward); prints no JSON")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU seconds of the oracle sample")
     args = p.parse_args(argv)
@@ -286,6 +289,14 @@ def main(argv=None):
     fwd = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk, device=device)
     fwd(q, k, v)
     torch.cuda.synchronize(device)
+    if args.profile_forwards > 0:
+        for _ in range(args.profile_forwards - 1):
+            fwd(q, k, v)
+        torch.cuda.synchronize(device)
+        status = bsa.device_status()
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0 if status == 0 else 1
     peak_mb = (torch.cuda.max_memory_allocated(device) - mem0) / 2**20
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)

@@ -16,7 +16,7 @@
 //   scan     exclusive prefix over the bins -> CSR offsets, plus the work
 //            list of the fine stage (fine items per bin, merge items per
 //            range, see scan_kernel)
-//   scatter  writes every pair id p = (h*n + i)*k + s into its block's
+//   scatter  writes every pair id p = ((h*n + i) << 5) | s into its block's
 //            range (order inside a range is arbitrary; results do not
 //            depend on it); queries with no valid slot get O = 0 here
 //
@@ -29,9 +29,16 @@ namespace bsa {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kQueriesPerCta = 1024;   // queries of one head per count/scatter CTA
+constexpr int kQueriesPerCta = 256;    // queries of one head per count/scatter CTA
+constexpr int kScanThreads = 1024;
+constexpr int kScanV = 4;              // bins per thread per scan chunk
+static_assert(kFineBmItemPairs == 512, "fine items are cut at 512 pairs (shift below)");
 
 __device__ __forceinline__ bool valid_block(int32_t b, int64_t nb) { return b >= 0 && b < nb; }
+
+// floor(e / k) for 0 <= e < 2^16 and 1 <= k <= 32: e * ceil(2^32 / k) / 2^32,
+// exact because the rounding error (< e / 2^32) stays below 1 / k.
+__device__ __forceinline__ uint32_t div_small(uint32_t e, uint32_t magic) { return __umulhi(e, magic); }
 
 // grid: (ceil(n / kQueriesPerCta), bh); dynamic smem: nb ints
 __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restrict__ list,
@@ -45,28 +52,31 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restri
     const int64_t i1 = i64min(n, i0 + kQueriesPerCta);
     for (int64_t b = threadIdx.x; b < nb; b += kThreads) hist[b] = 0;
     __syncthreads();
-    const int32_t *base = list + (h * n) * k;
+    const int32_t *base = list + (h * n + i0) * k;
+    const int32_t m = int32_t((i1 - i0) * k);
     bool bad = false;
-    for (int64_t e = i0 * k + threadIdx.x; e < i1 * k; e += kThreads) {
+    for (int32_t e = threadIdx.x; e < m; e += kThreads) {
         const int32_t b = __ldg(base + e);
         if (valid_block(b, nb)) atomicAdd(&hist[b], 1);
         else if (b >= 0 || b < -1) bad = true;
     }
     if (bad) report_status(status, kStatusBadIndex);
     __syncthreads();
-    const int64_t bin0 = (h * nranges + i0 / range) * nb;
+    int32_t *dst = counts + (h * nranges + i0 / range) * nb;
     for (int64_t b = threadIdx.x; b < nb; b += kThreads)
-        if (hist[b] != 0) atomicAdd(counts + bin0 + b, hist[b]);
+        if (hist[b] != 0) atomicAdd(dst + b, hist[b]);
 }
 
-// Block-wide exclusive scan of two int64 values per thread (1024 threads).
-__device__ __forceinline__ void block_scan2(int64_t &a, int64_t &b, int64_t *wa, int64_t *wb) {
+// Block-wide exclusive scan of two int32 values per thread (kScanThreads
+// threads); also returns the block totals.
+__device__ __forceinline__ void block_scan2(int32_t &a, int32_t &b, int32_t &ta, int32_t &tb,
+                                            int32_t *wa, int32_t *wb) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t a0 = a, b0 = b;
+    const int32_t a0 = a, b0 = b;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int64_t x = __shfl_up_sync(0xffffffffu, a, o);
-        const int64_t y = __shfl_up_sync(0xffffffffu, b, o);
+        const int32_t x = __shfl_up_sync(0xffffffffu, a, o);
+        const int32_t y = __shfl_up_sync(0xffffffffu, b, o);
         if (lane >= o) {
             a += x;
             b += y;
@@ -78,11 +88,11 @@ __device__ __forceinline__ void block_scan2(int64_t &a, int64_t &b, int64_t *wa,
     }
     __syncthreads();
     if (warp == 0) {
-        int64_t x = wa[lane], y = wb[lane];
+        int32_t x = wa[lane], y = wb[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int64_t u = __shfl_up_sync(0xffffffffu, x, o);
-            const int64_t v = __shfl_up_sync(0xffffffffu, y, o);
+            const int32_t u = __shfl_up_sync(0xffffffffu, x, o);
+            const int32_t v = __shfl_up_sync(0xffffffffu, y, o);
             if (lane >= o) {
                 x += u;
                 y += v;
@@ -94,90 +104,106 @@ __device__ __forceinline__ void block_scan2(int64_t &a, int64_t &b, int64_t *wa,
     __syncthreads();
     a = a - a0 + (warp > 0 ? wa[warp - 1] : 0);
     b = b - b0 + (warp > 0 ? wb[warp - 1] : 0);
+    ta = wa[31];
+    tb = wb[31];
     __syncthreads();
 }
 
 // One CTA of 1024 threads.  Builds the CSR offsets over the bins
 // (range-major: bin = range * nb + block, range = head * nranges + r) and
 // the two work lists of the fine stage: fine items {bin, first pair} (at
-// most item_pairs pairs each) in bin order, and merge items {range, first
-// query} (qm queries each) in range order.
-__global__ void __launch_bounds__(1024) scan_kernel(
+// most 512 pairs each) in bin order, and merge items {range, first query}
+// (qm queries each) in range order.  Bins are scanned in coalesced chunks of
+// 4 bins per thread with a running carry.
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(
     const int32_t *__restrict__ counts, int64_t nb, int64_t nr, int64_t nranges, int64_t range,
     int64_t n, int32_t item_pairs, int32_t qm, int32_t *__restrict__ offsets,
     int32_t *__restrict__ fitem_off, int32_t *__restrict__ fpre, int32_t *__restrict__ mpre,
     int32_t *__restrict__ range_total, int32_t *__restrict__ range_merges,
     int2 *__restrict__ fine_items, int2 *__restrict__ merge_items, int32_t *__restrict__ n_fine,
     int32_t *__restrict__ n_merge) {
-    __shared__ int64_t wa[32], wb[32];
+    __shared__ int32_t wa[32], wb[32];
     const int t = threadIdx.x;
-    const int64_t nbins = nr * nb;
-    // 1. bins: pair offsets and fine-item offsets
-    const int64_t per = (nbins + 1023) / 1024;
-    const int64_t e0 = i64min(nbins, t * per), e1 = i64min(nbins, e0 + per);
-    int64_t pairs = 0, fitems = 0;
-    for (int64_t e = e0; e < e1; ++e) {
-        const int64_t c = counts[e];
-        pairs += c;
-        fitems += (c + item_pairs - 1) / item_pairs;
+    const int32_t nbins = int32_t(nr * nb);
+    // 1. bins: pair offsets, fine-item offsets and the fine items themselves
+    int32_t carry_p = 0, carry_f = 0;
+    for (int32_t base = 0; base < nbins; base += kScanThreads * kScanV) {
+        const int32_t e = base + t * kScanV;
+        int32_t c[kScanV];
+        if (e + kScanV <= nbins) {
+            const int4 v = *reinterpret_cast<const int4 *>(counts + e);   // 16-byte aligned
+            c[0] = v.x, c[1] = v.y, c[2] = v.z, c[3] = v.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < kScanV; ++j) c[j] = e + j < nbins ? counts[e + j] : 0;
+        }
+        int32_t p = 0, f = 0;
+#pragma unroll
+        for (int j = 0; j < kScanV; ++j) {
+            p += c[j];
+            f += (c[j] + 511) >> 9;
+        }
+        int32_t tp, tf;
+        block_scan2(p, f, tp, tf, wa, wb);
+        p += carry_p;
+        f += carry_f;
+#pragma unroll
+        for (int j = 0; j < kScanV; ++j) {
+            if (e + j >= nbins) break;
+            offsets[e + j] = p;
+            fitem_off[e + j] = f;
+            for (int32_t x = 0; x < c[j]; x += 512) fine_items[f++] = make_int2(e + j, x);
+            p += c[j];
+        }
+        carry_p += tp;
+        carry_f += tf;
     }
-    int64_t poff = pairs, foff = fitems;
-    block_scan2(poff, foff, wa, wb);
-    for (int64_t e = e0; e < e1; ++e) {
-        const int64_t c = counts[e];
-        offsets[e] = int32_t(poff);
-        fitem_off[e] = int32_t(foff);
-        poff += c;
-        foff += (c + item_pairs - 1) / item_pairs;
-    }
-    if (t == 1023) {
-        offsets[nbins] = int32_t(poff);
-        fitem_off[nbins] = int32_t(foff);
-    }
-    __syncthreads();
-    // 2. ranges: pair totals, fine-item and merge-item prefixes
-    const int64_t rper = (nr + 1023) / 1024;
-    const int64_t r0 = i64min(nr, t * rper), r1 = i64min(nr, r0 + rper);
-    int64_t f_sum = 0, m_sum = 0;
-    for (int64_t r = r0; r < r1; ++r) {
-        const int64_t rr = r % nranges;
-        const int64_t queries = i64min(range, n - rr * range);
-        const int64_t m = (queries + qm - 1) / qm;
-        range_total[r] = offsets[(r + 1) * nb] - offsets[r * nb];
-        range_merges[r] = int32_t(m);
-        f_sum += fitem_off[(r + 1) * nb] - fitem_off[r * nb];
-        m_sum += m;
-    }
-    int64_t fo = f_sum, mo = m_sum;
-    block_scan2(fo, mo, wa, wb);
-    for (int64_t r = r0; r < r1; ++r) {
-        fpre[r] = int32_t(fo);
-        mpre[r] = int32_t(mo);
-        fo += fitem_off[(r + 1) * nb] - fitem_off[r * nb];
-        mo += range_merges[r];
-    }
-    if (t == 1023) {
-        fpre[nr] = int32_t(fo);
-        fpre[nr + 1] = int32_t(fo);
-        mpre[nr] = int32_t(mo);
-        *n_fine = int32_t(fo);
-        *n_merge = int32_t(mo);
+    if (t == 0) {
+        offsets[nbins] = carry_p;
+        fitem_off[nbins] = carry_f;
+        *n_fine = carry_f;
     }
     __syncthreads();
-    // 3. the work lists: fine items in bin order, merge items in range order
-    for (int64_t e = e0; e < e1; ++e) {
-        const int64_t c = counts[e];
-        int64_t pos = fitem_off[e];
-        for (int64_t f = 0; f < c; f += item_pairs) fine_items[pos++] = make_int2(int(e), int(f));
+    // 2. ranges: pair totals, merge-item counts and prefixes
+    int32_t carry_m = 0;
+    for (int64_t base = 0; base < nr; base += kScanThreads) {
+        const int64_t r = base + t;
+        int32_t m = 0, dummy = 0;
+        if (r < nr) {
+            const int64_t rr = r % nranges;
+            const int64_t queries = i64min(range, n - rr * range);
+            m = int32_t((queries + qm - 1) / qm);
+            range_total[r] = offsets[(r + 1) * nb] - offsets[r * nb];
+            range_merges[r] = m;
+            fpre[r] = fitem_off[r * nb];
+        }
+        int32_t mo = m, tm, td;
+        block_scan2(mo, dummy, tm, td, wa, wb);
+        if (r < nr) mpre[r] = carry_m + mo;
+        carry_m += tm;
     }
-    for (int64_t r = r0; r < r1; ++r) {
-        int64_t pos = mpre[r];
-        for (int64_t j = 0; j < range_merges[r]; ++j)
-            merge_items[pos++] = make_int2(int(r), int(j * qm));
+    if (t == 0) {
+        fpre[nr] = carry_f;
+        fpre[nr + 1] = carry_f;
+        mpre[nr] = carry_m;
+        *n_merge = carry_m;
+    }
+    __syncthreads();
+    // 3. merge items, one per thread.  Every head has the same ranges: full
+    //    ones with range / qm items and a last one with m_last items, so the
+    //    range of item mi follows in closed form.
+    const int32_t m_full = int32_t(range / qm);
+    const int32_t m_last = int32_t((n - (nranges - 1) * range + qm - 1) / qm);
+    const int32_t m_head = int32_t(nranges - 1) * m_full + m_last;
+    for (int32_t mi = t; mi < carry_m; mi += kScanThreads) {
+        const int32_t hh = mi / m_head, rem = mi - hh * m_head;
+        const int32_t rr = min(rem / m_full, int32_t(nranges - 1));
+        const int32_t j = rem - rr * m_full;
+        merge_items[mi] = make_int2(int(hh * nranges + rr), j * qm);
     }
 }
 
-// grid: (ceil(n / kQueriesPerCta), bh); dynamic smem: 2 * nb ints
+// grid: (ceil(n / kQueriesPerCta), bh); dynamic smem: 2 * nb + kQueriesPerCta ints
 template <typename OutT>
 __global__ void __launch_bounds__(kThreads) scatter_kernel(
     const int32_t *__restrict__ list, int64_t n, int64_t nb, int32_t k, int64_t range,
@@ -186,13 +212,16 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
     extern __shared__ int32_t sm[];
     int32_t *hist = sm;          // pairs of this CTA per block
     int32_t *base = sm + nb;     // first slot of this CTA inside the block's range
+    int32_t *any = sm + 2 * nb;  // per query of the CTA: some slot is a block
     const int64_t h = blockIdx.y;
     const int64_t i0 = int64_t(blockIdx.x) * kQueriesPerCta;
     const int64_t i1 = i64min(n, i0 + kQueriesPerCta);
     for (int64_t b = threadIdx.x; b < nb; b += kThreads) hist[b] = 0;
+    for (int q = threadIdx.x; q < kQueriesPerCta; q += kThreads) any[q] = 0;
     __syncthreads();
-    const int32_t *lh = list + (h * n) * k;
-    for (int64_t e = i0 * k + threadIdx.x; e < i1 * k; e += kThreads) {
+    const int32_t *lh = list + (h * n + i0) * k;
+    const int32_t m = int32_t((i1 - i0) * k);
+    for (int32_t e = threadIdx.x; e < m; e += kThreads) {
         const int32_t b = __ldg(lh + e);
         if (valid_block(b, nb)) atomicAdd(&hist[b], 1);
     }
@@ -204,19 +233,21 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
         hist[b] = 0;
     }
     __syncthreads();
-    for (int64_t e = i0 * k + threadIdx.x; e < i1 * k; e += kThreads) {
+    const uint32_t magic = 0xFFFFFFFFu / uint32_t(k) + 1u;
+    const int32_t row0 = int32_t(h * n + i0);
+    for (int32_t e = threadIdx.x; e < m; e += kThreads) {
         const int32_t b = __ldg(lh + e);
         if (valid_block(b, nb)) {
+            const int32_t il = int32_t(div_small(uint32_t(e), magic));
             const int32_t r = atomicAdd(&hist[b], 1);
-            const int64_t i = e / k;
-            entries[base[b] + r] = int32_t(((h * n + i) << 5) | (e - i * k));
+            entries[base[b] + r] = ((row0 + il) << 5) | (e - il * k);
+            any[il] = 1;
         }
     }
+    __syncthreads();
     // queries whose list admits nothing: their output is zero
     for (int64_t i = i0 + threadIdx.x; i < i1; i += kThreads) {
-        bool any = false;
-        for (int s = 0; s < k; ++s) any |= valid_block(__ldg(lh + i * k + s), nb);
-        if (!any) {
+        if (!any[i - i0]) {
             OutT *o = out + (h * n + i) * d;
             for (int c = 0; c < d; ++c) o[c] = OutT(0);
         }
@@ -226,8 +257,9 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
 }  // namespace
 
 int64_t invert_query_range(int64_t n, int64_t nb, int32_t k) {
-    // about two full 128-pair tiles per (range, block) on average
-    int64_t r = kQueriesPerCta;
+    // about two full 128-pair tiles per (range, block) on average; a power
+    // of two >= 1024, so a count/scatter CTA never straddles two ranges
+    int64_t r = 1024;
     while (r * k < int64_t(256) * nb && r < n) r *= 2;
     return r;
 }
@@ -251,23 +283,24 @@ cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb
                           int32_t d, int32_t *status, cudaStream_t st) {
     const dim3 grid(unsigned((n + kQueriesPerCta - 1) / kQueriesPerCta), unsigned(bh));
     const size_t smem1 = size_t(nb) * sizeof(int32_t);
+    const size_t smem2 = 2 * smem1 + kQueriesPerCta * sizeof(int32_t);
     cudaError_t e = cudaSuccess;
     if (smem1 > 48 * 1024 &&
         (e = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(smem1))) != cudaSuccess)
         return e;
-    if (2 * smem1 > 48 * 1024 &&
+    if (smem2 > 48 * 1024 &&
         (e = cudaFuncSetAttribute(scatter_kernel<uint16_t>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(2 * smem1))) !=
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem2))) !=
             cudaSuccess)
         return e;
     count_kernel<<<grid, kThreads, smem1, st>>>(list, n, nb, k, p.range, p.nranges, w.counts,
                                                status);
-    scan_kernel<<<1, 1024, 0, st>>>(w.counts, nb, p.nr, p.nranges, p.range, n, p.item_pairs, p.qm,
+    scan_kernel<<<1, kScanThreads, 0, st>>>(w.counts, nb, p.nr, p.nranges, p.range, n, p.item_pairs, p.qm,
                                     w.offsets, w.fitem_off, w.fpre, w.mpre, w.range_total,
                                     w.range_merges, w.fine_items, w.merge_items, w.n_fine,
                                     w.n_merge);
-    scatter_kernel<uint16_t><<<grid, kThreads, 2 * smem1, st>>>(list, n, nb, k, p.range,
+    scatter_kernel<uint16_t><<<grid, kThreads, smem2, st>>>(list, n, nb, k, p.range,
                                                                 p.nranges, w.offsets, w.cursors,
                                                                 w.entries, out_bf16, d);
     return cudaGetLastError();

@@ -181,8 +181,9 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k,
  *     device that loads the library holds it until the process exits.  A
  *     problem whose bsa_forward_workspace_size() exceeds 32 MiB is rejected
  *     with BSA_ERR_WORKSPACE (2 heads x 1024 tokens, top-4 needs about
- *     1.6 MiB and fits; 8 heads x 8192 tokens, top-16 needs about 21 MiB;
- *     the workspace grows with heads * n * k).
+ *     2.1 MiB and fits; 8 heads x 8192 tokens, top-16 needs about 25 MiB
+ *     and fits; 8 heads x 32768 tokens, top-16 needs about 100 MiB and is
+ *     rejected; the workspace grows with heads * n * k).
  *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
  *     call.  The first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current; make that
