@@ -11,10 +11,17 @@
 // chunks of kChunk = 128 blocks (MMA N = 128), double-buffered in shared
 // memory and in tensor memory:
 //   warp 0      TMA producer: Q tile once, then Kbar chunks (hi and lo parts)
-//   warp 1      allocates tensor memory; one lane issues the MMAs
-//   warps 2..5  epilogue: each thread reads its query's scores from tensor
-//               memory (tcgen05.ld 32 columns at a time) and keeps a running
-//               top-k in registers
+//   warp 1      allocates tensor memory; runs the MMA loop warp-uniformly and
+//               one elected lane issues
+//   warps 2..9  epilogue, two groups of four warps (one per TMEM lane
+//               quadrant); group e reads the 32-column slices j = e mod 2 of
+//               every chunk, so each thread scans half of its query's scores
+//               and keeps a running top-k in registers; the two lists are
+//               merged at the end
+// Selection: each 16-score slice is first filtered without branches against
+// the thread's current k-th key into a small shared-memory queue, and only
+// the survivors go through the sorted insertion, so a warp runs insertions
+// for the lanes that need them instead of for every score.
 // Precision: Kbar enters as a bf16 pair (hi = bf16(Kbar), lo = bf16(Kbar -
 // hi)); S = Q.hi + Q.lo accumulates in fp32, i.e. about 2^-16 relative to
 // the fp32 mean -- far inside the 1e-3 relative tie band of the selection.
@@ -40,8 +47,12 @@ namespace {
 constexpr int kTileM = 128;        // queries per CTA (TMEM lanes)
 constexpr int kChunk = 128;        // blocks per MMA (N)
 constexpr int kStages = 2;         // shared-memory stages of Kbar chunks
-constexpr int kThreads = 192;      // 6 warps
+constexpr int kGroups = 2;         // epilogue warpgroups (column split)
+constexpr int kEpi = kGroups * kTileM;
+constexpr int kThreads = 64 + kEpi;
 constexpr int kTmemCols = 2 * kChunk;
+constexpr int kQueue = 16;         // filtered keys per thread per slice
+constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>
 struct CoarseSmem {
@@ -50,7 +61,10 @@ struct CoarseSmem {
     static constexpr int kKBytes = kSub * kChunk * 128;       // one of hi / lo
     static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kTiles = kQBytes + kStages * kStageBytes;
-    static constexpr int kTotal = kTiles + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int oQueue = kTiles;                     // uint32 [kQueue][kEpi]; after the
+                                                              // scan, [KMAX <= 32][kTileM] lists
+    static constexpr int oBar = oQueue + kQueue * kEpi * 4;
+    static constexpr int kTotal = oBar + 256 /*barriers*/ + 1024 /*align*/;
 };
 
 __device__ __forceinline__ uint32_t score_key(float s, uint32_t col, uint32_t mask) {
@@ -70,7 +84,7 @@ __device__ __forceinline__ void key_insert(uint32_t (&L)[KMAX], uint32_t key) {
 }
 
 template <int D, int KMAX>
-__global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
+__global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_hi,
     const __grid_constant__ CUtensorMap tm_lo, int64_t n, int64_t nb, int32_t topk,
     uint32_t key_mask, int32_t *__restrict__ idx, int32_t *status) {
@@ -79,7 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
     uint8_t *smem = tc::align_smem_1024(smem_raw);
     uint8_t *sQ = smem;
     uint8_t *sK = smem + S::kQBytes;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::kTiles);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::oBar);
+    uint32_t *queue = reinterpret_cast<uint32_t *>(smem + S::oQueue);
+    uint32_t *merge = queue;                // reused once every queue is drained
     uint64_t *q_full = bars + 0;
     uint64_t *kv_full = bars + 1;       // [kStages]
     uint64_t *kv_empty = bars + 3;      // [kStages]
@@ -103,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(acc_full + s, 1);
-            tc::mbar_init(acc_empty + s, kTileM);
+            tc::mbar_init(acc_empty + s, kEpi);
         }
         tc::fence_barrier_init();
     }
@@ -146,17 +162,20 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileM, kChunk);
-            bool ok = tc::mbar_wait(q_full, 0, status);
-            const uint32_t q_addr = tc::smem_u32(sQ);
-            for (int c = 0; ok && c < nchunks; ++c) {
-                const int s = c % kStages;
-                const int buf = c & 1;
-                if (!tc::mbar_wait(kv_full + s, (c / kStages) & 1, status)) break;
-                if (c >= 2 && !tc::mbar_wait(acc_empty + buf, ((c >> 1) - 1) & 1, status)) break;
-                tc::tc_fence_after();
+        // ---------------------------------------------------- MMA issuer
+        // warp-uniform loop, one elected lane issues
+        constexpr uint32_t idesc = tc::idesc_bf16_f32(kTileM, kChunk);
+        bool ok = tc::mbar_wait(q_full, 0, status);
+        ok = __all_sync(kFull, ok);
+        const uint32_t q_addr = tc::smem_u32(sQ);
+        for (int c = 0; ok && c < nchunks; ++c) {
+            const int s = c % kStages;
+            const int buf = c & 1;
+            ok = tc::mbar_wait(kv_full + s, (c / kStages) & 1, status);
+            if (ok && c >= 2) ok = tc::mbar_wait(acc_empty + buf, ((c >> 1) - 1) & 1, status);
+            if (!__all_sync(kFull, ok)) break;
+            tc::tc_fence_after();
+            if (tc::elect_one()) {
                 const uint32_t hi_addr = tc::smem_u32(sK + s * S::kStageBytes);
                 const uint32_t lo_addr = hi_addr + S::kKBytes;
                 const uint32_t d_tmem = tmem + uint32_t(buf * kChunk);
@@ -177,11 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
                 tc::mma_commit(kv_empty + s);
                 tc::mma_commit(acc_full + buf);
             }
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------------ epilogue
+        const int eg = (warp - 2) >> 2;            // column group
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row inside the tile
+        uint32_t *qu = queue + eg * kTileM + r;    // [kQueue][kEpi], this thread's column
         uint32_t L[KMAX];
 #pragma unroll
         for (int t = 0; t < KMAX; ++t) L[t] = 0u;  // 0 = empty (below every real key)
@@ -192,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
             tc::tc_fence_after();
             if (ok) {
                 const int valid = int(i64min(kChunk, nb - int64_t(c) * kChunk));
-                for (int j = 0; j < kChunk / 32; ++j) {
+                for (int j = eg; j < kChunk / 32; j += kGroups) {
                     if (j * 32 >= valid) break;
                     uint32_t v[32];
                     tc::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kChunk + j * 32), v);
@@ -200,9 +222,19 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
                     const uint32_t col0 = uint32_t(c * kChunk + j * 32);
                     const int lim = valid - j * 32;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        if (e < lim) {
-                            const uint32_t key = score_key(__uint_as_float(v[e]), col0 + e, key_mask);
+                    for (int hf = 0; hf < 2; ++hf) {
+                        // branch-free filter against the current k-th key
+                        const uint32_t thr = L[KMAX - 1];
+                        int cnt = 0;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int x = hf * 16 + e;
+                            const uint32_t key = score_key(__uint_as_float(v[x]), col0 + x, key_mask);
+                            qu[cnt * kEpi] = key;
+                            cnt += (x < lim && key > thr) ? 1 : 0;
+                        }
+                        for (int t = 0; t < cnt; ++t) {
+                            const uint32_t key = qu[t * kEpi];
                             if (key > L[KMAX - 1]) key_insert<KMAX>(L, key);
                         }
                     }
@@ -211,8 +243,21 @@ __global__ void __launch_bounds__(kThreads, 1) coarse_topk_tc_kernel(
             tc::tc_fence_before();
             tc::mbar_arrive(acc_empty + buf);
         }
+        // group 1 hands its list to group 0, which merges and writes
+        static_assert(KMAX * kTileM <= kQueue * kEpi, "merge lists fit the queue region");
+        tc::named_bar_sync(1, kEpi);               // every queue drained
+        if (eg == 1) {
+#pragma unroll
+            for (int t = 0; t < KMAX; ++t) merge[t * kTileM + r] = L[t];
+        }
+        tc::named_bar_sync(1, kEpi);
         const int64_t i = row0 + r;
-        if (i < n) {
+        if (eg == 0 && i < n) {
+#pragma unroll
+            for (int t = 0; t < KMAX; ++t) {
+                const uint32_t key = merge[t * kTileM + r];
+                if (key > L[KMAX - 1]) key_insert<KMAX>(L, key);
+            }
             int ids[KMAX];
             const int kk = int(i64min(topk, nb));
 #pragma unroll

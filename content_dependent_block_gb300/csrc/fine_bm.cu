@@ -8,16 +8,16 @@
 // selected the block.  One persistent CTA per SM runs six warp roles that
 // hand work to each other through mbarrier rings in shared memory:
 //
-//   prefetch  (warp 13)     takes fine items (one bin, <= 512 pairs) from a
+//   prefetch  (warp 12)     takes fine items (one bin, <= 512 pairs) from a
 //                           global queue and stages each item's descriptor
 //                           and pair ids in a shared-memory ring
-//   gather    (warps 0-3)   per staged item: loads K_b, V_b by TMA (128-byte
+//   gather    (4 warps)     per staged item: loads K_b, V_b by TMA (128-byte
 //                           swizzle, one buffer per item in flight); per tile
 //                           of 128 pairs, 128 threads copy the query rows
 //                           with cp.async straight into the swizzled operand
 //                           layout, and publish a tile once the next one is
 //                           in flight (or before any wait that may block)
-//   MMA       (warp 12)     S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
+//   MMA       (warp 0)      S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
 //                           one of two TMEM score buffers, then O[j] = P . V_b
 //                           (N = d, V MN-major) into one of two TMEM outputs;
 //                           an event loop that issues whichever is ready
@@ -26,7 +26,7 @@
 //   epilogue  (warps 8-11)  reads O, stores the pair's partial state
 //                           o = O / l (bf16) and lse = m + log2 l into a ring
 //                           of query ranges, counts the range's finished pairs
-//   merge     (warps 14-15) each takes merge items (256 queries of one range)
+//   merge     (2 warps)     each takes merge items (256 queries of one range)
 //                           from a second queue once the range's pairs are all
 //                           done, pulls the queries' partial states into
 //                           shared-memory stages with bulk copies and merges
@@ -56,7 +56,20 @@ constexpr int kNI = 2;                   // staged fine-item ring
 constexpr int kItemMax = 512;            // pairs per fine item (kFineBmItemPairs)
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kWarpSoftmax = 4, kWarpEpi = 8, kWarpMma = 12, kWarpFetch = 13, kWarpMerge = 14;
+// Warp w runs on SM sub-partition w % 4.  Softmax and epilogue need one warp
+// per TMEM lane quadrant (w % 4 = 0..3); the other roles are placed so that
+// no sub-partition runs more than three different role code paths:
+//   partition 0: MMA (0), softmax, epilogue, prefetch (12)
+//   partitions 1, 2: gather (1, 13 and 2, 14), softmax, epilogue
+//   partition 3: merge (3, 15), softmax, epilogue
+constexpr int kWarpMma = 0, kWarpFetch = 12;
+constexpr int kWarpSoftmax = 4, kWarpEpi = 8;            // 4-7, 8-11
+__device__ __forceinline__ int gather_index(int w) {     // warps 1, 13, 2, 14 -> 0..3
+    return w == 1 ? 0 : w == 13 ? 1 : w == 2 ? 2 : w == 14 ? 3 : -1;
+}
+__device__ __forceinline__ int merge_index(int w) {      // warps 3, 15 -> 0, 1
+    return w == 3 ? 0 : w == 15 ? 1 : -1;
+}
 constexpr int kGather = 128;             // gather threads (warps 0-3)
 constexpr int kMergeWarps = 2;
 constexpr int kStageBytes = 17408;       // one merge stage: >= 2 queries at d = 128, k = 32
@@ -131,17 +144,23 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
 }
 
 // Bounded wait until *p >= target (acquire).  False on timeout, or when
-// another wait in the grid already timed out.
+// another wait in the grid already timed out.  The (slow) global timer is read
+// only every 64 polls.
 __device__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status) {
     if (ld_acquire(p) >= target) return true;
-    const uint64_t t0 = tc::global_ns();
-    for (;;) {
+    uint64_t t0 = 0;
+    for (uint32_t spin = 1;; ++spin) {
         __nanosleep(64);
         if (ld_acquire(p) >= target) return true;
-        if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return false;
-        if (tc::global_ns() - t0 > tc::kWaitLimitNs) {
-            report_status(status, kStatusTimeout);
-            return false;
+        if ((spin & 63u) == 0) {
+            if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return false;
+            const uint64_t now = tc::global_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > tc::kWaitLimitNs) {
+                report_status(status, kStatusTimeout);
+                return false;
+            }
         }
     }
 }
@@ -342,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::mbar_arrive(bars + C::bItFull + slot);
             if (!valid) break;
         }
-    } else if (warp < kWarpSoftmax) {
+    } else if (gather_index(warp) >= 0) {
         // --------------------------------------------------------- gather
         // Thread gt owns pair row gt of each tile (its pid and query row);
         // for the copies, lane l of warp gw moves 16-byte chunk (l & 7) of
@@ -351,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         // arrive) once kLag later tiles are in flight, or before any wait
         // that may block.
         constexpr int kLag = C::kNQ - 1;
-        const int gw = warp, gt = threadIdx.x;
+        const int gw = gather_index(warp), gt = gw * 32 + lane;
         const int chunk = lane & 7, rsub = lane >> 3;
         int g = 0, item_idx = 0, npend = 0;      // tiles g - npend .. g - 1 unpublished
         bool ok = true;
@@ -574,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             }
         }
         __syncwarp();
-    } else if (warp < kWarpEpi) {
+    } else if (warp >= kWarpSoftmax && warp < kWarpEpi) {
         // -------------------------------------------------------- softmax
         // One thread per score row, in two passes over the row in TMEM (32
         // columns at a time, rolled loops to keep the code small): the row
@@ -640,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(bars + C::bPFull + j);
         }
-    } else if (warp < kWarpMma) {
+    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
         // ------------------------------------------------------- epilogue
         // Thread `row` owns one pair: o = O / l (bf16) and lse = m + log2 l.
         // O is read from TMEM 64 columns at a time (the buffer is released
@@ -721,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 tc::mbar_arrive(bars + C::bTiFree + slot);
             }
         }
-    } else if (warp >= kWarpMerge) {
+    } else if (merge_index(warp) >= 0) {
         // ---------------------------------------------------------- merge
         // Each merge warp runs on its own: it takes a merge item, waits for
         // the range's pairs, then streams the item's queries through its
@@ -730,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         // D/16 lanes merges one query, each lane owning 16 channels.
         constexpr int LPQ = D / 16;                  // lanes per query
         constexpr int QP = 32 / LPQ;                 // queries per pass
-        const int mw = warp - kWarpMerge;
+        const int mw = merge_index(warp);
         const int gq = lane / LPQ, gl = lane % LPQ;
         const int n_merge = *a.w.n_merge;
         const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;

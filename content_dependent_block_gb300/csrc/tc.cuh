@@ -91,22 +91,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Gives up
-// after kWaitLimitNs, or as soon as another wait in the grid has (the status
-// word then already holds BSA_ERR_TIMEOUT).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
+// after about kWaitLimitNs, or as soon as another wait in the grid has (the
+// status word then already holds BSA_ERR_TIMEOUT).  The global timer is slow
+// to read, so it is read only every 1024 probes: a wait that ends within the
+// first probes costs no timer read at all.
+// The polling loop is kept out of line: the wait sites are many and the
+// instruction cache is shared by every warp role of an SM sub-partition.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int32_t *status) {
+    uint64_t t0 = 0;
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255u) == 0) {
+        if ((spin & 1023u) == 0) {
             if (status != nullptr && *reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout)
                 return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            const uint64_t now = global_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitNs) {
                 report_status(status, kStatusTimeout);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, status);
 }
 
 // Named barrier among `count` threads (a multiple of 32) of the CTA.
