@@ -56,7 +56,7 @@ cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const 
 
 // ---- block-major fine stage over per-query lists [bh][n][k] ----------
 constexpr int32_t kFineBmItemPairs = 512;   // pairs per fine work item (<= 4 tiles)
-constexpr int32_t kMergeQueries = 64;       // queries per merge work item
+constexpr int32_t kMergeQueries = 32;       // queries per merge work item
 constexpr int32_t kPartialRing = 4;         // query ranges whose partials coexist
 
 // Bins are (head, query range of `range` queries, key block).

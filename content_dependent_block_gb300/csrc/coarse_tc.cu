@@ -51,7 +51,7 @@ constexpr int kGroups = 2;         // epilogue warpgroups (column split)
 constexpr int kEpi = kGroups * kTileM;
 constexpr int kThreads = 64 + kEpi;
 constexpr int kTmemCols = 2 * kChunk;
-constexpr int kQueue = 16;         // filtered keys per thread per slice
+constexpr int kQueue = 16;         // scores filtered per drain (divides 32)
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>
@@ -63,7 +63,8 @@ struct CoarseSmem {
     static constexpr int kTiles = kQBytes + kStages * kStageBytes;
     static constexpr int oQueue = kTiles;                     // uint32 [kQueue][kEpi]; after the
                                                               // scan, [KMAX <= 32][kTileM] lists
-    static constexpr int oBar = oQueue + kQueue * kEpi * 4;
+    static constexpr int kQueueWords = kQueue * kEpi > 32 * kTileM ? kQueue * kEpi : 32 * kTileM;
+    static constexpr int oBar = oQueue + kQueueWords * 4;
     static constexpr int kTotal = oBar + 256 /*barriers*/ + 1024 /*align*/;
 };
 
@@ -222,13 +223,13 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
                     const uint32_t col0 = uint32_t(c * kChunk + j * 32);
                     const int lim = valid - j * 32;
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
+                    for (int hf = 0; hf < 32 / kQueue; ++hf) {
                         // branch-free filter against the current k-th key
                         const uint32_t thr = L[KMAX - 1];
                         int cnt = 0;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int x = hf * 16 + e;
+                        for (int e = 0; e < kQueue; ++e) {
+                            const int x = hf * kQueue + e;
                             const uint32_t key = score_key(__uint_as_float(v[x]), col0 + x, key_mask);
                             qu[cnt * kEpi] = key;
                             cnt += (x < lim && key > thr) ? 1 : 0;
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
             tc::mbar_arrive(acc_empty + buf);
         }
         // group 1 hands its list to group 0, which merges and writes
-        static_assert(KMAX * kTileM <= kQueue * kEpi, "merge lists fit the queue region");
+        static_assert(KMAX * kTileM <= S::kQueueWords, "merge lists fit the queue region");
         tc::named_bar_sync(1, kEpi);               // every queue drained
         if (eg == 1) {
 #pragma unroll
