@@ -389,6 +389,8 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
     a.sliding = mask.sliding;
     a.scale_log2 = sl2;
     a.status = status;
+    if (bsa::fine_static_tc_supported(a, shape.dtype))
+        return launched(bsa::launch_fine_static_tc(a, st), "fine attention (tensor-core tiles) launch");
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }
 
@@ -462,6 +464,8 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     a.mask_kind = BSA_MASK_NONE;
     a.scale_log2 = sl2;
     a.status = status;
+    if (bsa::fine_static_tc_supported(a, shape.dtype))
+        return launched(bsa::launch_fine_static_tc(a, st), "fine attention (tensor-core tiles) launch");
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }
 

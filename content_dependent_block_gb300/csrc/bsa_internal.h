@@ -112,5 +112,10 @@ cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st);
 
 cudaError_t launch_fine_query_major(const FineArgs &a, int32_t dtype,
                                     cudaStream_t st);
+// Static or dense lists of bf16 inputs on the tensor cores: d in {64, 128},
+// 64-key blocks, one list row per 128-query tile (or no list), at most 512
+// listed blocks per row.
+bool fine_static_tc_supported(const FineArgs &a, int32_t dtype);
+cudaError_t launch_fine_static_tc(const FineArgs &a, cudaStream_t st);
 
 }  // namespace bsa

@@ -1,0 +1,405 @@
+// Stage 2 over static block lists on the tensor cores: every query of a
+// 128-query tile attends the tokens of the tile's listed 64-key blocks,
+// restricted by a token-level predicate (page "yayme/CUDA-kernel" README:
+// local window |i - j| <= w or global stride j % s == 0 over a precomputed
+// active-tile list; page "Block-Sparse & Linear Attention Kernels",
+// section 2: sliding window over the nearest W tokens), with softmax scaled
+// by 1/sqrt(d) (same page, sliding-window formula).  A NULL list means every
+// block.
+//
+// Query-tile-major: one CTA per (head, 128-query tile).  The list is shared
+// by the tile, so K_b and V_b are loaded once per tile and every block is a
+// dense 128 x 64 x d contraction.  The softmax is exact and two-pass: pass 0
+// computes the row maxima over all listed blocks, pass 1 recomputes the
+// scores, forms p = exp2(s * scale * log2 e - m) once, accumulates l and
+// O += P V in tensor memory.  O is never rescaled, at the price of computing
+// Q K^T twice.
+//
+//   warp 0     producer: TMA of the Q tile once, then K (pass 0) or K and V
+//              (pass 1) of each listed block into a ring of stages
+//   warp 1     MMA, warp-uniform loop, one elected lane issues:
+//              S = Q K_b^T (M 128, N 64) into one of two TMEM buffers;
+//              in pass 1 also O += P V_b (N = d, V MN-major)
+//   warps 2-5  softmax and epilogue, one thread per query row: masked row
+//              max (pass 0); masked p, l, P (bf16) into shared memory
+//              (pass 1); then O / l to the output row
+#include <cmath>
+
+#include <cudaTypedefs.h>
+
+#include "bsa_device.cuh"
+#include "bsa_internal.h"
+#include "tc.cuh"
+
+namespace bsa {
+namespace {
+
+constexpr int kTile = 128;             // queries per CTA (TMEM lanes)
+constexpr int kB = 64;                 // keys per block
+constexpr int kThreads = 192;
+constexpr int kMaxList = 512;          // listed blocks held in shared memory per chunk
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D>
+struct SCfg {
+    static constexpr int kSub = D / 64;
+    static constexpr int kStages = 3;
+    static constexpr int kQBytes = kSub * kTile * 128;
+    static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
+    static constexpr int kPBytes = kTile * 128;
+    static constexpr int oQ = 0;
+    static constexpr int oK = oQ + kQBytes;
+    static constexpr int oV = oK + kStages * kKBytes;
+    static constexpr int oP = oV + kStages * kKBytes;
+    static constexpr int oList = oP + 2 * kPBytes;          // int32 [kMaxList]
+    static constexpr int oBar = oList + kMaxList * 4;
+    enum {
+        bQFull = 0,
+        bKvFull = 1,
+        bKvEmpty = bKvFull + kStages,
+        bSFull = bKvEmpty + kStages,
+        bSFree = bSFull + 2,
+        bPFull = bSFree + 2,
+        bPFree = bPFull + 2,
+        bOFull = bPFree + 2,
+        bCount = bOFull + 1
+    };
+    static constexpr int oMisc = oBar + bCount * 8;
+    static constexpr int kTotal = oMisc + 64 + 1024;
+    static constexpr uint32_t kTmemCols = 256;              // S[2] at 0, 64; O at 128
+    static constexpr uint32_t cO = 128;
+};
+static_assert(SCfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Every (row, key) pair of the tile and block admitted by the predicate?
+__device__ __forceinline__ bool block_full(const FineArgs &a, int64_t i0, int64_t j0) {
+    const int64_t i1 = i64min(a.n, i0 + kTile) - 1, j1 = i64min(a.n, j0 + kB) - 1;
+    if (j0 + kB > a.n) return false;                     // ragged last block: mask the tail
+    if (a.mask_kind == 0) return true;
+    if (a.mask_kind == 2) return j1 <= i0 && j0 > i1 - a.sliding;
+    // local + global: every pair within the window
+    return a.window >= 0 && i1 - j0 <= a.window && j1 - i0 <= a.window;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const FineArgs a) {
+    using C = SCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = tc::align_smem_1024(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::oBar);
+    int32_t *list_s = reinterpret_cast<int32_t *>(sm + C::oList);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::oMisc);
+    int32_t *nlist_s = reinterpret_cast<int32_t *>(sm + C::oMisc + 16);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t *status = a.status;
+    if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
+    const int64_t h = blockIdx.y;
+    const int64_t i0 = int64_t(blockIdx.x) * kTile;
+
+    // the tile's list, compacted to valid ids (padding and bad ids dropped)
+    if (warp == 0) {
+        int cnt = 0;
+        if (a.list == nullptr) {
+            for (int64_t b = lane; b < a.nb && b < kMaxList; b += 32) list_s[b] = int32_t(b);
+            cnt = int(i64min(a.nb, kMaxList));
+        } else {
+            const int64_t row = i0 / a.q_group;
+            const int32_t *lr = a.list + ((a.per_head ? h * a.list_rows : 0) + row) * a.max_blocks;
+            bool bad = false;
+            for (int base = 0; base < a.max_blocks; base += 32) {
+                const int e = base + lane;
+                const int32_t b = e < a.max_blocks ? __ldg(lr + e) : -1;
+                const bool ok = b >= 0 && b < a.nb;
+                bad |= e < a.max_blocks && !ok && b != -1;
+                const unsigned m = __ballot_sync(kFull, ok);
+                if (ok) {
+                    const int pos = cnt + __popc(m & ((1u << lane) - 1u));
+                    if (pos < kMaxList) list_s[pos] = b;
+                }
+                cnt += __popc(m);
+            }
+            if (__any_sync(kFull, bad) && lane == 0) report_status(status, kStatusBadIndex);
+            cnt = min(cnt, kMaxList);
+        }
+        if (lane == 0) *nlist_s = cnt;
+    }
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bars + C::bQFull, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            tc::mbar_init(bars + C::bKvFull + s, 1);
+            tc::mbar_init(bars + C::bKvEmpty + s, 1);
+        }
+        for (int j = 0; j < 2; ++j) {
+            tc::mbar_init(bars + C::bSFull + j, 1);
+            tc::mbar_init(bars + C::bSFree + j, kTile);
+            tc::mbar_init(bars + C::bPFull + j, kTile);
+            tc::mbar_init(bars + C::bPFree + j, 1);
+        }
+        tc::mbar_init(bars + C::bOFull, 1);
+        tc::fence_barrier_init();
+        tc::prefetch_tensormap(&tm_q);
+        tc::prefetch_tensormap(&tm_k);
+        tc::prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, C::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int nl = *nlist_s;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            tc::mbar_arrive_expect_tx(bars + C::bQFull, C::kQBytes);
+#pragma unroll
+            for (int sub = 0; sub < C::kSub; ++sub)
+                tc::tma_load_3d(sm + C::oQ + sub * kTile * 128, &tm_q, bars + C::bQFull, sub * 64,
+                                int32_t(i0), int32_t(h));
+            for (int u = 0; u < 2 * nl; ++u) {
+                const int pass = u >= nl, j = pass ? u - nl : u, s = u % C::kStages;
+                if (u >= C::kStages &&
+                    !tc::mbar_wait(bars + C::bKvEmpty + s, ((u / C::kStages) - 1) & 1, status))
+                    break;
+                const int32_t key0 = list_s[j] * kB;
+                tc::mbar_arrive_expect_tx(bars + C::bKvFull + s, (pass ? 2 : 1) * C::kKBytes);
+#pragma unroll
+                for (int sub = 0; sub < C::kSub; ++sub) {
+                    tc::tma_load_3d(sm + C::oK + s * C::kKBytes + sub * kB * 128, &tm_k,
+                                    bars + C::bKvFull + s, sub * 64, key0, int32_t(h));
+                    if (pass)
+                        tc::tma_load_3d(sm + C::oV + s * C::kKBytes + sub * kB * 128, &tm_v,
+                                        bars + C::bKvFull + s, sub * 64, key0, int32_t(h));
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
+        constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
+        bool ok = __all_sync(kFull, tc::mbar_wait(bars + C::bQFull, 0, status));
+        const uint32_t aq = tc::smem_u32(sm + C::oQ);
+        auto issue_pv = [&](int u) {          // P.V of the pass-1 block in stage-use u
+            const int jj = u - nl, j2 = jj & 1, s = u % C::kStages;
+            ok = ok && __all_sync(kFull, tc::mbar_wait(bars + C::bPFull + j2, (jj >> 1) & 1, status));
+            if (!ok) return;
+            tc::tc_fence_after();
+            if (tc::elect_one()) {
+                const uint32_t ap = tc::smem_u32(sm + C::oP + j2 * C::kPBytes);
+                const uint32_t av = tc::smem_u32(sm + C::oV + s * C::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < kB / 16; ++kk)
+                    tc::mma_bf16(tmem + C::cO, tc::smem_desc_sw128(ap + kk * 32, 1024),
+                                 tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
+                                 (jj > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(bars + C::bPFree + j2);
+                tc::mma_commit(bars + C::bKvEmpty + s);
+                if (jj == nl - 1) tc::mma_commit(bars + C::bOFull);
+            }
+            __syncwarp();
+        };
+        for (int u = 0; ok && u < 2 * nl; ++u) {
+            const int pass = u >= nl, s = u % C::kStages, j = u & 1;
+            ok = tc::mbar_wait(bars + C::bKvFull + s, (u / C::kStages) & 1, status);
+            if (ok && u >= 2) ok = tc::mbar_wait(bars + C::bSFree + j, ((u >> 1) - 1) & 1, status);
+            ok = __all_sync(kFull, ok);
+            if (!ok) break;
+            tc::tc_fence_after();
+            if (tc::elect_one()) {
+                const uint32_t ak = tc::smem_u32(sm + C::oK + s * C::kKBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
+                    const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
+                    tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
+                                 tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+                }
+                tc::mma_commit(bars + C::bSFull + j);
+                if (!pass) tc::mma_commit(bars + C::bKvEmpty + s);   // K only: free after S
+            }
+            __syncwarp();
+            if (pass && u > nl) issue_pv(u - 1);                    // P.V of the previous block
+        }
+        if (ok && nl > 0) issue_pv(2 * nl - 1);
+    } else {
+        // ----------------------------------------- softmax and epilogue
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int64_t i = i0 + row;
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        float m2 = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int u = 0; u < 2 * nl; ++u) {
+            const int pass = u >= nl, jb = pass ? u - nl : u, j = u & 1;
+            if (!tc::mbar_wait(bars + C::bSFull + j, (u >> 1) & 1, status)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            const int64_t j0 = int64_t(list_s[jb]) * kB;
+            const bool full = block_full(a, i0, j0);
+            if (pass == 0) {
+                float mraw = -INFINITY;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kB; c0 += 32) {
+                    uint32_t sv[32];
+                    tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const bool adm = full || (j0 + c0 + c < a.n &&
+                                                  mask_admits(a.mask_kind, a.window, a.stride, a.sliding,
+                                                              i, j0 + c0 + c));
+                        if (adm) mraw = fmaxf(mraw, __uint_as_float(sv[c]));
+                    }
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(bars + C::bSFree + j);
+                m2 = fmaxf(m2, mraw * a.scale_log2);                 // scale > 0 keeps the order
+            } else {
+                const float mm = m2 == -INFINITY ? 0.f : m2;          // a row with no admitted key
+                uint8_t *sP = sm + C::oP + (jb & 1) * C::kPBytes + row * 128;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kB; c0 += 32) {
+                    uint32_t sv[32];
+                    tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                    tc::tmem_ld_wait();
+                    if (c0 + 32 == kB) {
+                        tc::tc_fence_before();
+                        tc::mbar_arrive(bars + C::bSFree + j);
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        float p[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int64_t jj = j0 + c0 + c + e;
+                            const bool adm = full || (jj < a.n && mask_admits(a.mask_kind, a.window,
+                                                                              a.stride, a.sliding, i, jj));
+                            p[e] = adm ? ex2(fmaf(__uint_as_float(sv[c + e]), a.scale_log2, -mm)) : 0.f;
+                        }
+                        l += p[0] + p[1];
+                        pk[c >> 1] = pack_bf16x2(p[0], p[1]);
+                    }
+                    if (c0 == 0 && jb >= 2 &&
+                        !tc::mbar_wait(bars + C::bPFree + (jb & 1), ((jb >> 1) - 1) & 1, status)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = (c0 >> 3) + c;
+                        *reinterpret_cast<uint4 *>(sP + ((chunk ^ (row & 7)) << 4)) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                    }
+                }
+                if (!ok) break;
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(bars + C::bPFull + (jb & 1));
+            }
+        }
+        // epilogue: O / l
+        if (ok && nl > 0 && tc::mbar_wait(bars + C::bOFull, 0, status)) {
+            tc::tc_fence_after();
+            const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            uint16_t *dst = static_cast<uint16_t *>(a.out) + (h * a.n + i) * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t ov[32];
+                tc::tmem_ld32(tmem + C::cO + uint32_t(c0) + lane_off, ov);
+                tc::tmem_ld_wait();
+                if (i < a.n) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        reinterpret_cast<uint4 *>(dst + c0)[v] = make_uint4(
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 0]) * inv_l, __uint_as_float(ov[8 * v + 1]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 2]) * inv_l, __uint_as_float(ov[8 * v + 3]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 4]) * inv_l, __uint_as_float(ov[8 * v + 5]) * inv_l),
+                            pack_bf16x2(__uint_as_float(ov[8 * v + 6]) * inv_l, __uint_as_float(ov[8 * v + 7]) * inv_l));
+                }
+            }
+        } else if (nl == 0 && i < a.n) {
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (h * a.n + i) * D);
+#pragma unroll
+            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);   // nothing listed
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// [bh][n][d] bf16 viewed as a 3-D tensor, box 64 x rows x 1, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int64_t bh, int64_t n, int d, int rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(n), cuuint64_t(bh)};
+    cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(n) * d * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const FineArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, cudaStream_t st) {
+    using C = SCfg<D>;
+    auto kern = fine_static_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(unsigned((a.n + kTile - 1) / kTile), unsigned(a.bh));
+    kern<<<grid, kThreads, C::kTotal, st>>>(mq, mk, mv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool fine_static_tc_supported(const FineArgs &a, int32_t dtype) {
+    return dtype == 0 /*bf16*/ && (a.d == 64 || a.d == 128) && a.kb == kB &&
+           (a.list == nullptr || a.q_group == kTile) && a.bh <= 65535 &&
+           (a.list == nullptr ? a.nb <= kMaxList : a.max_blocks <= kMaxList);
+}
+
+cudaError_t launch_fine_static_tc(const FineArgs &a, cudaStream_t st) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, a.q, a.bh, a.n, a.d, kTile) || !make_map(&mk, a.k, a.bh, a.n, a.d, kB) ||
+        !make_map(&mv, a.v, a.bh, a.n, a.d, kB))
+        return cudaErrorInvalidValue;
+    if (a.d == 64) return launch_d<64>(a, mq, mk, mv, st);
+    return launch_d<128>(a, mq, mk, mv, st);
+}
+
+}  // namespace bsa

@@ -211,3 +211,46 @@ def test_dense_list_null_is_full_attention():
     rows = oracle.all_rows(1, 200)
     dense, _, _ = oracle.masked(t.q, t.k, t.v, 0, rows)
     parity.assert_close(parity.from_device(out).reshape(-1, 64), dense, "fp32", "null list")
+
+
+# ------------------------------------- static lists on the tensor cores
+# bf16, 64-key blocks, one list row per 128-query tile: the query-tile-major
+# tcgen05 kernel (exact two-pass softmax), against the plain masked definition.
+@pytest.mark.parametrize("n,d,per_head", [(4096, 64, False), (4100, 64, True), (1000, 128, False)])
+def test_static_tc_local_global_bf16(n, d, per_head):
+    import torch
+    t, (q, k, v) = _small(2, n, d, seed=n + 7)
+    m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, 32, 512)
+    lst, _, _ = bsa.static_blocks(n, 128, 64, m)
+    dl = torch.from_numpy(np.ascontiguousarray(np.stack([lst, lst]) if per_head else lst)).cuda()
+    out = bsa.fine_attention(q, k, v, dl, key_block=64, q_group=128, per_head=per_head, mask=m)
+    rows = oracle.all_rows(2, n)
+    ref, _, psum = oracle.masked(t.q, t.k, t.v, oracle.MASK_LOCAL_GLOBAL, rows, w=32, s=512)
+    np.testing.assert_allclose(psum, 1.0, atol=1e-12)
+    parity.assert_close(parity.from_device(out).reshape(-1, d), ref, "bf16",
+                        f"tensor-core local+global n={n} d={d}")
+    assert bsa.device_status() == 0
+
+
+@pytest.mark.parametrize("n,d,win", [(1000, 128, 300), (4100, 64, 4096), (777, 64, 1)])
+def test_static_tc_sliding_bf16(n, d, win):
+    import torch
+    t, (q, k, v) = _small(1, n, d, seed=win)
+    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=win)
+    lst, _, _ = bsa.static_blocks(n, 128, 64, m)
+    out = bsa.fine_attention(q, k, v, torch.from_numpy(lst).cuda(), key_block=64, q_group=128,
+                             per_head=False, mask=m)
+    rows = oracle.all_rows(1, n)
+    ref, _, _ = oracle.masked(t.q, t.k, t.v, oracle.MASK_SLIDING, rows, W=win)
+    parity.assert_close(parity.from_device(out).reshape(-1, d), ref, "bf16",
+                        f"tensor-core sliding n={n} W={win}")
+    assert bsa.device_status() == 0
+
+
+def test_static_tc_null_list_is_dense_bf16():
+    t, (q, k, v) = _small(2, 700, 64, seed=11)
+    out = bsa.fine_attention(q, k, v, None, key_block=64)
+    rows = oracle.all_rows(2, 700)
+    dense, _, _ = oracle.masked(t.q, t.k, t.v, 0, rows)
+    parity.assert_close(parity.from_device(out).reshape(-1, 64), dense, "bf16", "dense bf16")
+    assert bsa.device_status() == 0
