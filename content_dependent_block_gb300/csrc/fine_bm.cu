@@ -19,10 +19,11 @@
 //                           in flight (or before any wait that may block)
 //   MMA       (warp 0)      S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
 //                           one of two TMEM score buffers, then O[j] = P . V_b
-//                           (N = d, V MN-major) into one of two TMEM outputs;
+//                           (A = P read from TMEM, N = d, V MN-major) into one
+//                           of two TMEM outputs;
 //                           an event loop that issues whichever is ready
 //   softmax   (warps 4-7)   one thread per row: m = max s, p = exp2(s - m),
-//                           l = sum p; P (bf16) to shared memory, (m, l) aside
+//                           l = sum p; P (bf16 pairs) to TMEM, (m, l) aside
 //   epilogue  (warps 8-11)  reads O, stores the pair's partial state
 //                           o = O / l (bf16) and lse = m + log2 l into a ring
 //                           of query ranges, counts the range's finished pairs
@@ -97,11 +98,9 @@ struct Cfg {
     static constexpr int kNKV = D == 64 ? 3 : 2;           // K/V buffers (items in flight)
     static constexpr int kMS = D == 64 ? 2 : 1;            // merge stages per merge warp
     static constexpr int kQBytes = kSub * kTile * 128;
-    static constexpr int kPBytes = kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int oQ = 0;
-    static constexpr int oP = oQ + kNQ * kQBytes;
-    static constexpr int oK = oP + 2 * kPBytes;
+    static constexpr int oK = oQ + kNQ * kQBytes;
     static constexpr int oV = oK + kNKV * kKBytes;
     static constexpr int oMs = oV + kNKV * kKBytes;        // merge stages
     static constexpr int oEpi = oMs + kMergeWarps * kMS * kStageBytes;  // 4 warps x 32 rows x 64 B
@@ -131,8 +130,9 @@ struct Cfg {
     };
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
-    static constexpr uint32_t kTmemCols = D == 64 ? 256 : 512;
+    static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t cO = 2 * kB;                 // O[j] at cO + j*D; S[j] at j*64
+    static constexpr uint32_t cP = 2 * kB + 2 * D;         // P[j] (bf16 pairs) at cP + j*32
 };
 static_assert(Cfg<64>::kTotal <= 227 * 1024, "shared memory (d = 64)");
 static_assert(Cfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
@@ -519,11 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     tc::tc_fence_after();
                     const int ib = t_ib[g2 & 3];
                     if (tc::elect_one()) {
-                        const uint32_t ap = tc::smem_u32(sm + C::oP + j * C::kPBytes);
                         const uint32_t av = tc::smem_u32(sm + C::oV + ib * C::kKBytes);
 #pragma unroll
                         for (int kk = 0; kk < kB / 16; ++kk)
-                            tc::mma_bf16(tmem + C::cO + uint32_t(j * D), tc::smem_desc_sw128(ap + kk * 32, 1024),
+                            tc::mma_bf16_ts(tmem + C::cO + uint32_t(j * D), tmem + C::cP + uint32_t(j * 32 + kk * 8),
                                          tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
                                          kk > 0);
                         tc::mma_commit(bars + C::bOFull + j);
@@ -622,7 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const float m2 = mraw * a.scale_log2;     // scale > 0 keeps the argmax
             float l = 0.f;
             bool ok = true;
-            uint8_t *sP = sm + C::oP + j * C::kPBytes + row * 128;
 #pragma unroll 1
             for (int c0 = 0; c0 < 64; c0 += 32) {
                 uint32_t sv[32];
@@ -644,19 +642,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     ok = false;
                     break;
                 }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = (c0 >> 3) + c;          // 16-byte chunk of the 128-byte row
-                    *reinterpret_cast<uint4 *>(sP + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                }
+                tc::tmem_st16(tmem + C::cP + uint32_t(j * 32 + (c0 >> 1)) + lane_off, pk);
             }
             if (!ok) break;
             // (m, l) live with the tile slot, which the gather group reuses
             // only after this tile's epilogue is done
             ml[slot * kTile + row] = make_float2(m2, l);
             tc::mbar_arrive(bars + C::bMlFull + slot);
-            tc::fence_proxy_async_smem();
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
             tc::mbar_arrive(bars + C::bPFull + j);
         }
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
