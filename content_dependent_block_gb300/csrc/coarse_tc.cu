@@ -18,10 +18,10 @@
 //               every chunk, so each thread scans half of its query's scores
 //               and keeps a running top-k in registers; the two lists are
 //               merged at the end
-// Selection: each 16-score slice is first filtered without branches against
-// the thread's current k-th key into a small shared-memory queue, and only
-// the survivors go through the sorted insertion, so a warp runs insertions
-// for the lanes that need them instead of for every score.
+// Selection: every 16 scores of a thread are sorted by a bitonic network and
+// merged into its running top-k (element-wise max against the reversed batch,
+// then a bitonic merge): the same compare-exchanges on every lane, no
+// data-dependent branches.
 // Precision: Kbar enters as a bf16 pair (hi = bf16(Kbar), lo = bf16(Kbar -
 // hi)); S = Q.hi + Q.lo accumulates in fp32, i.e. about 2^-16 relative to
 // the fp32 mean -- far inside the 1e-3 relative tie band of the selection.
@@ -74,14 +74,46 @@ __device__ __forceinline__ uint32_t score_key(float s, uint32_t col, uint32_t ma
     return (u & ~mask) | (mask - col);
 }
 
-template <int KMAX>
-__device__ __forceinline__ void key_insert(uint32_t (&L)[KMAX], uint32_t key) {
+// Compare-exchange: afterwards a >= b.
+__device__ __forceinline__ void cx(uint32_t &a, uint32_t &b) {
+    const uint32_t hi = max(a, b), lo = min(a, b);
+    a = hi;
+    b = lo;
+}
+
+// Sort 16 keys in descending order (bitonic network, 80 compare-exchanges).
+__device__ __forceinline__ void sort16_desc(uint32_t (&B)[16]) {
 #pragma unroll
-    for (int t = 0; t < KMAX; ++t) {
-        const uint32_t o = L[t];
-        L[t] = max(o, key);
-        key = min(o, key);
-    }
+    for (int k = 2; k <= 16; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int l = i ^ j;
+                if (l > i) {
+                    if ((i & k) == 0) cx(B[i], B[l]);
+                    else cx(B[l], B[i]);
+                }
+            }
+}
+
+// L (KMAX keys, descending) becomes the top KMAX of L and B (N keys,
+// descending).  Against B reversed, the element-wise max of L's last
+// min(KMAX, N) slots is a bitonic sequence holding the top KMAX of the union;
+// a bitonic merge sorts it descending.  No branches: every lane runs the same
+// compare-exchanges.
+template <int KMAX, int N>
+__device__ __forceinline__ void merge_sorted(uint32_t (&L)[KMAX], const uint32_t (&B)[N]) {
+    constexpr int NB = KMAX < N ? KMAX : N;
+#pragma unroll
+    for (int t = 0; t < NB; ++t) L[KMAX - NB + t] = max(L[KMAX - NB + t], B[NB - 1 - t]);
+#pragma unroll
+    for (int j = KMAX >> 1; j > 0; j >>= 1)
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+            const int l = i ^ j;
+            if (l > i) cx(L[i], L[l]);
+        }
 }
 
 template <int D, int KMAX>
@@ -204,7 +236,6 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
         const int eg = (warp - 2) >> 2;            // column group
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row inside the tile
-        uint32_t *qu = queue + eg * kTileM + r;    // [kQueue][kEpi], this thread's column
         uint32_t L[KMAX];
 #pragma unroll
         for (int t = 0; t < KMAX; ++t) L[t] = 0u;  // 0 = empty (below every real key)
@@ -222,22 +253,18 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
                     tc::tmem_ld_wait();
                     const uint32_t col0 = uint32_t(c * kChunk + j * 32);
                     const int lim = valid - j * 32;
+#pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        // 16 keys: sort them, merge them into the running top-k
+                        uint32_t B[16];
 #pragma unroll
-                    for (int hf = 0; hf < 32 / kQueue; ++hf) {
-                        // branch-free filter against the current k-th key
-                        const uint32_t thr = L[KMAX - 1];
-                        int cnt = 0;
-#pragma unroll
-                        for (int e = 0; e < kQueue; ++e) {
-                            const int x = hf * kQueue + e;
-                            const uint32_t key = score_key(__uint_as_float(v[x]), col0 + x, key_mask);
-                            qu[cnt * kEpi] = key;
-                            cnt += (x < lim && key > thr) ? 1 : 0;
+                        for (int e = 0; e < 16; ++e) {
+                            const int x = hf * 16 + e;
+                            const uint32_t vx = hf ? v[16 + e] : v[e];
+                            B[e] = x < lim ? score_key(__uint_as_float(vx), col0 + x, key_mask) : 0u;
                         }
-                        for (int t = 0; t < cnt; ++t) {
-                            const uint32_t key = qu[t * kEpi];
-                            if (key > L[KMAX - 1]) key_insert<KMAX>(L, key);
-                        }
+                        sort16_desc(B);
+                        merge_sorted<KMAX, 16>(L, B);
                     }
                 }
             }
@@ -254,11 +281,10 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
         tc::named_bar_sync(1, kEpi);
         const int64_t i = row0 + r;
         if (eg == 0 && i < n) {
+            uint32_t B[KMAX];
 #pragma unroll
-            for (int t = 0; t < KMAX; ++t) {
-                const uint32_t key = merge[t * kTileM + r];
-                if (key > L[KMAX - 1]) key_insert<KMAX>(L, key);
-            }
+            for (int t = 0; t < KMAX; ++t) B[t] = merge[t * kTileM + r];
+            merge_sorted<KMAX, KMAX>(L, B);
             int ids[KMAX];
             const int kk = int(i64min(topk, nb));
 #pragma unroll
