@@ -263,6 +263,31 @@ def reference_arm(args, rank, world, w):
     return 0
 
 
+def profile_static(args, w, device, dist):
+    """--profile-forwards N on a sliding-window workload: N untimed calls of
+    the static-list fine stage on the tensors of the dynamic workload of the
+    same shape (one launch each)."""
+    import torch
+    from content_dependent_block_gb300 import bsa
+    base = next(x for x in workloads.WORKLOADS.values()
+                if x.kind == "dynamic" and (x.bh, x.n, x.d) == (w.bh, w.n, w.d))
+    t = workloads.generate(base)
+    q, k, v = (torch.from_numpy(getattr(t, x).view("int16")).view(torch.bfloat16).to(device)
+               for x in "qkv")
+    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=w.sliding)
+    lst, _, _ = bsa.static_blocks(w.n, w.q_group, w.key_block, m)
+    dl = torch.from_numpy(lst).to(device)
+    out = torch.empty_like(q)
+    for _ in range(args.profile_forwards):
+        bsa.fine_attention(q, k, v, dl, key_block=w.key_block, q_group=w.q_group,
+                           per_head=False, mask=m, out=out)
+    torch.cuda.synchronize(device)
+    status = bsa.device_status()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0 if status == 0 else 1
+
+
 def config_of(w):
     return {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "key_block": w.key_block,
             "topk": w.topk, "dtype": w.dtype, "inputs": w.note,
@@ -291,6 +316,8 @@ def main(argv=None):
     barrier(dist, device)
     bsa.lib()
 
+    if args.profile_forwards > 0 and w.kind == "sliding":
+        return profile_static(args, w, device, dist)
     t = workloads.generate(w, seed=w.seed + rank)
     torch.cuda.reset_peak_memory_stats(device)
     mem0 = torch.cuda.memory_allocated(device)
