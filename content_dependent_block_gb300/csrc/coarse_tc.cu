@@ -142,7 +142,10 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
     const int64_t row0 = int64_t(blockIdx.x) * kTileM;
     const int nchunks = int((nb + kChunk - 1) / kChunk);
     // A wait elsewhere already ran out: do no work (results are invalid anyway).
-    if (status != nullptr && *reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
+    // The whole CTA takes the same decision.
+    if (__syncthreads_or(status != nullptr &&
+                         *reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout))
+        return;
 
     if (threadIdx.x == 0) {
         tc::mbar_init(q_full, 1);

@@ -269,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = a.status;
-    if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
+    // A wait elsewhere already ran out: the whole CTA leaves together.
+    if (__syncthreads_or(*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout)) return;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNQ; ++i) {

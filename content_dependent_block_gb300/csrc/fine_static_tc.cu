@@ -13,16 +13,21 @@
 // computes the row maxima over all listed blocks, pass 1 recomputes the
 // scores, forms p = exp2(s * scale * log2 e - m) once, accumulates l and
 // O += P V in tensor memory.  O is never rescaled, at the price of computing
-// Q K^T twice.
+// Q K^T twice.  Stage-use u runs over u < nl (pass 0, block u) and
+// nl <= u < 2 nl (pass 1, block u - nl).
 //
-//   warp 0     producer: TMA of the Q tile once, then K (pass 0) or K and V
-//              (pass 1) of each listed block into a ring of stages
+//   warp 0     producer: TMA of the Q tile once, then K of every stage-use
+//              into a ring of three, V of every pass-1 block into a ring of
+//              four (one per P buffer)
 //   warp 1     MMA, warp-uniform loop, one elected lane issues:
-//              S = Q K_b^T (M 128, N 64) into one of two TMEM buffers;
-//              in pass 1 also O += P V_b (N = d, V MN-major)
-//   warps 2-5  softmax and epilogue, one thread per query row: masked row
-//              max (pass 0); masked p, l, P (bf16) into shared memory
-//              (pass 1); then O / l to the output row
+//              S_u = Q K^T (M 128, N 64) into TMEM buffer u mod 4; the P.V
+//              of a pass-1 block (N = d, V MN-major) two uses later, so the
+//              next scores are ready while a warpgroup still works
+//   warps 2-5  softmax warpgroup 0: the even stage-uses
+//   warps 6-9  softmax warpgroup 1: the odd stage-uses; one thread per
+//              query row: masked row max (pass 0), combined over the two
+//              groups through shared memory; masked p, l, P (bf16) into the
+//              block's P buffer (pass 1); then O / l, half the columns each
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -36,40 +41,47 @@ namespace {
 
 constexpr int kTile = 128;             // queries per CTA (TMEM lanes)
 constexpr int kB = 64;                 // keys per block
-constexpr int kThreads = 192;
+constexpr int kGroups = 2;             // softmax warpgroups
+constexpr int kThreads = 64 + kGroups * 128;
 constexpr int kMaxList = 512;          // listed blocks held in shared memory per chunk
+constexpr uint32_t kBarGroups = 1;     // named barrier of the softmax warpgroups
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>
 struct SCfg {
     static constexpr int kSub = D / 64;
-    static constexpr int kStages = 3;
+    static constexpr int kKStages = 3;                      // K ring
+    static constexpr int kRing = 4;                         // V ring = P buffers = S buffers
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int kPBytes = kTile * 128;
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQBytes;
-    static constexpr int oV = oK + kStages * kKBytes;
-    static constexpr int oP = oV + kStages * kKBytes;
-    static constexpr int oList = oP + 2 * kPBytes;          // int32 [kMaxList]
-    static constexpr int oBar = oList + kMaxList * 4;
+    static constexpr int oV = oK + kKStages * kKBytes;
+    static constexpr int oP = oV + kRing * kKBytes;
+    static constexpr int oList = oP + kRing * kPBytes;      // int32 [kMaxList]
+    static constexpr int oRed = oList + kMaxList * 4;       // float [2][kGroups][kTile]
+    static constexpr int oBar = oRed + 2 * kGroups * kTile * 4;
     enum {
         bQFull = 0,
-        bKvFull = 1,
-        bKvEmpty = bKvFull + kStages,
-        bSFull = bKvEmpty + kStages,
-        bSFree = bSFull + 2,
-        bPFull = bSFree + 2,
-        bPFree = bPFull + 2,
-        bOFull = bPFree + 2,
+        bKFull = 1,
+        bKEmpty = bKFull + kKStages,
+        bVFull = bKEmpty + kKStages,
+        bVEmpty = bVFull + kRing,
+        bSFull = bVEmpty + kRing,
+        bSFree = bSFull + kRing,
+        bPFull = bSFree + kRing,
+        bPFree = bPFull + kRing,
+        bOFull = bPFree + kRing,
         bCount = bOFull + 1
     };
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
-    static constexpr uint32_t kTmemCols = 256;              // S[2] at 0, 64; O at 128
-    static constexpr uint32_t cO = 128;
+    static constexpr uint32_t kTmemCols = 512;              // S[4] at 0..255; O at 256
+    static constexpr uint32_t cO = kRing * kB;
 };
 static_assert(SCfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
+static_assert(SCfg<128>::cO + 128 <= SCfg<128>::kTmemCols, "tensor memory (d = 128)");
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -96,12 +108,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
     uint8_t *sm = tc::align_smem_1024(smem_raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::oBar);
     int32_t *list_s = reinterpret_cast<int32_t *>(sm + C::oList);
+    float *m_part = reinterpret_cast<float *>(sm + C::oRed);           // [kGroups][kTile]
+    float *l_part = m_part + kGroups * kTile;                           // [kGroups][kTile]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::oMisc);
     int32_t *nlist_s = reinterpret_cast<int32_t *>(sm + C::oMisc + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = a.status;
-    if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return;
+    // A wait elsewhere already ran out: the whole CTA leaves together.
+    if (__syncthreads_or(*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout)) return;
     const int64_t h = blockIdx.y;
     const int64_t i0 = int64_t(blockIdx.x) * kTile;
 
@@ -134,13 +149,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
     }
     if (threadIdx.x == 0) {
         tc::mbar_init(bars + C::bQFull, 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            tc::mbar_init(bars + C::bKvFull + s, 1);
-            tc::mbar_init(bars + C::bKvEmpty + s, 1);
+        for (int s = 0; s < C::kKStages; ++s) {
+            tc::mbar_init(bars + C::bKFull + s, 1);
+            tc::mbar_init(bars + C::bKEmpty + s, 1);
         }
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < C::kRing; ++j) {
+            tc::mbar_init(bars + C::bVFull + j, 1);
+            tc::mbar_init(bars + C::bVEmpty + j, 1);
             tc::mbar_init(bars + C::bSFull + j, 1);
-            tc::mbar_init(bars + C::bSFree + j, kTile);
+            tc::mbar_init(bars + C::bSFree + j, kTile);     // one warpgroup per stage-use
             tc::mbar_init(bars + C::bPFull + j, kTile);
             tc::mbar_init(bars + C::bPFree + j, 1);
         }
@@ -169,19 +186,26 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 tc::tma_load_3d(sm + C::oQ + sub * kTile * 128, &tm_q, bars + C::bQFull, sub * 64,
                                 int32_t(i0), int32_t(h));
             for (int u = 0; u < 2 * nl; ++u) {
-                const int pass = u >= nl, j = pass ? u - nl : u, s = u % C::kStages;
-                if (u >= C::kStages &&
-                    !tc::mbar_wait(bars + C::bKvEmpty + s, ((u / C::kStages) - 1) & 1, status))
+                const int pass = u >= nl, jb = pass ? u - nl : u, s = u % C::kKStages;
+                if (u >= C::kKStages &&
+                    !tc::mbar_wait(bars + C::bKEmpty + s, ((u / C::kKStages) - 1) & 1, status))
                     break;
-                const int32_t key0 = list_s[j] * kB;
-                tc::mbar_arrive_expect_tx(bars + C::bKvFull + s, (pass ? 2 : 1) * C::kKBytes);
+                const int32_t key0 = list_s[jb] * kB;
+                tc::mbar_arrive_expect_tx(bars + C::bKFull + s, C::kKBytes);
 #pragma unroll
-                for (int sub = 0; sub < C::kSub; ++sub) {
+                for (int sub = 0; sub < C::kSub; ++sub)
                     tc::tma_load_3d(sm + C::oK + s * C::kKBytes + sub * kB * 128, &tm_k,
-                                    bars + C::bKvFull + s, sub * 64, key0, int32_t(h));
-                    if (pass)
-                        tc::tma_load_3d(sm + C::oV + s * C::kKBytes + sub * kB * 128, &tm_v,
-                                        bars + C::bKvFull + s, sub * 64, key0, int32_t(h));
+                                    bars + C::bKFull + s, sub * 64, key0, int32_t(h));
+                if (pass) {
+                    const int r = jb % C::kRing;
+                    if (jb >= C::kRing &&
+                        !tc::mbar_wait(bars + C::bVEmpty + r, ((jb / C::kRing) - 1) & 1, status))
+                        break;
+                    tc::mbar_arrive_expect_tx(bars + C::bVFull + r, C::kKBytes);
+#pragma unroll
+                    for (int sub = 0; sub < C::kSub; ++sub)
+                        tc::tma_load_3d(sm + C::oV + r * C::kKBytes + sub * kB * 128, &tm_v,
+                                        bars + C::bVFull + r, sub * 64, key0, int32_t(h));
                 }
             }
         }
@@ -192,135 +216,159 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
         constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
         bool ok = __all_sync(kFull, tc::mbar_wait(bars + C::bQFull, 0, status));
         const uint32_t aq = tc::smem_u32(sm + C::oQ);
-        auto issue_pv = [&](int u) {          // P.V of the pass-1 block in stage-use u
-            const int jj = u - nl, j2 = jj & 1, s = u % C::kStages;
-            ok = ok && __all_sync(kFull, tc::mbar_wait(bars + C::bPFull + j2, (jj >> 1) & 1, status));
+        auto issue_pv = [&](int jb) {         // O += P_jb V_jb
+            const int r = jb % C::kRing, ph = (jb / C::kRing) & 1;
+            bool w = tc::mbar_wait(bars + C::bVFull + r, ph, status);
+            w = w && tc::mbar_wait(bars + C::bPFull + r, ph, status);
+            ok = __all_sync(kFull, w);
             if (!ok) return;
             tc::tc_fence_after();
             if (tc::elect_one()) {
-                const uint32_t ap = tc::smem_u32(sm + C::oP + j2 * C::kPBytes);
-                const uint32_t av = tc::smem_u32(sm + C::oV + s * C::kKBytes);
+                const uint32_t ap = tc::smem_u32(sm + C::oP + r * C::kPBytes);
+                const uint32_t av = tc::smem_u32(sm + C::oV + r * C::kKBytes);
 #pragma unroll
                 for (int kk = 0; kk < kB / 16; ++kk)
                     tc::mma_bf16(tmem + C::cO, tc::smem_desc_sw128(ap + kk * 32, 1024),
                                  tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
-                                 (jj > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(bars + C::bPFree + j2);
-                tc::mma_commit(bars + C::bKvEmpty + s);
-                if (jj == nl - 1) tc::mma_commit(bars + C::bOFull);
+                                 (jb > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(bars + C::bPFree + r);
+                tc::mma_commit(bars + C::bVEmpty + r);
+                if (jb == nl - 1) tc::mma_commit(bars + C::bOFull);
             }
             __syncwarp();
         };
-        for (int u = 0; ok && u < 2 * nl; ++u) {
-            const int pass = u >= nl, s = u % C::kStages, j = u & 1;
-            ok = tc::mbar_wait(bars + C::bKvFull + s, (u / C::kStages) & 1, status);
-            if (ok && u >= 2) ok = tc::mbar_wait(bars + C::bSFree + j, ((u >> 1) - 1) & 1, status);
-            ok = __all_sync(kFull, ok);
-            if (!ok) break;
-            tc::tc_fence_after();
-            if (tc::elect_one()) {
-                const uint32_t ak = tc::smem_u32(sm + C::oK + s * C::kKBytes);
+        for (int u = 0; ok && u < 2 * nl + 2; ++u) {
+            if (u < 2 * nl) {
+                const int s = u % C::kKStages, j = u % C::kRing;
+                bool w = tc::mbar_wait(bars + C::bKFull + s, (u / C::kKStages) & 1, status);
+                if (w && u >= C::kRing)
+                    w = tc::mbar_wait(bars + C::bSFree + j, ((u / C::kRing) - 1) & 1, status);
+                ok = __all_sync(kFull, w);
+                if (!ok) break;
+                tc::tc_fence_after();
+                if (tc::elect_one()) {
+                    const uint32_t ak = tc::smem_u32(sm + C::oK + s * C::kKBytes);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
-                    const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
-                    tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
-                                 tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
+                        const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
+                        tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
+                                     tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+                    }
+                    tc::mma_commit(bars + C::bSFull + j);
+                    tc::mma_commit(bars + C::bKEmpty + s);             // K is read by S only
                 }
-                tc::mma_commit(bars + C::bSFull + j);
-                if (!pass) tc::mma_commit(bars + C::bKvEmpty + s);   // K only: free after S
+                __syncwarp();
             }
-            __syncwarp();
-            if (pass && u > nl) issue_pv(u - 1);                    // P.V of the previous block
+            // P.V two stage-uses behind the scores
+            if (u - 2 >= nl) issue_pv(u - 2 - nl);
         }
-        if (ok && nl > 0) issue_pv(2 * nl - 1);
     } else {
         // ----------------------------------------- softmax and epilogue
+        const int g = (warp - 2) >> 2;                 // warpgroup: stage-uses u = g mod 2
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int64_t i = i0 + row;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int u = 0; u < 2 * nl; ++u) {
-            const int pass = u >= nl, jb = pass ? u - nl : u, j = u & 1;
-            if (!tc::mbar_wait(bars + C::bSFull + j, (u >> 1) & 1, status)) {
+        // pass 0: masked row maxima of this group's blocks
+        for (int u = g; ok && u < nl; u += kGroups) {
+            const int j = u % C::kRing;
+            if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kRing) & 1, status)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            const int64_t j0 = int64_t(list_s[u]) * kB;
+            const bool full = block_full(a, i0, j0);
+            float mraw = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kB; c0 += 32) {
+                uint32_t sv[32];
+                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const bool adm = full || (j0 + c0 + c < a.n &&
+                                              mask_admits(a.mask_kind, a.window, a.stride, a.sliding,
+                                                          i, j0 + c0 + c));
+                    if (adm) mraw = fmaxf(mraw, __uint_as_float(sv[c]));
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(bars + C::bSFree + j);
+            m2 = fmaxf(m2, mraw * a.scale_log2);                     // scale > 0 keeps the order
+        }
+        // the row maximum over both groups (every group thread passes here once)
+        m_part[g * kTile + row] = m2;
+        tc::named_bar_sync(kBarGroups, kGroups * 128);
+        m2 = fmaxf(m_part[row], m_part[kTile + row]);
+        const float mm = m2 == -INFINITY ? 0.f : m2;                  // a row with no admitted key
+        // pass 1: p, l and P of this group's blocks
+        for (int u = nl + ((nl ^ g) & 1); ok && u < 2 * nl; u += kGroups) {
+            const int jb = u - nl, j = u % C::kRing, r = jb % C::kRing;
+            if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kRing) & 1, status)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
             const int64_t j0 = int64_t(list_s[jb]) * kB;
             const bool full = block_full(a, i0, j0);
-            if (pass == 0) {
-                float mraw = -INFINITY;
+            uint8_t *sP = sm + C::oP + r * C::kPBytes + row * 128;
 #pragma unroll 1
-                for (int c0 = 0; c0 < kB; c0 += 32) {
-                    uint32_t sv[32];
-                    tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
-                    tc::tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const bool adm = full || (j0 + c0 + c < a.n &&
-                                                  mask_admits(a.mask_kind, a.window, a.stride, a.sliding,
-                                                              i, j0 + c0 + c));
-                        if (adm) mraw = fmaxf(mraw, __uint_as_float(sv[c]));
-                    }
+            for (int c0 = 0; c0 < kB; c0 += 32) {
+                uint32_t sv[32];
+                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                tc::tmem_ld_wait();
+                if (c0 + 32 == kB) {
+                    tc::tc_fence_before();
+                    tc::mbar_arrive(bars + C::bSFree + j);
                 }
-                tc::tc_fence_before();
-                tc::mbar_arrive(bars + C::bSFree + j);
-                m2 = fmaxf(m2, mraw * a.scale_log2);                 // scale > 0 keeps the order
-            } else {
-                const float mm = m2 == -INFINITY ? 0.f : m2;          // a row with no admitted key
-                uint8_t *sP = sm + C::oP + (jb & 1) * C::kPBytes + row * 128;
-#pragma unroll 1
-                for (int c0 = 0; c0 < kB; c0 += 32) {
-                    uint32_t sv[32];
-                    tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
-                    tc::tmem_ld_wait();
-                    if (c0 + 32 == kB) {
-                        tc::tc_fence_before();
-                        tc::mbar_arrive(bars + C::bSFree + j);
-                    }
-                    uint32_t pk[16];
+                uint32_t pk[16];
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        float p[2];
+                for (int c = 0; c < 32; c += 2) {
+                    float p[2];
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int64_t jj = j0 + c0 + c + e;
-                            const bool adm = full || (jj < a.n && mask_admits(a.mask_kind, a.window,
-                                                                              a.stride, a.sliding, i, jj));
-                            p[e] = adm ? ex2(fmaf(__uint_as_float(sv[c + e]), a.scale_log2, -mm)) : 0.f;
-                        }
-                        l += p[0] + p[1];
-                        pk[c >> 1] = pack_bf16x2(p[0], p[1]);
+                    for (int e = 0; e < 2; ++e) {
+                        const int64_t jj = j0 + c0 + c + e;
+                        const bool adm = full || (jj < a.n && mask_admits(a.mask_kind, a.window,
+                                                                          a.stride, a.sliding, i, jj));
+                        p[e] = adm ? ex2(fmaf(__uint_as_float(sv[c + e]), a.scale_log2, -mm)) : 0.f;
                     }
-                    if (c0 == 0 && jb >= 2 &&
-                        !tc::mbar_wait(bars + C::bPFree + (jb & 1), ((jb >> 1) - 1) & 1, status)) {
-                        ok = false;
-                        break;
-                    }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int chunk = (c0 >> 3) + c;
-                        *reinterpret_cast<uint4 *>(sP + ((chunk ^ (row & 7)) << 4)) =
-                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                    }
+                    l += p[0] + p[1];
+                    pk[c >> 1] = pack_bf16x2(p[0], p[1]);
                 }
-                if (!ok) break;
-                tc::fence_proxy_async_smem();
-                tc::mbar_arrive(bars + C::bPFull + (jb & 1));
+                if (c0 == 0 && jb >= C::kRing &&
+                    !tc::mbar_wait(bars + C::bPFree + r, ((jb / C::kRing) - 1) & 1, status)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = (c0 >> 3) + c;
+                    *reinterpret_cast<uint4 *>(sP + ((chunk ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
             }
+            if (!ok) break;
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(bars + C::bPFull + r);
         }
-        // epilogue: O / l
+        // the row sum over both groups
+        l_part[g * kTile + row] = l;
+        tc::named_bar_sync(kBarGroups, kGroups * 128);
+        l = l_part[row] + l_part[kTile + row];
+        // epilogue: O / l, columns [g D / 2, (g + 1) D / 2) of the row
+        constexpr int kHalf = D / kGroups;
         if (ok && nl > 0 && tc::mbar_wait(bars + C::bOFull, 0, status)) {
             tc::tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            uint16_t *dst = static_cast<uint16_t *>(a.out) + (h * a.n + i) * D;
+            uint16_t *dst = static_cast<uint16_t *>(a.out) + (h * a.n + i) * D + g * kHalf;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < kHalf; c0 += 32) {
                 uint32_t ov[32];
-                tc::tmem_ld32(tmem + C::cO + uint32_t(c0) + lane_off, ov);
+                tc::tmem_ld32(tmem + C::cO + uint32_t(g * kHalf + c0) + lane_off, ov);
                 tc::tmem_ld_wait();
                 if (i < a.n) {
 #pragma unroll
@@ -333,9 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 }
             }
         } else if (nl == 0 && i < a.n) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (h * a.n + i) * D);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (h * a.n + i) * D +
+                                                   g * kHalf);
 #pragma unroll
-            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);   // nothing listed
+            for (int v = 0; v < kHalf / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);   // nothing listed
         }
     }
 
