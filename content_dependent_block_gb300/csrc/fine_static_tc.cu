@@ -16,18 +16,19 @@
 // Q K^T twice.  Stage-use u runs over u < nl (pass 0, block u) and
 // nl <= u < 2 nl (pass 1, block u - nl).
 //
-//   warp 0     producer: TMA of the Q tile once, then K of every stage-use
-//              into a ring of three, V of every pass-1 block into a ring of
-//              four (one per P buffer)
+//   warp 0     producer of Q (once) and of K for every stage-use, into a
+//              ring of three
 //   warp 1     MMA, warp-uniform loop, one elected lane issues:
-//              S_u = Q K^T (M 128, N 64) into TMEM buffer u mod 4; the P.V
-//              of a pass-1 block (N = d, V MN-major) two uses later, so the
-//              next scores are ready while a warpgroup still works
-//   warps 2-5  softmax warpgroup 0: the even stage-uses
-//   warps 6-9  softmax warpgroup 1: the odd stage-uses; one thread per
-//              query row: masked row max (pass 0), combined over the two
-//              groups through shared memory; masked p, l, P (bf16) into the
-//              block's P buffer (pass 1); then O / l, half the columns each
+//              S_u = Q K^T (M 128, N 64) into TMEM buffer u mod 6; the P.V
+//              of a pass-1 block (N = d, V MN-major) four stage-uses later,
+//              so the next scores are ready while the groups still work
+//   warp 2     producer of V for every pass-1 block, into a ring of four
+//              (one per P buffer), so K loads never wait on a P.V
+//   warps 3-18 four softmax warpgroups; group g takes the stage-uses
+//              u = g mod 4, one thread per query row: masked row max
+//              (pass 0), combined over the groups through shared memory;
+//              masked p, l, P (bf16) into the block's P buffer (pass 1);
+//              then O / l, 32-column chunks dealt round-robin to the groups
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -41,8 +42,10 @@ namespace {
 
 constexpr int kTile = 128;             // queries per CTA (TMEM lanes)
 constexpr int kB = 64;                 // keys per block
-constexpr int kGroups = 2;             // softmax warpgroups
-constexpr int kThreads = 64 + kGroups * 128;
+constexpr int kGroups = 4;             // softmax warpgroups
+constexpr int kLag = kGroups;          // P.V of a block this many stage-uses behind its scores
+constexpr int kWarpSoftmax = 3;       // first softmax warp
+constexpr int kThreads = 32 * kWarpSoftmax + kGroups * 128;
 constexpr int kMaxList = 512;          // listed blocks held in shared memory per chunk
 constexpr uint32_t kBarGroups = 1;     // named barrier of the softmax warpgroups
 constexpr unsigned kFull = 0xffffffffu;
@@ -51,7 +54,8 @@ template <int D>
 struct SCfg {
     static constexpr int kSub = D / 64;
     static constexpr int kKStages = 3;                      // K ring
-    static constexpr int kRing = 4;                         // V ring = P buffers = S buffers
+    static constexpr int kRing = 4;                         // V ring = P buffers
+    static constexpr int kS = 2 * kGroups < 6 ? 2 * kGroups : 6;   // S buffers in TMEM
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int kPBytes = kTile * 128;
@@ -69,19 +73,20 @@ struct SCfg {
         bVFull = bKEmpty + kKStages,
         bVEmpty = bVFull + kRing,
         bSFull = bVEmpty + kRing,
-        bSFree = bSFull + kRing,
-        bPFull = bSFree + kRing,
+        bSFree = bSFull + kS,
+        bPFull = bSFree + kS,
         bPFree = bPFull + kRing,
         bOFull = bPFree + kRing,
         bCount = bOFull + 1
     };
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
-    static constexpr uint32_t kTmemCols = 512;              // S[4] at 0..255; O at 256
-    static constexpr uint32_t cO = kRing * kB;
+    static constexpr uint32_t kTmemCols = 512;              // S[kS] from 0; O after them
+    static constexpr uint32_t cO = kS * kB;
 };
 static_assert(SCfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
 static_assert(SCfg<128>::cO + 128 <= SCfg<128>::kTmemCols, "tensor memory (d = 128)");
+static_assert(kGroups >= 1 && kGroups <= 4, "softmax warpgroups");
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -156,10 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
         for (int j = 0; j < C::kRing; ++j) {
             tc::mbar_init(bars + C::bVFull + j, 1);
             tc::mbar_init(bars + C::bVEmpty + j, 1);
-            tc::mbar_init(bars + C::bSFull + j, 1);
-            tc::mbar_init(bars + C::bSFree + j, kTile);     // one warpgroup per stage-use
-            tc::mbar_init(bars + C::bPFull + j, kTile);
+            tc::mbar_init(bars + C::bPFull + j, kTile);     // one warpgroup per stage-use
             tc::mbar_init(bars + C::bPFree + j, 1);
+        }
+        for (int j = 0; j < C::kS; ++j) {
+            tc::mbar_init(bars + C::bSFull + j, 1);
+            tc::mbar_init(bars + C::bSFree + j, kTile);
         }
         tc::mbar_init(bars + C::bOFull, 1);
         tc::fence_barrier_init();
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 tc::tma_load_3d(sm + C::oQ + sub * kTile * 128, &tm_q, bars + C::bQFull, sub * 64,
                                 int32_t(i0), int32_t(h));
             for (int u = 0; u < 2 * nl; ++u) {
-                const int pass = u >= nl, jb = pass ? u - nl : u, s = u % C::kKStages;
+                const int jb = u >= nl ? u - nl : u, s = u % C::kKStages;
                 if (u >= C::kKStages &&
                     !tc::mbar_wait(bars + C::bKEmpty + s, ((u / C::kKStages) - 1) & 1, status))
                     break;
@@ -196,17 +203,22 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 for (int sub = 0; sub < C::kSub; ++sub)
                     tc::tma_load_3d(sm + C::oK + s * C::kKBytes + sub * kB * 128, &tm_k,
                                     bars + C::bKFull + s, sub * 64, key0, int32_t(h));
-                if (pass) {
-                    const int r = jb % C::kRing;
-                    if (jb >= C::kRing &&
-                        !tc::mbar_wait(bars + C::bVEmpty + r, ((jb / C::kRing) - 1) & 1, status))
-                        break;
-                    tc::mbar_arrive_expect_tx(bars + C::bVFull + r, C::kKBytes);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ producer of V
+        if (lane == 0) {
+            for (int jb = 0; jb < nl; ++jb) {
+                const int r = jb % C::kRing;
+                if (jb >= C::kRing &&
+                    !tc::mbar_wait(bars + C::bVEmpty + r, ((jb / C::kRing) - 1) & 1, status))
+                    break;
+                tc::mbar_arrive_expect_tx(bars + C::bVFull + r, C::kKBytes);
 #pragma unroll
-                    for (int sub = 0; sub < C::kSub; ++sub)
-                        tc::tma_load_3d(sm + C::oV + r * C::kKBytes + sub * kB * 128, &tm_v,
-                                        bars + C::bVFull + r, sub * 64, key0, int32_t(h));
-                }
+                for (int sub = 0; sub < C::kSub; ++sub)
+                    tc::tma_load_3d(sm + C::oV + r * C::kKBytes + sub * kB * 128, &tm_v,
+                                    bars + C::bVFull + r, sub * 64, list_s[jb] * kB, int32_t(h));
             }
         }
         __syncwarp();
@@ -237,12 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             }
             __syncwarp();
         };
-        for (int u = 0; ok && u < 2 * nl + 2; ++u) {
+        for (int u = 0; ok && u < 2 * nl + kLag; ++u) {
             if (u < 2 * nl) {
-                const int s = u % C::kKStages, j = u % C::kRing;
+                const int s = u % C::kKStages, j = u % C::kS;
                 bool w = tc::mbar_wait(bars + C::bKFull + s, (u / C::kKStages) & 1, status);
-                if (w && u >= C::kRing)
-                    w = tc::mbar_wait(bars + C::bSFree + j, ((u / C::kRing) - 1) & 1, status);
+                if (w && u >= C::kS)
+                    w = tc::mbar_wait(bars + C::bSFree + j, ((u / C::kS) - 1) & 1, status);
                 ok = __all_sync(kFull, w);
                 if (!ok) break;
                 tc::tc_fence_after();
@@ -260,12 +272,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 }
                 __syncwarp();
             }
-            // P.V two stage-uses behind the scores
-            if (u - 2 >= nl) issue_pv(u - 2 - nl);
+            // P.V kLag stage-uses behind the scores
+            if (u - kLag >= nl) issue_pv(u - kLag - nl);
         }
     } else {
         // ----------------------------------------- softmax and epilogue
-        const int g = (warp - 2) >> 2;                 // warpgroup: stage-uses u = g mod 2
+        const int g = (warp - kWarpSoftmax) >> 2;                 // warpgroup: stage-uses u = g mod kGroups
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int64_t i = i0 + row;
@@ -274,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
         bool ok = true;
         // pass 0: masked row maxima of this group's blocks
         for (int u = g; ok && u < nl; u += kGroups) {
-            const int j = u % C::kRing;
-            if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kRing) & 1, status)) {
+            const int j = u % C::kS;
+            if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kS) & 1, status)) {
                 ok = false;
                 break;
             }
@@ -300,15 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             tc::mbar_arrive(bars + C::bSFree + j);
             m2 = fmaxf(m2, mraw * a.scale_log2);                     // scale > 0 keeps the order
         }
-        // the row maximum over both groups (every group thread passes here once)
+        // the row maximum over the groups (every group thread passes here once)
         m_part[g * kTile + row] = m2;
         tc::named_bar_sync(kBarGroups, kGroups * 128);
-        m2 = fmaxf(m_part[row], m_part[kTile + row]);
+#pragma unroll
+        for (int o = 0; o < kGroups; ++o) m2 = fmaxf(m2, m_part[o * kTile + row]);
         const float mm = m2 == -INFINITY ? 0.f : m2;                  // a row with no admitted key
         // pass 1: p, l and P of this group's blocks
-        for (int u = nl + ((nl ^ g) & 1); ok && u < 2 * nl; u += kGroups) {
-            const int jb = u - nl, j = u % C::kRing, r = jb % C::kRing;
-            if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kRing) & 1, status)) {
+        for (int u = nl + (g + kGroups - nl % kGroups) % kGroups; ok && u < 2 * nl; u += kGroups) {
+            const int jb = u - nl, j = u % C::kS, r = jb % C::kRing;
+            if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kS) & 1, status)) {
                 ok = false;
                 break;
             }
@@ -355,20 +368,21 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             tc::fence_proxy_async_smem();
             tc::mbar_arrive(bars + C::bPFull + r);
         }
-        // the row sum over both groups
+        // the row sum over the groups
         l_part[g * kTile + row] = l;
         tc::named_bar_sync(kBarGroups, kGroups * 128);
-        l = l_part[row] + l_part[kTile + row];
-        // epilogue: O / l, columns [g D / 2, (g + 1) D / 2) of the row
-        constexpr int kHalf = D / kGroups;
+        l = 0.f;
+#pragma unroll
+        for (int o = 0; o < kGroups; ++o) l += l_part[o * kTile + row];
+        // epilogue: O / l; group g writes the 32-column chunks c = g mod kGroups
         if (ok && nl > 0 && tc::mbar_wait(bars + C::bOFull, 0, status)) {
             tc::tc_fence_after();
             const float inv_l = l > 0.f ? 1.f / l : 0.f;
-            uint16_t *dst = static_cast<uint16_t *>(a.out) + (h * a.n + i) * D + g * kHalf;
+            uint16_t *dst = static_cast<uint16_t *>(a.out) + (h * a.n + i) * D;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kHalf; c0 += 32) {
+            for (int c0 = g * 32; c0 < D; c0 += kGroups * 32) {
                 uint32_t ov[32];
-                tc::tmem_ld32(tmem + C::cO + uint32_t(g * kHalf + c0) + lane_off, ov);
+                tc::tmem_ld32(tmem + C::cO + uint32_t(c0) + lane_off, ov);
                 tc::tmem_ld_wait();
                 if (i < a.n) {
 #pragma unroll
@@ -381,10 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 }
             }
         } else if (nl == 0 && i < a.n) {
-            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (h * a.n + i) * D +
-                                                   g * kHalf);
+            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + (h * a.n + i) * D);
+            for (int v = g * 4; v < D / 8; v += kGroups * 4) {               // nothing listed
 #pragma unroll
-            for (int v = 0; v < kHalf / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);   // nothing listed
+                for (int e = 0; e < 4; ++e) dst[v + e] = make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
 
