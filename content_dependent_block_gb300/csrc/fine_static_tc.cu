@@ -104,6 +104,69 @@ __device__ __forceinline__ bool block_full(const FineArgs &a, int64_t i0, int64_
     return a.window >= 0 && i1 - j0 <= a.window && j1 - i0 <= a.window;
 }
 
+// Bits [lo, hi) of a 32-bit word, the bounds clamped to [0, 32].
+__device__ __forceinline__ uint32_t bits_between(int64_t lo, int64_t hi) {
+    const int l = int(lo < 0 ? 0 : (lo > 32 ? 32 : lo));
+    const int h = int(hi < 0 ? 0 : (hi > 32 ? 32 : hi));
+    if (l >= h) return 0u;
+    return (h == 32 ? 0xffffffffu : (1u << h) - 1u) & ~((1u << l) - 1u);
+}
+
+// Bit c set iff key jc + c (c < 32) lies in the sequence and the predicate
+// admits it for query i: the same sets as mask_admits, built once per 32 keys
+// from the ranges they form (|i - j| <= w and i - W < j <= i are intervals of
+// j; j mod s == 0 is every s-th column).
+__device__ __forceinline__ uint32_t admitted_bits(const FineArgs &a, int64_t i, int64_t jc) {
+    const uint32_t inside = bits_between(0, a.n - jc);
+    const int64_t d0 = i - jc;                           // key jc + c has i - j = d0 - c
+    if (a.mask_kind == 2) return inside & bits_between(d0 - a.sliding + 1, d0 + 1);
+    if (a.mask_kind != 1) return inside;
+    uint32_t m = a.window >= 0 ? bits_between(d0 - a.window, d0 + int64_t(a.window) + 1) : 0u;
+    if (a.stride > 0) {
+        const int64_t r0 = jc % a.stride;
+        for (int64_t c = r0 == 0 ? 0 : a.stride - r0; c < 32; c += a.stride) m |= 1u << int(c);
+    }
+    return inside & m;
+}
+
+// Row maximum of 32 raw scores; kMasked keeps only the columns set in `adm`.
+template <bool kMasked>
+__device__ __forceinline__ float chunk_max(const uint32_t (&sv)[32], uint32_t adm) {
+    float m[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m[e] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        const float x = __uint_as_float(sv[c]);
+        m[c & 7] = fmaxf(m[c & 7], (!kMasked || ((adm >> c) & 1u)) ? x : -INFINITY);
+    }
+#pragma unroll
+    for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) m[e] = fmaxf(m[e], m[e + w]);
+    return m[0];
+}
+
+// p = 2^(s * scale_log2 - mm) of 32 raw scores (0 where not admitted), packed
+// to bf16 pairs; returns their fp32 sum.
+template <bool kMasked>
+__device__ __forceinline__ float chunk_exp(const uint32_t (&sv)[32], uint32_t adm, float scale_log2,
+                                           float mm, uint32_t (&pk)[16]) {
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+        float p[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            p[e] = ex2(fmaf(__uint_as_float(sv[c + e]), scale_log2, -mm));
+            if (kMasked && !((adm >> (c + e)) & 1u)) p[e] = 0.f;
+        }
+        ls[(c >> 1) & 3] += p[0] + p[1];
+        pk[c >> 1] = pack_bf16x2(p[0], p[1]);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -300,13 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 uint32_t sv[32];
                 tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
                 tc::tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const bool adm = full || (j0 + c0 + c < a.n &&
-                                              mask_admits(a.mask_kind, a.window, a.stride, a.sliding,
-                                                          i, j0 + c0 + c));
-                    if (adm) mraw = fmaxf(mraw, __uint_as_float(sv[c]));
-                }
+                mraw = fmaxf(mraw, full ? chunk_max<false>(sv, 0u)
+                                        : chunk_max<true>(sv, admitted_bits(a, i, j0 + c0)));
             }
             tc::tc_fence_before();
             tc::mbar_arrive(bars + C::bSFree + j);
@@ -339,19 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                     tc::mbar_arrive(bars + C::bSFree + j);
                 }
                 uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float p[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int64_t jj = j0 + c0 + c + e;
-                        const bool adm = full || (jj < a.n && mask_admits(a.mask_kind, a.window,
-                                                                          a.stride, a.sliding, i, jj));
-                        p[e] = adm ? ex2(fmaf(__uint_as_float(sv[c + e]), a.scale_log2, -mm)) : 0.f;
-                    }
-                    l += p[0] + p[1];
-                    pk[c >> 1] = pack_bf16x2(p[0], p[1]);
-                }
+                l += full ? chunk_exp<false>(sv, 0u, a.scale_log2, mm, pk)
+                          : chunk_exp<true>(sv, admitted_bits(a, i, j0 + c0), a.scale_log2, mm, pk);
                 if (c0 == 0 && jb >= C::kRing &&
                     !tc::mbar_wait(bars + C::bPFree + r, ((jb / C::kRing) - 1) & 1, status)) {
                     ok = false;

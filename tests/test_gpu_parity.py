@@ -216,19 +216,23 @@ def test_dense_list_null_is_full_attention():
 # ------------------------------------- static lists on the tensor cores
 # bf16, 64-key blocks, one list row per 128-query tile: the query-tile-major
 # tcgen05 kernel (exact two-pass softmax), against the plain masked definition.
-@pytest.mark.parametrize("n,d,per_head", [(4096, 64, False), (4100, 64, True), (1000, 128, False)])
-def test_static_tc_local_global_bf16(n, d, per_head):
+# Windows and strides that cut 32-key chunks at odd places: stride 1 (every
+# key), a window of 0 (the diagonal only), a stride that divides no block.
+@pytest.mark.parametrize("n,d,per_head,w,s", [(4096, 64, False, 32, 512), (4100, 64, True, 32, 512),
+                                              (1000, 128, False, 32, 512), (2000, 64, False, 70, 100),
+                                              (900, 128, False, -1, 1), (1500, 64, True, 0, 37)])
+def test_static_tc_local_global_bf16(n, d, per_head, w, s):
     import torch
     t, (q, k, v) = _small(2, n, d, seed=n + 7)
-    m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, 32, 512)
+    m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, w, s)
     lst, _, _ = bsa.static_blocks(n, 128, 64, m)
     dl = torch.from_numpy(np.ascontiguousarray(np.stack([lst, lst]) if per_head else lst)).cuda()
     out = bsa.fine_attention(q, k, v, dl, key_block=64, q_group=128, per_head=per_head, mask=m)
     rows = oracle.all_rows(2, n)
-    ref, _, psum = oracle.masked(t.q, t.k, t.v, oracle.MASK_LOCAL_GLOBAL, rows, w=32, s=512)
+    ref, _, psum = oracle.masked(t.q, t.k, t.v, oracle.MASK_LOCAL_GLOBAL, rows, w=w, s=s)
     np.testing.assert_allclose(psum, 1.0, atol=1e-12)
     parity.assert_close(parity.from_device(out).reshape(-1, d), ref, "bf16",
-                        f"tensor-core local+global n={n} d={d}")
+                        f"tensor-core local+global n={n} d={d} w={w} s={s}")
     assert bsa.device_status() == 0
 
 
