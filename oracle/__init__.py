@@ -26,7 +26,7 @@ _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
 BF16, FP32 = 0, 1
-MASK_LOCAL_GLOBAL, MASK_SLIDING = 1, 2
+MASK_LOCAL_GLOBAL, MASK_SLIDING, MASK_CAUSAL = 1, 2, 3
 
 _lib = None
 
@@ -56,8 +56,9 @@ def _load():
         lib.orc_pool.argtypes = [vp, i32, i64, i64, i64, i64, vp]
         lib.orc_scores.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, i64, vp]
         lib.orc_topk.argtypes = [vp, i64, i64, i64, vp, vp]
+        lib.orc_select.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, i32, i32, vp]
         lib.orc_fine.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, vp, i64,
-                                 vp, i64, dbl, vp, vp, vp]
+                                 vp, i64, i32, dbl, vp, vp, vp]
         lib.orc_mask.argtypes = [i32, i64, i64, i64, i64, i64]
         lib.orc_mask.restype = ctypes.c_int
         lib.orc_masked.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32, i64,
@@ -132,9 +133,31 @@ def topk(s: np.ndarray, k: int):
     return idx, kth
 
 
+def select(s: np.ndarray, rows: np.ndarray, n: int, key_block: int, k: int, *,
+           head_k: Optional[np.ndarray] = None, causal: bool = False,
+           local: bool = False) -> np.ndarray:
+    """Selection with options: per-(batch*head) budgets ``head_k`` (int, in
+    [0, k]; page "sparse-attention-triton-bench", What's next), causal
+    eligibility b <= i // key_block (page "Block-Sparse & Linear Attention
+    Kernels", section 1, causal pattern) and the always-include-local-block
+    variant.  ``s`` holds the scores of ``rows`` (flat bh*n + i).  Returns
+    ascending ids [len(rows), k], -1 padded."""
+    s = np.ascontiguousarray(s, dtype=np.float64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    nrows, nb = s.shape
+    if nrows != rows.size:
+        raise ValueError("one score row per requested query row")
+    hk = None if head_k is None else np.ascontiguousarray(head_k, dtype=np.int32)
+    idx = np.empty((nrows, k), dtype=np.int32)
+    _load().orc_select(_ptr(s), _ptr(rows), nrows, nb, n, key_block, k,
+                       None if hk is None else _ptr(hk), int(causal), int(local), _ptr(idx))
+    return idx
+
+
 def fine(q, k, v, key_block: int, idx: np.ndarray, rows: np.ndarray,
-         scale: Optional[float] = None):
-    """Softmax attention of each row over the tokens of its listed blocks.
+         scale: Optional[float] = None, causal: bool = False):
+    """Softmax attention of each row over the tokens of its listed blocks
+    (only keys j <= i with ``causal``).
 
     ``idx`` is [len(rows), kmax] int32 (entries < 0 ignored).  Returns
     (O [rows, d] float64, lse [rows], psum [rows]).
@@ -150,7 +173,7 @@ def fine(q, k, v, key_block: int, idx: np.ndarray, rows: np.ndarray,
     lse = np.empty(rows.size, dtype=np.float64)
     psum = np.empty(rows.size, dtype=np.float64)
     _load().orc_fine(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), bh, n, d,
-                     key_block, _ptr(idx), kk, _ptr(rows), rows.size,
+                     key_block, _ptr(idx), kk, _ptr(rows), rows.size, int(causal),
                      ctypes.c_double(scale), _ptr(o), _ptr(lse), _ptr(psum))
     return o, lse, psum
 
@@ -190,12 +213,19 @@ def active_tiles(n: int, tq: int, tk: int, kind: int, *, w: int = -1,
 
 
 def forward(q, k, v, key_block: int, topk_k: int, rows: np.ndarray,
-            scale: Optional[float] = None):
+            scale: Optional[float] = None, *, head_k: Optional[np.ndarray] = None,
+            causal: bool = False, local: bool = False):
     """The whole dynamic path for the requested rows, step by step:
-    pool -> scores -> top-k -> fine.  Returns a dict of every intermediate."""
+    pool -> scores -> top-k (or the selection with options) -> fine.
+    Returns a dict of every intermediate (``kth`` only without options)."""
     kbar = pool(k, key_block)
     s = scores(q, kbar, rows)
-    idx, kth = topk(s, topk_k)
-    o, lse, psum = fine(q, k, v, key_block, idx, rows, scale)
+    if head_k is None and not causal and not local:
+        idx, kth = topk(s, topk_k)
+    else:
+        idx = select(s, rows, q.shape[1], key_block, topk_k, head_k=head_k,
+                     causal=causal, local=local)
+        kth = None
+    o, lse, psum = fine(q, k, v, key_block, idx, rows, scale, causal=causal)
     return {"kbar": kbar, "scores": s, "idx": idx, "kth": kth, "o": o,
             "lse": lse, "psum": psum}

@@ -17,7 +17,12 @@
  *        attends key j iff |i-j| <= w (local window) or j % s == 0 (global
  *        stride); a tile is skipped iff it holds no active pair.
  *   [P3] "Block-Sparse & Linear Attention Kernels", section 2, "Sliding
- *        Window Attention (Mistral)": softmax(q_i K_win^T / sqrt(d_k)) V_win.
+ *        Window Attention (Mistral)": softmax(q_i K_win^T / sqrt(d_k)) V_win;
+ *        section 1, "Common Sparse Patterns": the causal (lower-triangle)
+ *        pattern.
+ *   [P1] section "What's next", per-head sparsity budgets: top_k chosen per
+ *        head instead of one global value, on the same per-head stage-1
+ *        scores.
  *
  * Readings where the pages are silent:
  *   - softmax scale 1/sqrt(d) comes from [P3]; the caller passes it;
@@ -30,7 +35,15 @@
  *     itself: i-W < j <= i;
  *   - the softmax is a plain two-pass softmax (max, then exponentials), NOT
  *     an online one, so it shares no structure with the GPU path;
- *   - a row with no selected token yields O = 0, lse = -inf, psum = 0.
+ *   - a row with no selected token yields O = 0, lse = -inf, psum = 0;
+ *   - causal dynamic selection: query i may select only the blocks that hold
+ *     a key j <= i, i.e. b <= floor(i / B), and attends only keys j <= i
+ *     inside them (the causal pattern of [P3] section 1 applied at both
+ *     stages);
+ *   - the always-include-local-block variant: the query's own block
+ *     floor(i / B) is selected first and the other k - 1 blocks by score;
+ *     a budget of 0 selects nothing;
+ *   - a per-head budget k_h lies in [0, k]; k is the list width.
  *
  * Layout: Q, K, V are [BH][N][d] row-major, element type bf16 (raw bit
  * patterns, widened exactly) or fp32.  All outputs are double.
@@ -48,6 +61,7 @@
 
 #define ORC_MASK_LOCAL_GLOBAL 1
 #define ORC_MASK_SLIDING 2
+#define ORC_MASK_CAUSAL 3
 
 /* Exact widening of one input element to double. */
 static double widen(const void *base, int dtype, int64_t i) {
@@ -164,6 +178,51 @@ void orc_topk(const double *S, int64_t nrows, int64_t nb, int64_t k,
 }
 
 /*
+ * Stage 2 selection with the options ([P1] "What's next" per-head budgets;
+ * [P3] section 1 causal pattern; the local-block variant).  Row r is query
+ * i of (batch*head) row bh, rows[r] = bh*N + i.  Its budget is
+ * k_r = head_k[bh] (or k when head_k is NULL); its eligible blocks are all
+ * nb blocks, or b <= floor(i/B) when causal.  With `local`, block
+ * floor(i/B) is taken first (if k_r >= 1) and the other k_r - 1 are the
+ * best-scoring eligible blocks except it; without, the k_r best eligible
+ * blocks.  Best = (score desc, block asc).  Output as orc_topk: ascending
+ * ids, -1 padded to width k.
+ */
+void orc_select(const double *S, const int64_t *rows, int64_t nrows,
+                int64_t nb, int64_t N, int64_t B, int64_t k,
+                const int32_t *head_k, int causal, int local, int32_t *idx) {
+#pragma omp parallel
+    {
+        scored_block *tmp = (scored_block *)malloc(sizeof(scored_block) * (size_t)nb);
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < nrows; ++r) {
+            int64_t bh = rows[r] / N;
+            int64_t i = rows[r] % N;
+            int64_t own = i / B;
+            int64_t kr = head_k ? head_k[bh] : k;
+            if (kr < 0) kr = 0;
+            if (kr > k) kr = k;
+            int64_t last = causal ? own : nb - 1;   /* eligible: b <= last */
+            int32_t *out = idx + r * k;
+            int64_t taken = 0;
+            if (local && kr >= 1) out[taken++] = (int32_t)own;
+            int64_t ne = 0;
+            for (int64_t b = 0; b <= last; ++b) {
+                if (local && b == own) continue;
+                tmp[ne].score = S[r * nb + b];
+                tmp[ne].block = (int32_t)b;
+                ++ne;
+            }
+            qsort(tmp, (size_t)ne, sizeof(scored_block), by_score_then_block);
+            for (int64_t t = 0; t < ne && taken < kr; ++t) out[taken++] = tmp[t].block;
+            qsort(out, (size_t)taken, sizeof(int32_t), ascending_int);
+            for (int64_t t = taken; t < k; ++t) out[t] = -1;
+        }
+        free(tmp);
+    }
+}
+
+/*
  * Softmax attention of one query over an explicit token list, two passes:
  * s_j = scale * q.k_j ; m = max s_j ; p_j = exp(s_j - m) ; l = sum p_j ;
  * o = sum p_j v_j / l.  Also returns lse = m + log l and the row sum of the
@@ -212,13 +271,14 @@ static void attend_tokens(const void *Q, const void *K, const void *V,
  * [P1] Stage 2, fine attention: for row r (rows[r] = bh*N + i) the token set
  * is the union of the B tokens of each listed block idx[r][0..k) (entries
  * < 0 are padding; a ragged last block contributes its valid tokens only),
- * and the output is dense softmax attention over that set.
+ * and the output is dense softmax attention over that set.  With `causal`
+ * only the keys j <= i of those blocks are in the set ([P3] section 1).
  * O is [nrows][d]; lse and psum are [nrows].
  */
 void orc_fine(const void *Q, const void *K, const void *V, int dtype,
               int64_t BH, int64_t N, int64_t d, int64_t B,
               const int32_t *idx, int64_t k, const int64_t *rows,
-              int64_t nrows, double scale, double *O, double *lse,
+              int64_t nrows, int causal, double scale, double *O, double *lse,
               double *psum) {
     (void)BH;
 #pragma omp parallel
@@ -234,7 +294,7 @@ void orc_fine(const void *Q, const void *K, const void *V, int dtype,
                 int32_t b = idx[r * k + t];
                 if (b < 0) continue;
                 for (int64_t j = (int64_t)b * B; j < ((int64_t)b + 1) * B && j < N; ++j)
-                    tok[ntok++] = j;
+                    if (!causal || j <= i) tok[ntok++] = j;
             }
             attend_tokens(Q, K, V, dtype, N, d, bh, i, tok, ntok, scale, sb,
                           O + r * d, lse + r, psum + r);
@@ -249,6 +309,7 @@ void orc_fine(const void *Q, const void *K, const void *V, int dtype,
  *  [P2] local + global: |i-j| <= w  or  j % s == 0  (w < 0 disables the
  *       local band, s <= 0 disables the global columns);
  *  [P3] sliding window, causal, W tokens including i:  i-W < j <= i.
+ *  [P3] section 1, causal (lower triangle):  j <= i.
  */
 int orc_mask(int kind, int64_t w, int64_t s, int64_t W, int64_t i, int64_t j) {
     if (kind == ORC_MASK_LOCAL_GLOBAL) {
@@ -258,6 +319,7 @@ int orc_mask(int kind, int64_t w, int64_t s, int64_t W, int64_t i, int64_t j) {
         return local || global;
     }
     if (kind == ORC_MASK_SLIDING) return (j > i - W) && (j <= i);
+    if (kind == ORC_MASK_CAUSAL) return j <= i;
     return 1;
 }
 
