@@ -17,7 +17,7 @@ import numpy as np
 from . import _build
 
 BF16, FP32 = 0, 1
-MASK_NONE, MASK_LOCAL_GLOBAL, MASK_SLIDING = 0, 1, 2
+MASK_NONE, MASK_LOCAL_GLOBAL, MASK_SLIDING, MASK_CAUSAL = 0, 1, 2, 3
 
 STATUS = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
           3: "BSA_ERR_BAD_INDEX", 4: "BSA_ERR_WORKSPACE", 5: "BSA_ERR_CUDA",
@@ -26,8 +26,9 @@ STATUS = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
 # Every symbol include/bsa.h declares.
 EXPORTS = (
     "bsa_pool_blocks", "bsa_coarse_topk_workspace_size", "bsa_coarse_topk",
-    "bsa_fine_attention_workspace_size", "bsa_fine_attention",
-    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_noalloc", "bsa_forward_launches",
+    "bsa_coarse_topk_ex", "bsa_fine_attention_workspace_size", "bsa_fine_attention",
+    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_ex", "bsa_forward_noalloc",
+    "bsa_forward_launches",
     "bsa_static_max_blocks",
     "bsa_static_blocks", "bsa_get_device_status", "bsa_status_string",
     "bsa_last_error", "bsa_version",
@@ -55,6 +56,13 @@ class ListDesc(ctypes.Structure):
                 ("max_blocks", ctypes.c_int32), ("per_head", ctypes.c_int32)]
 
 
+class Select(ctypes.Structure):
+    """bsa_select: per-head budgets (device int32 [bh] or NULL), causal
+    selection, always-include-local-block."""
+    _fields_ = [("head_topk", ctypes.c_void_p), ("causal", ctypes.c_int32),
+                ("local_block", ctypes.c_int32)]
+
+
 _lib = None
 
 
@@ -77,10 +85,14 @@ def lib():
         "bsa_pool_blocks": ([Shape, vp, i32, vp, vp], i32),
         "bsa_coarse_topk_workspace_size": ([Shape, i32, i32], sz),
         "bsa_coarse_topk": ([Shape, vp, vp, i32, i32, vp, vp, sz, vp], i32),
+        "bsa_coarse_topk_ex": ([Shape, vp, vp, i32, i32, ctypes.POINTER(Select), vp, vp, sz, vp],
+                               i32),
         "bsa_fine_attention_workspace_size": ([Shape, ListDesc, Mask], sz),
         "bsa_fine_attention": ([Shape, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, sz, vp], i32),
         "bsa_forward_workspace_size": ([Shape, i32, i32], sz),
         "bsa_forward": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp], i32),
+        "bsa_forward_ex": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp, vp, vp,
+                            sz, vp], i32),
         "bsa_forward_noalloc": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp], i32),
         "bsa_forward_launches": ([Shape, i32, i32], i32),
         "bsa_static_max_blocks": ([i64, i32, i32, Mask], i32),
@@ -148,14 +160,29 @@ def pool_blocks(k, key_block: int):
     return kbar
 
 
-def coarse_topk(q, kbar, key_block: int, topk: int):
-    """Top-k block ids [bh, n, topk] int32 (ascending, -1 padded)."""
+def _select(head_topk, causal: bool, local_block: bool):
+    """A Select for the options, or None when there are none."""
+    if head_topk is None and not causal and not local_block:
+        return None
+    if head_topk is not None and (head_topk.dtype != _torch().int32 or not head_topk.is_cuda
+                                  or not head_topk.is_contiguous()):
+        raise TypeError("head_topk must be a contiguous int32 CUDA tensor [bh]")
+    return Select(None if head_topk is None else head_topk.data_ptr(), int(bool(causal)),
+                  int(bool(local_block)))
+
+
+def coarse_topk(q, kbar, key_block: int, topk: int, *, head_topk=None, causal: bool = False,
+                local_block: bool = False):
+    """Top-k block ids [bh, n, topk] int32 (ascending, -1 padded); with the
+    selection options of bsa_coarse_topk_ex when any is given."""
     s = _shape(q)
     idx = _torch().empty((s.bh, s.n, topk), dtype=_torch().int32, device=q.device)
     ws_n = lib().bsa_coarse_topk_workspace_size(s, key_block, topk)
     ws = _workspace(ws_n, q.device)
-    _check(lib().bsa_coarse_topk(s, _ptr(q), _ptr(kbar), key_block, topk, _ptr(idx),
-                                 _ptr(ws), ws_n, _stream()))
+    sel = _select(head_topk, causal, local_block)
+    _check(lib().bsa_coarse_topk_ex(s, _ptr(q), _ptr(kbar), key_block, topk,
+                                    None if sel is None else ctypes.byref(sel), _ptr(idx),
+                                    _ptr(ws), ws_n, _stream()))
     return idx
 
 
@@ -188,10 +215,13 @@ class Forward:
     one shape so repeated calls allocate nothing."""
 
     def __init__(self, bh: int, n: int, d: int, key_block: int, topk: int, device="cuda",
-                 scale: float = 0.0):
+                 scale: float = 0.0, *, head_topk=None, causal: bool = False,
+                 local_block: bool = False):
         torch = _torch()
         self.shape = Shape(bh, n, d, BF16)
         self.key_block, self.topk, self.scale = key_block, topk, scale
+        self.head_topk = head_topk            # kept alive: the library reads it on every call
+        self.sel = _select(head_topk, causal, local_block)
         self.ws_bytes = lib().bsa_forward_workspace_size(self.shape, key_block, topk)
         self.ws = _workspace(self.ws_bytes, device)
         self.out = torch.empty((bh, n, d), dtype=torch.bfloat16, device=device)
@@ -206,17 +236,21 @@ class Forward:
         s = _shape(q)
         if (s.bh, s.n, s.d) != (self.shape.bh, self.shape.n, self.shape.d):
             raise ValueError("shape differs from the one this Forward was built for")
-        _check(lib().bsa_forward(self.shape, _ptr(q), _ptr(k), _ptr(v), self.key_block,
-                                 self.topk, float(self.scale), _ptr(self.out),
-                                 _ptr(self.idx if keep_idx else None), _ptr(self.ws),
-                                 self.ws_bytes, _stream()))
+        _check(lib().bsa_forward_ex(self.shape, _ptr(q), _ptr(k), _ptr(v), self.key_block,
+                                    self.topk, None if self.sel is None else ctypes.byref(self.sel),
+                                    float(self.scale), _ptr(self.out),
+                                    _ptr(self.idx if keep_idx else None), _ptr(self.ws),
+                                    self.ws_bytes, _stream()))
         return self.out
 
 
-def forward(q, k, v, key_block: int, topk: int, scale: float = 0.0) -> Tuple[object, object]:
-    """Whole dynamic forward; returns (out, idx)."""
+def forward(q, k, v, key_block: int, topk: int, scale: float = 0.0, *, head_topk=None,
+            causal: bool = False, local_block: bool = False) -> Tuple[object, object]:
+    """Whole dynamic forward (with the selection options of bsa_forward_ex);
+    returns (out, idx)."""
     s = _shape(q)
-    f = Forward(s.bh, s.n, s.d, key_block, topk, device=q.device, scale=scale)
+    f = Forward(s.bh, s.n, s.d, key_block, topk, device=q.device, scale=scale,
+                head_topk=head_topk, causal=causal, local_block=local_block)
     out = f(q, k, v, keep_idx=True)
     return out, f.idx
 

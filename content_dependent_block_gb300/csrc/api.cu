@@ -115,11 +115,31 @@ ForwardLayout forward_layout(const bsa_shape &s, int32_t kb, int32_t topk) {
 
 // Scoring + selection from fp32 means (and their bf16 pair when present).
 cudaError_t run_coarse(const bsa_shape &s, const void *q, const float *kbar, const uint16_t *hi,
-                       const uint16_t *lo, int64_t nb, int32_t topk, int32_t *idx,
-                       int32_t *status, cudaStream_t st) {
+                       const uint16_t *lo, int64_t nb, int32_t topk, const bsa::SelectOpts &o,
+                       int32_t *idx, int32_t *status, cudaStream_t st) {
     if (hi != nullptr && bsa::coarse_tc_supported(nb))
-        return bsa::launch_coarse_topk_tc(q, hi, lo, s.bh, s.n, s.d, nb, topk, idx, status, st);
-    return bsa::launch_coarse_topk_simt(q, kbar, s.bh, s.n, s.d, nb, topk, idx, st);
+        return bsa::launch_coarse_topk_tc(q, hi, lo, s.bh, s.n, s.d, nb, topk, o, idx, status, st);
+    return bsa::launch_coarse_topk_simt(q, kbar, s.bh, s.n, s.d, nb, topk, o, idx, status, st);
+}
+
+// The selection options of `sel` (NULL: none) for blocks of kb tokens.
+bsa::SelectOpts select_opts(const bsa_select *sel, int32_t kb) {
+    bsa::SelectOpts o;
+    o.kb = kb;
+    if (sel != nullptr) {
+        o.head_k = sel->head_topk;
+        o.causal = sel->causal ? 1 : 0;
+        o.local = sel->local_block ? 1 : 0;
+    }
+    return o;
+}
+
+bool has_options(const bsa::SelectOpts &o) { return o.head_k != nullptr || o.causal || o.local; }
+
+bsa_status check_select(const bsa_select *sel) {
+    if (sel != nullptr && sel->head_topk != nullptr && !aligned(sel->head_topk, 4))
+        return fail(BSA_ERR_ALIGNMENT, "head_topk is not 4-byte aligned");
+    return BSA_OK;
 }
 
 // Workspace of the block-major fine stage over per-query lists [bh][n][k].
@@ -180,8 +200,8 @@ bool bm_path(const bsa_shape &s, int32_t kb, int64_t nb) {
 // Invert the lists and run the block-major fine stage; ws points at L.
 cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const void *v,
                         const int32_t *list, int32_t kb, int32_t topk, bool full_lists,
-                        float scale_log2, void *out, char *ws, const BmLayout &L,
-                        int32_t *status, cudaStream_t st) {
+                        bool causal, const bsa::SelectOpts *sel, float scale_log2, void *out,
+                        char *ws, const BmLayout &L, int32_t *status, cudaStream_t st) {
     const int64_t nb = ceil_div(s.n, kb);
     cudaError_t e = cudaMemsetAsync(ws + L.zero, 0, L.zero_bytes, st);
     if (e != cudaSuccess) return e;
@@ -219,6 +239,9 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     a.d = s.d;
     a.k = topk;
     a.full_lists = full_lists ? 1 : 0;
+    a.causal = causal ? 1 : 0;
+    a.sel_lists = sel != nullptr ? 1 : 0;
+    a.head_k = sel != nullptr ? sel->head_k : nullptr;
     a.scale_log2 = scale_log2;
     a.part_o = reinterpret_cast<uint16_t *>(ws + L.part_o);
     a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
@@ -295,6 +318,12 @@ size_t bsa_coarse_topk_workspace_size(bsa_shape shape, int32_t key_block, int32_
 
 bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, int32_t key_block,
                            int32_t topk, int32_t *idx, void *ws, size_t ws_bytes, void *stream) {
+    return bsa_coarse_topk_ex(shape, q, kbar, key_block, topk, nullptr, idx, ws, ws_bytes, stream);
+}
+
+bsa_status bsa_coarse_topk_ex(bsa_shape shape, const void *q, const float *kbar, int32_t key_block,
+                              int32_t topk, const bsa_select *sel, int32_t *idx, void *ws,
+                              size_t ws_bytes, void *stream) {
     BSA_TRY(check_shape(shape));
     if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "scoring takes bf16 queries");
     BSA_TRY(check_key_block(key_block));
@@ -302,6 +331,7 @@ bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, in
     BSA_TRY(check_ptr(q, "q"));
     BSA_TRY(check_ptr(kbar, "kbar"));
     BSA_TRY(check_ptr(idx, "idx"));
+    BSA_TRY(check_select(sel));
     const size_t need = bsa_coarse_topk_workspace_size(shape, key_block, topk);
     BSA_TRY(check_ws(ws, ws_bytes, need));
     const int64_t nb = ceil_div(shape.n, key_block);
@@ -315,25 +345,30 @@ bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar, in
         BSA_TRY(launched(bsa::launch_split_kbar(kbar, shape.bh * nb * shape.d, hi, lo, st),
                          "split launch"));
     }
-    return launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, idx, status, st),
+    return launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, select_opts(sel, key_block), idx,
+                               status, st),
                     "coarse top-k launch");
 }
 
-// Per-query lists (q_group = 1, one list per head) of bf16 inputs with
-// 64-token blocks take the block-major tensor-core schedule; everything else
-// (static tile lists, fp32, other block sizes) the query-major kernel.
+// Per-query lists (q_group = 1, one list per head, no mask or the causal
+// one) of bf16 inputs with 64-token blocks take the block-major tensor-core
+// schedule; everything else (static tile lists, fp32, other block sizes) the
+// query-major kernel.
+bool bm_lists(const bsa_shape &shape, const bsa_list_desc &ld, const bsa_mask &mask) {
+    return ld.q_group == 1 && ld.per_head &&
+           (mask.kind == BSA_MASK_NONE || mask.kind == BSA_MASK_CAUSAL) && ld.max_blocks >= 1 &&
+           ld.max_blocks <= 32 && bm_path(shape, ld.key_block, ceil_div(shape.n, ld.key_block));
+}
+
 bool fine_uses_bm(const bsa_shape &shape, const int32_t *list, const bsa_list_desc &ld,
                   const bsa_mask &mask) {
-    return list != nullptr && ld.q_group == 1 && ld.per_head && mask.kind == BSA_MASK_NONE &&
-           ld.max_blocks <= 32 && bm_path(shape, ld.key_block, ceil_div(shape.n, ld.key_block));
+    return list != nullptr && bm_lists(shape, ld, mask);
 }
 
 size_t bsa_fine_attention_workspace_size(bsa_shape shape, bsa_list_desc ld, bsa_mask mask) {
     if (check_shape(shape) != BSA_OK || check_key_block(ld.key_block) != BSA_OK) return 0;
     // a non-null list is assumed; the query-major path needs no workspace
-    if (!(ld.q_group == 1 && ld.per_head && mask.kind == BSA_MASK_NONE && ld.max_blocks >= 1 &&
-          ld.max_blocks <= 32 && bm_path(shape, ld.key_block, ceil_div(shape.n, ld.key_block))))
-        return 0;
+    if (!bm_lists(shape, ld, mask)) return 0;
     return bm_layout(shape, ld.key_block, ld.max_blocks, 0).total;
 }
 
@@ -351,7 +386,7 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
         if (ld.q_group < 1 || ld.max_blocks < 1)
             return fail(BSA_ERR_INVALID_ARG, "list needs q_group >= 1 and max_blocks >= 1");
     }
-    if (mask.kind < BSA_MASK_NONE || mask.kind > BSA_MASK_SLIDING)
+    if (mask.kind < BSA_MASK_NONE || mask.kind > BSA_MASK_CAUSAL)
         return fail(BSA_ERR_INVALID_ARG, "bad mask kind %d", mask.kind);
     if (mask.kind == BSA_MASK_SLIDING && mask.sliding < 1)
         return fail(BSA_ERR_INVALID_ARG, "sliding window needs W >= 1");
@@ -364,8 +399,9 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
     const float sl2 = softmax_scale_log2(scale, shape.d);
     if (bm) {
         const BmLayout L = bm_layout(shape, ld.key_block, ld.max_blocks, 0);
-        return launched(run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false, sl2,
-                                    out, static_cast<char *>(ws), L, status, st),
+        return launched(run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false,
+                                    mask.kind == BSA_MASK_CAUSAL, nullptr, sl2, out,
+                                    static_cast<char *>(ws), L, status, st),
                         "fine attention (block-major) launch");
     }
     bsa::FineArgs a{};
@@ -414,6 +450,13 @@ int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk) {
 bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void *v,
                        int32_t key_block, int32_t topk, float scale, void *out, int32_t *idx_out,
                        void *ws, size_t ws_bytes, void *stream) {
+    return bsa_forward_ex(shape, q, k, v, key_block, topk, nullptr, scale, out, idx_out, ws,
+                          ws_bytes, stream);
+}
+
+bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const void *v,
+                          int32_t key_block, int32_t topk, const bsa_select *sel, float scale,
+                          void *out, int32_t *idx_out, void *ws, size_t ws_bytes, void *stream) {
     BSA_TRY(check_shape(shape));
     if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "the dynamic forward takes bf16");
     BSA_TRY(check_key_block(key_block));
@@ -423,6 +466,8 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     BSA_TRY(check_ptr(v, "v"));
     BSA_TRY(check_ptr(out, "out"));
     if (idx_out != nullptr) BSA_TRY(check_ptr(idx_out, "idx_out"));
+    BSA_TRY(check_select(sel));
+    const bsa::SelectOpts opts = select_opts(sel, key_block);
     const ForwardLayout L = forward_layout(shape, key_block, topk);
     BSA_TRY(check_ws(ws, ws_bytes, bsa_forward_workspace_size(shape, key_block, topk)));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -437,13 +482,15 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
 
     BSA_TRY(launched(bsa::launch_pool(k, shape.bh, shape.n, shape.d, key_block, kbar, hi, lo, nb,
                                       st), "pool launch"));
-    BSA_TRY(launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, idx, status, st),
+    BSA_TRY(launched(run_coarse(shape, q, kbar, hi, lo, nb, topk, opts, idx, status, st),
                      "coarse top-k launch"));
     const float sl2 = softmax_scale_log2(scale, shape.d);
     if (bm_path(shape, key_block, nb)) {
         const BmLayout B = bm_layout(shape, key_block, topk, L.total);
-        return launched(run_fine_bm(shape, q, k, v, idx, key_block, topk, true, sl2, out, base, B,
-                                    status, st),
+        // options leave -1 padding (budgets, early causal queries): lists are not full
+        return launched(run_fine_bm(shape, q, k, v, idx, key_block, topk, !has_options(opts),
+                                    opts.causal != 0, has_options(opts) ? &opts : nullptr, sl2,
+                                    out, base, B, status, st),
                         "fine attention (block-major) launch");
     }
     bsa::FineArgs a{};
@@ -461,7 +508,7 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
     a.max_blocks = topk;
     a.per_head = 1;
     a.list_rows = shape.n;
-    a.mask_kind = BSA_MASK_NONE;
+    a.mask_kind = opts.causal ? BSA_MASK_CAUSAL : BSA_MASK_NONE;
     a.scale_log2 = sl2;
     a.status = status;
     if (bsa::fine_static_tc_supported(a, shape.dtype))

@@ -7,6 +7,7 @@
 namespace bsa {
 
 // Status codes written by kernels (values match bsa_status in bsa.h).
+constexpr int32_t kStatusInvalidArg = 1;
 constexpr int32_t kStatusBadIndex = 3;
 constexpr int32_t kStatusTimeout = 6;
 
@@ -60,7 +61,29 @@ __device__ __forceinline__ bool mask_admits(int32_t kind, int32_t window,
         return (window >= 0 && dist <= window) || (stride > 0 && (j % stride) == 0);
     }
     if (kind == 2) return j > i - sliding && j <= i;
+    if (kind == 3) return j <= i;
     return true;
+}
+
+// Selection options applied to one query's candidates, held as block ids in
+// descending score order (INT_MAX = empty): keep the first `kr` (the
+// per-head budget of page "sparse-attention-triton-bench", What's next) and,
+// with `local`, make sure the query's own block `own` is among them by
+// putting it in place of the last one kept (the kept set is then own plus
+// the kr - 1 best of the other eligible blocks).
+template <int KMAX>
+__device__ __forceinline__ void apply_budget(int (&ids)[KMAX], int kr, int own, bool local) {
+    bool has_own = false;
+#pragma unroll
+    for (int t = 0; t < KMAX; ++t) {
+        if (t >= kr) ids[t] = 0x7fffffff;
+        has_own |= ids[t] == own;
+    }
+    if (local && !has_own) {
+#pragma unroll
+        for (int t = 0; t < KMAX; ++t)
+            if (t == kr - 1) ids[t] = own;
+    }
 }
 
 }  // namespace bsa

@@ -31,6 +31,14 @@ struct FineArgs {
     int32_t *status;       // device status word
 };
 
+// Options of the dynamic selection (bsa_select in bsa.h).
+struct SelectOpts {
+    const int32_t *head_k = nullptr;   // [bh] budgets in [0, topk], or null: topk
+    int32_t kb = 1;                    // key block: the query's own block is i / kb
+    int32_t causal = 0;                // eligible blocks b <= i / kb
+    int32_t local = 0;                 // the own block is always selected
+};
+
 // Records the one-line reason bsa_last_error() reports on this thread.
 void set_last_error(const char *msg);
 
@@ -41,8 +49,8 @@ cudaError_t launch_pool(const void *k, int64_t bh, int64_t n, int32_t d,
 
 cudaError_t launch_coarse_topk_simt(const void *q, const float *kbar,
                                     int64_t bh, int64_t n, int32_t d,
-                                    int64_t nb, int32_t topk, int32_t *idx,
-                                    cudaStream_t st);
+                                    int64_t nb, int32_t topk, const SelectOpts &o,
+                                    int32_t *idx, int32_t *status, cudaStream_t st);
 
 // fp32 block means -> bf16 (hi, lo) pair for the tensor-core scoring.
 cudaError_t launch_split_kbar(const float *kbar, int64_t count, uint16_t *hi, uint16_t *lo,
@@ -52,7 +60,8 @@ cudaError_t launch_split_kbar(const float *kbar, int64_t count, uint16_t *hi, ui
 bool coarse_tc_supported(int64_t nb);
 cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const uint16_t *kbar_lo,
                                   int64_t bh, int64_t n, int32_t d, int64_t nb, int32_t topk,
-                                  int32_t *idx, int32_t *status, cudaStream_t st);
+                                  const SelectOpts &o, int32_t *idx, int32_t *status,
+                                  cudaStream_t st);
 
 // ---- block-major fine stage over per-query lists [bh][n][k] ----------
 constexpr int32_t kFineBmItemPairs = 512;   // pairs per fine work item (<= 4 tiles)
@@ -101,6 +110,12 @@ struct FineBmArgs {
     int64_t bh, n, nb;
     int32_t d, k;
     int32_t full_lists;           // every row holds min(k, nb) valid ids, first
+    int32_t causal;               // query i attends only keys j <= i
+    // Lists written by the selection with options: row i of head h holds
+    // min(k_h, eligible) ids first (k_h = head_k[h] clamped to [0, k], or k;
+    // eligible = i / 64 + 1 when causal, else nb), -1 after them.
+    int32_t sel_lists;
+    const int32_t *head_k;
     float scale_log2;
     uint16_t *part_o;             // [ring][range * kpad][d] bf16
     float *part_lse;              // [ring][range * kpad]

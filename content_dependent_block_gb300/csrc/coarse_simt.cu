@@ -58,11 +58,14 @@ __device__ __forceinline__ void sort_ids(int (&ti)[KMAX], int kk) {
 template <int D, int KMAX>
 __global__ void __launch_bounds__(kQueries) coarse_topk_simt_kernel(
     const uint16_t *__restrict__ q, const float *__restrict__ kbar, int64_t n,
-    int64_t nb, int32_t topk, int32_t *__restrict__ idx) {
+    int64_t nb, int32_t topk, const SelectOpts o, int32_t *__restrict__ idx, int32_t *status) {
     __shared__ float ks[kChunk][D];
     const int64_t h = blockIdx.y;
     const int64_t i = int64_t(blockIdx.x) * kQueries + threadIdx.x;
     const bool valid = i < n;
+    const int64_t own = i / o.kb;                        // the query's own block
+    // eligible blocks: all, or b <= own (causal)
+    const int64_t last = o.causal ? own : nb - 1;
 
     float qr[D];
     {
@@ -93,31 +96,38 @@ __global__ void __launch_bounds__(kQueries) coarse_topk_simt_kernel(
             float s = 0.f;
 #pragma unroll
             for (int c = 0; c < D; ++c) s = fmaf(qr[c], ks[bb][c], s);
-            if (s > ts[KMAX - 1]) topk_insert<KMAX>(ts, ti, s, int(c0 + bb));
+            if (c0 + bb <= last && s > ts[KMAX - 1]) topk_insert<KMAX>(ts, ti, s, int(c0 + bb));
         }
     }
     if (!valid) return;
-    const int kk = int(i64min(topk, nb));
-    sort_ids<KMAX>(ti, kk);
+    int kr = topk;
+    if (o.head_k != nullptr) {
+        const int32_t hk = __ldg(o.head_k + h);
+        kr = min(max(hk, 0), topk);
+        if (hk != kr) report_status(status, kStatusInvalidArg);
+    }
+    apply_budget<KMAX>(ti, kr, int(own), o.local != 0);
+    sort_ids<KMAX>(ti, kr);
     int32_t *dst = idx + (h * n + i) * topk;
 #pragma unroll
     for (int t = 0; t < KMAX; ++t)
-        if (t < topk) dst[t] = (t < kk && ti[t] != INT_MAX) ? ti[t] : -1;
+        if (t < topk) dst[t] = (t < kr && ti[t] != INT_MAX) ? ti[t] : -1;
 }
 
 template <int D>
 cudaError_t launch_d(const void *q, const float *kbar, int64_t bh, int64_t n,
-                     int64_t nb, int32_t topk, int32_t *idx, cudaStream_t st) {
+                     int64_t nb, int32_t topk, const SelectOpts &o, int32_t *idx,
+                     int32_t *status, cudaStream_t st) {
     const dim3 grid(unsigned((n + kQueries - 1) / kQueries), unsigned(bh));
     const uint16_t *qq = static_cast<const uint16_t *>(q);
     if (topk <= 4)
-        coarse_topk_simt_kernel<D, 4><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, idx);
+        coarse_topk_simt_kernel<D, 4><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, o, idx, status);
     else if (topk <= 8)
-        coarse_topk_simt_kernel<D, 8><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, idx);
+        coarse_topk_simt_kernel<D, 8><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, o, idx, status);
     else if (topk <= 16)
-        coarse_topk_simt_kernel<D, 16><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, idx);
+        coarse_topk_simt_kernel<D, 16><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, o, idx, status);
     else
-        coarse_topk_simt_kernel<D, 32><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, idx);
+        coarse_topk_simt_kernel<D, 32><<<grid, kQueries, 0, st>>>(qq, kbar, n, nb, topk, o, idx, status);
     return cudaGetLastError();
 }
 
@@ -125,10 +135,10 @@ cudaError_t launch_d(const void *q, const float *kbar, int64_t bh, int64_t n,
 
 cudaError_t launch_coarse_topk_simt(const void *q, const float *kbar,
                                     int64_t bh, int64_t n, int32_t d,
-                                    int64_t nb, int32_t topk, int32_t *idx,
-                                    cudaStream_t st) {
-    if (d == 64) return launch_d<64>(q, kbar, bh, n, nb, topk, idx, st);
-    return launch_d<128>(q, kbar, bh, n, nb, topk, idx, st);
+                                    int64_t nb, int32_t topk, const SelectOpts &o,
+                                    int32_t *idx, int32_t *status, cudaStream_t st) {
+    if (d == 64) return launch_d<64>(q, kbar, bh, n, nb, topk, o, idx, status, st);
+    return launch_d<128>(q, kbar, bh, n, nb, topk, o, idx, status, st);
 }
 
 }  // namespace bsa

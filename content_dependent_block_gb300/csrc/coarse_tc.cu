@@ -116,11 +116,13 @@ __device__ __forceinline__ void merge_sorted(uint32_t (&L)[KMAX], const uint32_t
         }
 }
 
-template <int D, int KMAX>
+// kOpts: the selection options of `o` are in use (a separate instance, so
+// that the plain kernel carries none of their code).
+template <int D, int KMAX, bool kOpts>
 __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_hi,
     const __grid_constant__ CUtensorMap tm_lo, int64_t n, int64_t nb, int32_t topk,
-    uint32_t key_mask, int32_t *__restrict__ idx, int32_t *status) {
+    uint32_t key_mask, const SelectOpts o, int32_t *__restrict__ idx, int32_t *status) {
     using S = CoarseSmem<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = tc::align_smem_1024(smem_raw);
@@ -239,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
         const int eg = (warp - 2) >> 2;            // column group
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int r = quad * 32 + lane;            // row inside the tile
+        const int64_t own = kOpts ? (row0 + r) / o.kb : 0;   // the query's own block
         uint32_t L[KMAX];
 #pragma unroll
         for (int t = 0; t < KMAX; ++t) L[t] = 0u;  // 0 = empty (below every real key)
@@ -251,11 +254,16 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
                 const int valid = int(i64min(kChunk, nb - int64_t(c) * kChunk));
                 for (int j = eg; j < kChunk / 32; j += kGroups) {
                     if (j * 32 >= valid) break;
+                    const uint32_t col0 = uint32_t(c * kChunk + j * 32);
+                    int lim = valid - j * 32;
+                    if (kOpts && o.causal) {
+                        // eligible blocks b <= own; skip 32 columns no row of the warp may take
+                        lim = int(i64min(lim, i64max(0, own - int64_t(col0) + 1)));
+                        if (__all_sync(0xffffffffu, lim == 0)) continue;
+                    }
                     uint32_t v[32];
                     tc::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kChunk + j * 32), v);
                     tc::tmem_ld_wait();
-                    const uint32_t col0 = uint32_t(c * kChunk + j * 32);
-                    const int lim = valid - j * 32;
 #pragma unroll 1
                     for (int hf = 0; hf < 2; ++hf) {
                         // 16 keys: sort them, merge them into the running top-k
@@ -289,10 +297,16 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
             for (int t = 0; t < KMAX; ++t) B[t] = merge[t * kTileM + r];
             merge_sorted<KMAX, KMAX>(L, B);
             int ids[KMAX];
-            const int kk = int(i64min(topk, nb));
 #pragma unroll
             for (int t = 0; t < KMAX; ++t)
-                ids[t] = (t < kk && L[t] != 0u) ? int(key_mask - (L[t] & key_mask)) : INT_MAX;
+                ids[t] = L[t] != 0u ? int(key_mask - (L[t] & key_mask)) : INT_MAX;
+            int kr = topk;
+            if (kOpts && o.head_k != nullptr) {
+                const int32_t hk = __ldg(o.head_k + h);
+                kr = min(max(hk, 0), topk);
+                if (hk != kr) report_status(status, kStatusInvalidArg);
+            }
+            apply_budget<KMAX>(ids, kr, int(own), kOpts && o.local != 0);
 #pragma unroll
             for (int round = 0; round < KMAX; ++round) {
 #pragma unroll
@@ -346,25 +360,26 @@ bool make_map(CUtensorMap *m, const void *base, int64_t outer, int64_t rows, int
 
 template <int D, int KMAX>
 cudaError_t launch_dk(const CUtensorMap &mq, const CUtensorMap &mh, const CUtensorMap &ml,
-                      int64_t bh, int64_t n, int64_t nb, int32_t topk, uint32_t mask, int32_t *idx,
-                      int32_t *status, cudaStream_t st) {
+                      int64_t bh, int64_t n, int64_t nb, int32_t topk, uint32_t mask,
+                      const SelectOpts &o, int32_t *idx, int32_t *status, cudaStream_t st) {
     const int smem = CoarseSmem<D>::kTotal;
-    auto kern = coarse_topk_tc_kernel<D, KMAX>;
+    const bool opts = o.head_k != nullptr || o.causal || o.local;
+    auto kern = opts ? coarse_topk_tc_kernel<D, KMAX, true> : coarse_topk_tc_kernel<D, KMAX, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid(unsigned((n + kTileM - 1) / kTileM), unsigned(bh));
-    kern<<<grid, kThreads, smem, st>>>(mq, mh, ml, n, nb, topk, mask, idx, status);
+    kern<<<grid, kThreads, smem, st>>>(mq, mh, ml, n, nb, topk, mask, o, idx, status);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_d(const CUtensorMap &mq, const CUtensorMap &mh, const CUtensorMap &ml,
-                     int64_t bh, int64_t n, int64_t nb, int32_t topk, uint32_t mask, int32_t *idx,
-                     int32_t *status, cudaStream_t st) {
-    if (topk <= 4) return launch_dk<D, 4>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
-    if (topk <= 8) return launch_dk<D, 8>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
-    if (topk <= 16) return launch_dk<D, 16>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
-    return launch_dk<D, 32>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+                     int64_t bh, int64_t n, int64_t nb, int32_t topk, uint32_t mask,
+                     const SelectOpts &o, int32_t *idx, int32_t *status, cudaStream_t st) {
+    if (topk <= 4) return launch_dk<D, 4>(mq, mh, ml, bh, n, nb, topk, mask, o, idx, status, st);
+    if (topk <= 8) return launch_dk<D, 8>(mq, mh, ml, bh, n, nb, topk, mask, o, idx, status, st);
+    if (topk <= 16) return launch_dk<D, 16>(mq, mh, ml, bh, n, nb, topk, mask, o, idx, status, st);
+    return launch_dk<D, 32>(mq, mh, ml, bh, n, nb, topk, mask, o, idx, status, st);
 }
 
 }  // namespace
@@ -379,14 +394,15 @@ bool coarse_tc_supported(int64_t nb) { return coarse_tc_key_bits(nb) <= 12; }
 
 cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const uint16_t *kbar_lo,
                                   int64_t bh, int64_t n, int32_t d, int64_t nb, int32_t topk,
-                                  int32_t *idx, int32_t *status, cudaStream_t st) {
+                                  const SelectOpts &o, int32_t *idx, int32_t *status,
+                                  cudaStream_t st) {
     CUtensorMap mq, mh, ml;
     if (!make_map(&mq, q, bh, n, d, kTileM) || !make_map(&mh, kbar_hi, bh, nb, d, kChunk) ||
         !make_map(&ml, kbar_lo, bh, nb, d, kChunk))
         return cudaErrorInvalidValue;
     const uint32_t mask = (1u << coarse_tc_key_bits(nb)) - 1u;
-    if (d == 64) return launch_d<64>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
-    return launch_d<128>(mq, mh, ml, bh, n, nb, topk, mask, idx, status, st);
+    if (d == 64) return launch_d<64>(mq, mh, ml, bh, n, nb, topk, mask, o, idx, status, st);
+    return launch_d<128>(mq, mh, ml, bh, n, nb, topk, mask, o, idx, status, st);
 }
 
 }  // namespace bsa

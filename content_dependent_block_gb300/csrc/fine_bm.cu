@@ -79,15 +79,16 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // Per-tile constants, computed once by the gather group: keys in the block
 // (kv < 64 only for a ragged last block), flat row of the range's first
-// query (qbase) and the range's offset in the partial-state ring (roff).
+// query (qbase), the range's offset in the partial-state ring (roff), the
+// range's first query index (ibase) and the block's first key (j0).
 struct TileInfo {
-    int32_t bin, p0, count, item, last, rg, end, kv, qbase, roff, pad0, pad1;
+    int32_t bin, p0, count, item, last, rg, end, kv, qbase, roff, ibase, j0;
 };
 
 // A fine item staged by the prefetcher: descriptor plus all its pair ids
 // ((flat query row << 5) | slot).
 struct StagedItem {
-    int32_t bin, first, end, rg, h, b, valid, kv, qbase, roff, pad0, pad1;
+    int32_t bin, first, end, rg, h, b, valid, kv, qbase, roff, ibase, j0;
     int32_t pid[kItemMax];
 };
 
@@ -184,8 +185,10 @@ __device__ __forceinline__ float ex2(float x) {
 // by shuffles.  Neighbouring queries read their two chunks in opposite
 // order, so that a quarter warp touches all 32 banks once.  The slot loop
 // is rolled (four slots per trip) to keep the code small.  Returns false
-// when nothing is listed; else acc holds the merged channels.
-template <int D>
+// when nothing is listed; else acc holds the merged channels.  kOpts: a
+// listed slot may hold a partial that admitted no key (lse = -inf, under the
+// causal mask); it weighs 0.
+template <int D, bool kOpts>
 __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pl, uint32_t vm, int k,
                                             int lane, float (&acc)[16]) {
     constexpr int LPQ = D / 16;
@@ -206,7 +209,9 @@ __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pl,
 #pragma unroll
     for (int t = 0; t < SPL; ++t) {
         const int s = gl + LPQ * t;
-        w[t] = ((vm >> s) & 1u) ? ex2(w[t] - M) : 0.f;
+        // unlisted slots hold -inf, and so does a partial that admitted no key
+        const bool use = kOpts ? w[t] > -INFINITY : ((vm >> s) & 1u) != 0;
+        w[t] = use ? ex2(w[t] - M) : 0.f;
         L += w[t];
     }
 #pragma unroll
@@ -253,7 +258,10 @@ __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pl,
     return true;
 }
 
-template <int D>
+// kOpts: the causal key limit (a.causal) and selection-derived slot masks
+// (a.sel_lists) may be in use; a separate instance, so that the plain kernel
+// carries none of their code.
+template <int D, bool kOpts>
 __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const FineBmArgs a) {
@@ -355,6 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     si->kv = int32_t(i64min(kB, n - b * kB));
                     si->qbase = int32_t(h * n + rr * range);
                     si->roff = int32_t((rg % kPartialRing) * ring_stride);
+                    si->ibase = int32_t(rr * range);
+                    si->j0 = int32_t(b * kB);
                 }
             }
             if (lane == 0) si->valid = valid ? 1 : 0;
@@ -398,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (!si->valid) break;
             const int32_t first = si->first, end = si->end, bin = si->bin, rg = si->rg;
             const int32_t kv = si->kv, qbase = si->qbase, roff = si->roff;
+            const int32_t ibase = si->ibase, j0 = si->j0;
             if (gw == 0) {
                 if (rg >= kPartialRing) {
                     // the ring entry must have been merged by its previous range
@@ -474,7 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     x.kv = kv;
                     x.qbase = qbase;
                     x.roff = roff;
-                    x.pad0 = x.pad1 = 0;
+                    x.ibase = ibase;
+                    x.j0 = j0;
                     ti[slot] = x;
                 }
                 tc::mbar_arrive(bars + C::bTiFull + slot);
@@ -606,7 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
             const int32_t end_flag = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
             if (end_flag) break;
-            const int keys_valid = reinterpret_cast<volatile TileInfo *>(ti + slot)->kv;   // < 64: ragged
+            int keys_valid = reinterpret_cast<volatile TileInfo *>(ti + slot)->kv;   // < 64: ragged
+            if (kOpts && a.causal && row < reinterpret_cast<volatile TileInfo *>(ti + slot)->count) {
+                // causal: query i admits the keys j <= i of the block
+                const volatile TileInfo *x = ti + slot;
+                const int32_t i = (pids[slot * kTile + row] >> 5) - x->qbase + x->ibase;
+                keys_valid = min(keys_valid, i - x->j0 + 1);   // <= 0: nothing admitted
+            }
             if (!tc::mbar_wait(bars + C::bSFull + j, (g >> 1) & 1, status)) break;
             tc::tc_fence_after();
             float mraw = -INFINITY;
@@ -770,6 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (!__shfl_sync(kFull, got, 0)) break;
             const int64_t h = rg / nranges, rr = rg % nranges;
             const int64_t i_begin = rr * range + item.y;
+            // lists from the selection: the valid slots follow from the budget
+            const int kr_h = kOpts && a.head_k != nullptr ? min(max(__ldg(a.head_k + h), 0), k) : k;
             const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
             const int nq = int(i_end - i_begin);
             const int nch = (nq + qs - 1) / qs;
@@ -800,7 +820,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     const bool act = jq < qn;
                     const int64_t qrow = h * n + i_begin + q0 + (act ? jq : 0);
                     uint32_t vm = act ? full_mask : 0u;
-                    if (full_valid == 0) {
+                    if (kOpts && full_valid == 0 && a.sel_lists) {
+                        // the first min(k_h, eligible) slots hold ids
+                        const int64_t i = i_begin + q0 + jq;
+                        const int cnt = int(i64min(i64min(kr_h, nb), a.causal ? i / kB + 1 : nb));
+                        vm = act ? (cnt >= 32 ? kFull : (1u << cnt) - 1u) : 0u;
+                    } else if (full_valid == 0) {
                         // lists with padding: a slot counts only if its id is a block
                         vm = 0u;
                         for (int s = gl; act && s < k; s += LPQ) {
@@ -813,7 +838,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     float acc[16];
                     const uint16_t *po = reinterpret_cast<const uint16_t *>(st) + jq * kpad * D + gl * 16;
                     const float *pl = reinterpret_cast<const float *>(st + o_cap) + jq * kpad;
-                    if (merge_query<D>(po, pl, vm, k, lane, acc)) {   // nothing listed: O stays 0
+                    // every lane takes part (the merge shuffles across the warp); a
+                    // query with nothing listed was zeroed by the inversion, one
+                    // whose listed blocks admit nothing (causal mask) is zeroed here
+                    const bool any = merge_query<D, kOpts>(po, pl, vm, k, lane, acc);
+                    if (act && (any || kOpts)) {
+                        if (!any) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+                        }
                         uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow * D + gl * 16);
                         dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                                             pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
@@ -863,11 +896,11 @@ bool make_rows_map(CUtensorMap *m, const void *base, int64_t bh, int64_t n, int 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kOpts>
 cudaError_t launch_d(const FineBmArgs &a, const CUtensorMap &mk, const CUtensorMap &mv,
                      cudaStream_t st) {
     using C = Cfg<D>;
-    auto kern = fine_ws_kernel<D>;
+    auto kern = fine_ws_kernel<D, kOpts>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
@@ -888,8 +921,9 @@ cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st) {
     CUtensorMap mk, mv;
     if (!make_rows_map(&mk, a.k_ptr, a.bh, a.n, a.d, kB) || !make_rows_map(&mv, a.v_ptr, a.bh, a.n, a.d, kB))
         return cudaErrorInvalidValue;
-    if (a.d == 64) return launch_d<64>(a, mk, mv, st);
-    return launch_d<128>(a, mk, mv, st);
+    if (a.causal || a.sel_lists)
+        return a.d == 64 ? launch_d<64, true>(a, mk, mv, st) : launch_d<128, true>(a, mk, mv, st);
+    return a.d == 64 ? launch_d<64, false>(a, mk, mv, st) : launch_d<128, false>(a, mk, mv, st);
 }
 
 }  // namespace bsa

@@ -100,6 +100,7 @@ __device__ __forceinline__ bool block_full(const FineArgs &a, int64_t i0, int64_
     if (j0 + kB > a.n) return false;                     // ragged last block: mask the tail
     if (a.mask_kind == 0) return true;
     if (a.mask_kind == 2) return j1 <= i0 && j0 > i1 - a.sliding;
+    if (a.mask_kind == 3) return j1 <= i0;
     // local + global: every pair within the window
     return a.window >= 0 && i1 - j0 <= a.window && j1 - i0 <= a.window;
 }
@@ -114,12 +115,13 @@ __device__ __forceinline__ uint32_t bits_between(int64_t lo, int64_t hi) {
 
 // Bit c set iff key jc + c (c < 32) lies in the sequence and the predicate
 // admits it for query i: the same sets as mask_admits, built once per 32 keys
-// from the ranges they form (|i - j| <= w and i - W < j <= i are intervals of
-// j; j mod s == 0 is every s-th column).
+// from the ranges they form (|i - j| <= w, i - W < j <= i and j <= i are
+// intervals of j; j mod s == 0 is every s-th column).
 __device__ __forceinline__ uint32_t admitted_bits(const FineArgs &a, int64_t i, int64_t jc) {
     const uint32_t inside = bits_between(0, a.n - jc);
     const int64_t d0 = i - jc;                           // key jc + c has i - j = d0 - c
     if (a.mask_kind == 2) return inside & bits_between(d0 - a.sliding + 1, d0 + 1);
+    if (a.mask_kind == 3) return inside & bits_between(0, d0 + 1);
     if (a.mask_kind != 1) return inside;
     uint32_t m = a.window >= 0 ? bits_between(d0 - a.window, d0 + int64_t(a.window) + 1) : 0u;
     if (a.stride > 0) {

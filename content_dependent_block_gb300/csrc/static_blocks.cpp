@@ -9,6 +9,8 @@
 //                 is within w of some query of the tile;
 //   global stride the key blocks that contain a multiple of s (below n);
 //   sliding       keys within [i0 - W + 1, i1] (causal, W keys incl. self);
+//   causal        keys within [0, i1] (page "Block-Sparse & Linear
+//                 Attention Kernels", section 1, the lower triangle);
 // intersected with [0, n).  A block is listed iff the pattern admits at
 // least one (query, key) pair inside the tile x block rectangle.
 #include <algorithm>
@@ -22,7 +24,7 @@ namespace {
 bool valid_args(int64_t n, int32_t q_group, int32_t key_block, const bsa_mask &m) {
     if (n < 1 || q_group < 1 || key_block < 1) return false;
     if (m.kind == BSA_MASK_SLIDING) return m.sliding >= 1;
-    if (m.kind == BSA_MASK_LOCAL_GLOBAL) return true;
+    if (m.kind == BSA_MASK_LOCAL_GLOBAL || m.kind == BSA_MASK_CAUSAL) return true;
     return m.kind == BSA_MASK_NONE;
 }
 
@@ -51,6 +53,9 @@ void for_each_block(int64_t n, int32_t q_group, int32_t key_block, const bsa_mas
     int64_t lo_key = 0, hi_key = -1;   // empty band by default
     if (m.kind == BSA_MASK_SLIDING) {
         lo_key = std::max<int64_t>(0, i0 - int64_t(m.sliding) + 1);
+        hi_key = i1;
+    } else if (m.kind == BSA_MASK_CAUSAL) {
+        lo_key = 0;
         hi_key = i1;
     } else if (m.window >= 0) {
         lo_key = std::max<int64_t>(0, i0 - m.window);
@@ -82,6 +87,7 @@ void for_each_block(int64_t n, int32_t q_group, int32_t key_block, const bsa_mas
 int64_t count_pairs(int64_t n, const bsa_mask &m) {
     int64_t total = 0;
     if (m.kind == BSA_MASK_NONE) return n * n;
+    if (m.kind == BSA_MASK_CAUSAL) return n * (n + 1) / 2;
     if (m.kind == BSA_MASK_SLIDING) {
         for (int64_t i = 0; i < n; ++i) total += std::min<int64_t>(i + 1, m.sliding);
         return total;

@@ -68,15 +68,19 @@ typedef struct {
 typedef enum {
     BSA_MASK_NONE = 0,          /* every token of a listed block is attended   */
     BSA_MASK_LOCAL_GLOBAL = 1,  /* |i-j| <= window  or  j % stride == 0        */
-    BSA_MASK_SLIDING = 2        /* causal window: i - sliding < j <= i         */
+    BSA_MASK_SLIDING = 2,       /* causal window: i - sliding < j <= i         */
+    BSA_MASK_CAUSAL = 3         /* causal: j <= i                              */
 } bsa_mask_kind;
 
 /*
  * Token-level predicate applied inside the listed blocks (page
  * "yayme/CUDA-kernel" README, sparsity pattern; page "Block-Sparse & Linear
- * Attention Kernels", section 2, sliding window).  LOCAL_GLOBAL: window < 0
- * disables the band, stride <= 0 disables the global columns.  SLIDING:
- * sliding >= 1 is W, the number of keys up to and including the query.
+ * Attention Kernels", section 2, sliding window, and section 1, the causal
+ * lower triangle).  LOCAL_GLOBAL: window < 0 disables the band, stride <= 0
+ * disables the global columns.  SLIDING: sliding >= 1 is W, the number of
+ * keys up to and including the query.  CAUSAL takes no parameter; with
+ * per-query lists (q_group = 1) it is what a causal selection needs inside
+ * the query's own block.
  */
 typedef struct {
     int32_t kind;
@@ -132,6 +136,37 @@ bsa_status bsa_coarse_topk(bsa_shape shape, const void *q, const float *kbar,
                            void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Options of the selection (NULL = none, which is bsa_coarse_topk).
+ *   head_topk    optional DEVICE int32 [bh]: the budget k_h of each
+ *                (batch * head) row, in [0, topk] (page
+ *                "sparse-attention-triton-bench", What's next: per-head
+ *                sparsity budgets chosen at run time on the per-head stage-1
+ *                scores).  Row h of idx then holds min(k_h, eligible) ids and
+ *                -1 after them.  A value outside [0, topk] is clamped into it
+ *                and reported as BSA_ERR_INVALID_ARG through
+ *                bsa_get_device_status().  NULL: topk for every row.
+ *   causal       nonzero: query i may select only blocks b <= i / key_block
+ *                (blocks holding some key j <= i; page "Block-Sparse &
+ *                Linear Attention Kernels", section 1, the causal pattern),
+ *                and the fine stage of bsa_forward_ex attends only keys
+ *                j <= i.
+ *   local_block  nonzero: the query's own block i / key_block is always
+ *                selected (when its budget is >= 1); the other k_h - 1 are
+ *                the best-scoring eligible blocks except it.
+ * Ties and output order as bsa_coarse_topk.
+ */
+typedef struct {
+    const int32_t *head_topk;
+    int32_t causal;
+    int32_t local_block;
+} bsa_select;
+
+bsa_status bsa_coarse_topk_ex(bsa_shape shape, const void *q, const float *kbar,
+                              int32_t key_block, int32_t topk,
+                              const bsa_select *sel, int32_t *idx, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/*
  * Stage 2, fine attention over a block list (page
  * "sparse-attention-triton-bench", Stage 2 and "The Triton kernel": dense
  * softmax attention over the listed blocks' tokens with an online-softmax
@@ -159,7 +194,8 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k,
 /*
  * The whole dynamic forward: pool -> score + top-k -> fine attention, all
  * enqueued on `stream` (page "sparse-attention-triton-bench", Two-stage
- * block indexer).  bf16 only, non-causal.
+ * block indexer).  bf16 only, non-causal (bsa_forward_ex below takes the causal and
+ * per-head options).
  *   idx_out  optional [bh][n][topk] int32 (device) receiving the selection;
  *            NULL keeps it in the workspace.
  *   ws       device workspace of bsa_forward_workspace_size() bytes.
@@ -170,6 +206,18 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k,
                        const void *v, int32_t key_block, int32_t topk,
                        float scale, void *out, int32_t *idx_out, void *ws,
                        size_t ws_bytes, void *stream);
+
+/*
+ * bsa_forward with selection options (bsa_select above; NULL = none).  With
+ * `causal` the fine stage attends, for query i, only the keys j <= i of its
+ * selected blocks.  Same workspace as bsa_forward (its size does not depend
+ * on the options); same errors.
+ */
+bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k,
+                          const void *v, int32_t key_block, int32_t topk,
+                          const bsa_select *sel, float scale, void *out,
+                          int32_t *idx_out, void *ws, size_t ws_bytes,
+                          void *stream);
 
 /*
  * bsa_forward without a workspace argument, for callers that must not

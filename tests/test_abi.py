@@ -93,6 +93,22 @@ def test_pool_and_coarse_reject_fp32(L):
     s = _shape(dtype=bsa.FP32)
     assert L.bsa_pool_blocks(s, FAKE, 64, FAKE, None) == 2
     assert L.bsa_coarse_topk(s, FAKE, FAKE, 64, 4, FAKE, None, 0, None) == 2
+    assert L.bsa_coarse_topk_ex(s, FAKE, FAKE, 64, 4, None, FAKE, None, 0, None) == 2
+
+
+def test_select_options_are_checked(L):
+    s = _shape()
+    bad = bsa.Select(0x10002, 1, 0)                   # head_topk not 4-byte aligned
+    need = L.bsa_coarse_topk_workspace_size(s, 64, 4)
+    assert L.bsa_coarse_topk_ex(s, FAKE, FAKE, 64, 4, ctypes.byref(bad), FAKE, FAKE, need,
+                                None) == 7
+    need = L.bsa_forward_workspace_size(s, 64, 4)
+    assert L.bsa_forward_ex(s, FAKE, FAKE, FAKE, 64, 4, ctypes.byref(bad), 0.0, FAKE, None, FAKE,
+                            need, None) == 7
+    assert L.bsa_forward_ex(s, FAKE, FAKE, FAKE, 64, 33, None, 0.0, FAKE, None, FAKE, need,
+                            None) == 2
+    # the workspace does not depend on the options
+    assert L.bsa_forward_workspace_size(s, 64, 4) == need
 
 
 def test_static_blocks_rejects_bad_arguments(L):

@@ -31,6 +31,8 @@ CASES = [
     (1500, 128, 64, oracle.MASK_SLIDING, -1, 0, 256),
     (1500, 64, 64, oracle.MASK_SLIDING, -1, 0, 100),
     (300, 16, 16, oracle.MASK_SLIDING, -1, 0, 1),
+    (1000, 128, 64, oracle.MASK_CAUSAL, -1, 0, 0),
+    (333, 16, 32, oracle.MASK_CAUSAL, -1, 0, 0),
 ]
 
 
