@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import ctypes
 import hashlib
 import io
 import json
@@ -192,35 +193,88 @@ def kernel_traffic(kernel: str):
 
 
 # ------------------------------------------------------------ CPU oracle
+def select_args(w, device):
+    """Selection-option keyword arguments of bsa.Forward for workload w."""
+    import torch
+    hk = torch.tensor(w.head_topk, dtype=torch.int32, device=device) if w.head_topk else None
+    return dict(head_topk=hk, causal=w.causal, local_block=w.local_block)
+
+
+def eligible_scores(w) -> int:
+    """Coarse scores the selection needs: every block, or b <= i // B (causal)."""
+    import numpy as np
+    if not w.causal:
+        return w.bh * w.n * w.nb
+    return w.bh * int((np.arange(w.n) // w.key_block + 1).sum())
+
+
+def admitted_pairs(idx, w, rows=None) -> int:
+    """(query, key) pairs a selection admits: the valid keys of each listed
+    block, only keys j <= i when causal.  idx is a torch tensor [bh, n, k] or
+    a numpy array [len(rows), k] of the flat rows `rows`."""
+    import numpy as np
+    if rows is None:
+        import torch
+        b = idx.long()
+        i = torch.arange(w.n, device=idx.device).view(1, w.n, 1)
+        start = b * w.key_block
+        keys = torch.clamp(w.n - start, max=w.key_block)
+        if w.causal:
+            keys = torch.minimum(keys, i - start + 1)
+        return int((keys.clamp(min=0) * (b >= 0)).sum())
+    b = idx.astype(np.int64)
+    i = (rows % w.n)[:, None]
+    start = b * w.key_block
+    keys = np.minimum(w.n - start, w.key_block)
+    if w.causal:
+        keys = np.minimum(keys, i - start + 1)
+    return int((np.clip(keys, 0, None) * (b >= 0)).sum())
+
+
+def oracle_step(orc, w, t, rows):
+    """The oracle's whole dynamic path for `rows`; returns its FLOPs."""
+    import numpy as np
+    kbar = orc.pool(t.k, w.key_block)
+    s = orc.scores(t.q, kbar, rows)
+    if w.has_options:
+        hk = np.array(w.head_topk, dtype=np.int32) if w.head_topk else None
+        idx = orc.select(s, rows, w.n, w.key_block, w.topk, head_k=hk, causal=w.causal,
+                         local=w.local_block)
+    else:
+        idx, _ = orc.topk(s, w.topk)
+    orc.fine(t.q, t.k, t.v, w.key_block, idx, rows, causal=w.causal)
+    if not w.has_options:
+        return rows.size * metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk) / (w.n * w.bh)
+    return (metrics.pairs_flops(admitted_pairs(idx, w, rows), w.d)
+            + 2 * w.d * rows.size * eligible_scores(w) / (w.bh * w.n))
+
+
 def oracle_sample(w, t, seconds: float):
     """Time the oracle's whole dynamic path on a row sample; returns
     (TFLOP/s, rows, seconds, cores, description)."""
     import numpy as np
     import oracle
     cores = oracle.num_threads()
-    per_row = metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk) / (w.n * w.bh)
 
     def run(nrows):
         rows = workloads.sample_rows(w.bh, w.n, max(1, nrows // w.bh), seed=7)
         t0 = time.perf_counter()
-        kbar = oracle.pool(t.k, w.key_block)
-        s = oracle.scores(t.q, kbar, rows)
-        idx, _ = oracle.topk(s, w.topk)
-        oracle.fine(t.q, t.k, t.v, w.key_block, idx, rows)
-        return rows.size, time.perf_counter() - t0
+        fl = oracle_step(oracle, w, t, rows)
+        return rows.size, time.perf_counter() - t0, fl
 
-    r0, t0 = run(256 * w.bh)
+    r0, t0, _ = run(256 * w.bh)
     # bounded: at most 32768 rows per pass (the oracle keeps every row's
     # scores); passes repeat until about `seconds` of CPU time is spent
     nrows = int(min(w.bh * w.n, 32768, max(r0, r0 * seconds / max(t0, 1e-3))))
-    r1 = t1 = 0
+    r1 = t1 = f1 = 0
     passes = 0
     while passes == 0 or (t1 < seconds and passes < 64):
-        r, dt = run(nrows)
+        r, dt, fl = run(nrows)
         r1 += r
         t1 += dt
+        f1 += fl
         passes += 1
-    tflops = r1 * per_row / t1 / 1e12
+    tflops = f1 / t1 / 1e12
     desc = (f"{r1 // passes} of {w.bh * w.n} query rows (seeded sample) x {passes} passes, "
             f"full pool + scores + top-k + fine per row, fp64, {cores} threads")
     return tflops, r1 // passes, t1, cores, desc
@@ -233,22 +287,20 @@ def reference_arm(args, rank, world, w):
     import oracle  # noqa: F401
     t = workloads.generate(w)
     cores = None
-    per_row = metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk) / (w.n * w.bh)
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
     _, rows, secs, cores, desc = oracle_sample(w, t, budget)
     import oracle as orc
     times = []
     rws = workloads.sample_rows(w.bh, w.n, max(1, rows // w.bh), seed=7)
+    flops = 0.0
     for it in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        kbar = orc.pool(t.k, w.key_block)
-        s = orc.scores(t.q, kbar, rws)
-        idx, _ = orc.topk(s, w.topk)
-        orc.fine(t.q, t.k, t.v, w.key_block, idx, rws)
+        fl = oracle_step(orc, w, t, rws)
         if it >= args.warmup:
             times.append(time.perf_counter() - t0)
+            flops += fl
     total = sum(times)
-    value = rws.size * per_row * len(times) / total / 1e12
+    value = flops / total / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -289,10 +341,15 @@ def profile_static(args, w, device, dist):
 
 
 def config_of(w):
-    return {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "key_block": w.key_block,
-            "topk": w.topk, "dtype": w.dtype, "inputs": w.note,
-            "l2": "flushed before every timed step (256 MiB write)",
-            "parallelism": "independent problem per rank (weak)"}
+    c = {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "key_block": w.key_block,
+         "topk": w.topk, "dtype": w.dtype, "inputs": w.note,
+         "l2": "flushed before every timed step (256 MiB write)",
+         "parallelism": "independent problem per rank (weak)"}
+    if w.has_options:
+        c["select"] = {"causal": w.causal, "local_block": w.local_block,
+                       "head_topk": list(w.head_topk) or None}
+        c["flops"] = "counted from the selection: admitted (query, key) pairs x (4d+5) + eligible scores x 2d"
+    return c
 
 
 # ------------------------------------------------------------- GPU arm
@@ -323,7 +380,7 @@ def main(argv=None):
     mem0 = torch.cuda.memory_allocated(device)
     q, k, v = (torch.from_numpy(getattr(t, x).view("int16")).view(torch.bfloat16).to(device)
                for x in "qkv")
-    fwd = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk, device=device)
+    fwd = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk, device=device, **select_args(w, device))
     fwd(q, k, v)
     torch.cuda.synchronize(device)
     if args.profile_forwards > 0:
@@ -340,6 +397,11 @@ def main(argv=None):
 
     flops = metrics.sparse_flops(w.n, w.bh, w.d, w.key_block, w.topk)
     fine_flops = metrics.pairs_flops(w.n * w.bh * min(w.topk, w.nb) * w.key_block, w.d)
+    if w.has_options:
+        # the selection decides the work: count it from the first forward's lists
+        pairs, elig = admitted_pairs(fwd.idx, w), eligible_scores(w)
+        fine_flops = metrics.pairs_flops(pairs, w.d)
+        flops = fine_flops + 2 * w.d * elig
 
     def flush_l2():
         flush.fill_(1)
@@ -385,12 +447,14 @@ def main(argv=None):
         def pool():
             bsa._check(L.bsa_pool_blocks(shp, P(k), w.key_block, P(kbar), S()))
 
+        sel = None if fwd.sel is None else ctypes.byref(fwd.sel)
+
         def coarse():
-            bsa._check(L.bsa_coarse_topk(shp, P(q), P(kbar), w.key_block, w.topk, P(idx),
-                                         P(ws_cb), ws_c, S()))
+            bsa._check(L.bsa_coarse_topk_ex(shp, P(q), P(kbar), w.key_block, w.topk, sel, P(idx),
+                                            P(ws_cb), ws_c, S()))
 
         ld = bsa.ListDesc(1, w.key_block, w.topk, 1)
-        msk = bsa.mask_struct()
+        msk = bsa.mask_struct(bsa.MASK_CAUSAL) if w.causal else bsa.mask_struct()
         ws_f = L.bsa_fine_attention_workspace_size(shp, ld, msk)
         ws_fb = bsa._workspace(ws_f, device)
 
@@ -461,6 +525,8 @@ def main(argv=None):
     # compulsory bytes at the measured HBM bandwidth.  The FP32 peak is derived
     # from unit counts and clocks: SMs x 128 FP32 lanes x 2 FLOP x max clock.
     f_mma, f_alu = metrics.sparse_flops_split(w.n, w.bh, w.d, w.key_block, w.topk)
+    if w.has_options:
+        f_mma, f_alu = 4 * w.d * pairs + 2 * w.d * elig, 5 * pairs
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     p_fp32 = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
     bytes_fwd = metrics.unique_bytes(w.n, w.bh, w.d, 2)

@@ -43,6 +43,15 @@ class Workload:
     q_group: int = 1        # queries per list row (static lists)
     seed: int = 0
     note: str = ""
+    # selection options (dynamic only): causal selection, the query's own
+    # block always selected, per-(batch*head) budgets (empty: topk for all)
+    causal: bool = False
+    local_block: bool = False
+    head_topk: tuple = ()
+
+    @property
+    def has_options(self) -> bool:
+        return self.causal or self.local_block or bool(self.head_topk)
 
     @property
     def nb(self) -> int:
@@ -71,6 +80,15 @@ WORKLOADS = {
         "dyn_n32768", bh=8, n=32768, d=64, dtype="bf16", kind="dynamic",
         key_block=64, topk=16, centre_sigma=0.5,
         note="planted centres, 512 blocks, top-16 (1024 tokens/query)"),
+    "dyn_n32768_causal": Workload(
+        "dyn_n32768_causal", bh=8, n=32768, d=64, dtype="bf16", kind="dynamic",
+        key_block=64, topk=16, centre_sigma=0.5, causal=True, local_block=True,
+        note="as dyn_n32768; causal selection (blocks b <= i/64, keys j <= i), "
+             "own block always selected"),
+    "dyn_n32768_budgets": Workload(
+        "dyn_n32768_budgets", bh=8, n=32768, d=64, dtype="bf16", kind="dynamic",
+        key_block=64, topk=16, centre_sigma=0.5, head_topk=(16, 12, 8, 4, 16, 12, 8, 4),
+        note="as dyn_n32768; per-head budgets 16/12/8/4 (twice)"),
     "dyn_n131072": Workload(
         "dyn_n131072", bh=8, n=131072, d=128, dtype="bf16", kind="dynamic",
         key_block=64, topk=32, centre_sigma=0.5,
