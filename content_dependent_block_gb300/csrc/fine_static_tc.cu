@@ -8,27 +8,31 @@
 // block.
 //
 // Query-tile-major: one CTA per (head, 128-query tile).  The list is shared
-// by the tile, so K_b and V_b are loaded once per tile and every block is a
-// dense 128 x 64 x d contraction.  The softmax is exact and two-pass: pass 0
-// computes the row maxima over all listed blocks, pass 1 recomputes the
-// scores, forms p = exp2(s * scale * log2 e - m) once, accumulates l and
-// O += P V in tensor memory.  O is never rescaled, at the price of computing
-// Q K^T twice.  Stage-use u runs over u < nl (pass 0, block u) and
-// nl <= u < 2 nl (pass 1, block u - nl).
+// by the tile, so K_b and V_b are loaded once per tile.  Listed blocks are
+// taken two at a time ("superblocks" of 128 keys; an odd list ends with a
+// half made of keys past the sequence, loaded as zeros and masked out), so
+// that every score tile is a 128 x 128 x d contraction and every P.V one of
+// 128 keys: an N = 64 MMA costs nearly as long as an N = 128 one.  The
+// softmax is exact and two-pass: pass 0 computes the row maxima over all
+// listed blocks, pass 1 recomputes the scores, forms p = exp2(s * scale *
+// log2 e - m) once, accumulates l and O += P V in tensor memory.  O is never
+// rescaled, at the price of computing Q K^T twice.  Stage-use u runs over
+// u < ns (pass 0, superblock u) and ns <= u < 2 ns (pass 1, superblock
+// u - ns), ns = ceil(listed / 2).
 //
 //   warp 0     producer of Q (once) and of K for every stage-use, into a
-//              ring of three
+//              ring of three 128-key stages
 //   warp 1     MMA, warp-uniform loop, one elected lane issues:
-//              S_u = Q K^T (M 128, N 64) into TMEM buffer u mod 6; the P.V
-//              of a pass-1 block (N = d, V MN-major) four stage-uses later,
-//              so the next scores are ready while the groups still work
-//   warp 2     producer of V for every pass-1 block, into a ring of four
-//              (one per P buffer), so K loads never wait on a P.V
-//   warps 3-18 four softmax warpgroups; group g takes the stage-uses
-//              u = g mod 4, one thread per query row: masked row max
-//              (pass 0), combined over the groups through shared memory;
-//              masked p, l, P (bf16) into the block's P buffer (pass 1);
-//              then O / l, 32-column chunks dealt round-robin to the groups
+//              S_u = Q K^T (M 128, N 128) into TMEM buffer u mod 3; the P.V
+//              of a pass-1 superblock (A = P from TMEM, N = d, V MN-major)
+//              two stage-uses later
+//   warp 2     producer of V for every pass-1 superblock, into a ring of two
+//   warps 3-14 three softmax warpgroups; group g takes the stage-uses
+//              u = g mod 3 (TMEM buffer g), one thread per query row: masked
+//              row max (pass 0), combined over the groups through shared
+//              memory; masked p, l, and P (bf16) written over the scores
+//              already read (pass 1); then O / l, 32-column chunks dealt
+//              round-robin to the groups
 #include <cmath>
 
 #include <cudaTypedefs.h>
@@ -42,9 +46,10 @@ namespace {
 
 constexpr int kTile = 128;             // queries per CTA (TMEM lanes)
 constexpr int kB = 64;                 // keys per block
-constexpr int kGroups = 4;             // softmax warpgroups
-constexpr int kLag = kGroups;          // P.V of a block this many stage-uses behind its scores
-constexpr int kWarpSoftmax = 3;       // first softmax warp
+constexpr int kSB = 2 * kB;            // keys per superblock (two listed blocks)
+constexpr int kGroups = 3;             // softmax warpgroups = S buffers in TMEM
+constexpr int kLag = 2;                // P.V of a superblock this many stage-uses behind its scores
+constexpr int kWarpSoftmax = 3;        // first softmax warp
 constexpr int kThreads = 32 * kWarpSoftmax + kGroups * 128;
 constexpr int kMaxList = 512;          // listed blocks held in shared memory per chunk
 constexpr uint32_t kBarGroups = 1;     // named barrier of the softmax warpgroups
@@ -54,16 +59,15 @@ template <int D>
 struct SCfg {
     static constexpr int kSub = D / 64;
     static constexpr int kKStages = 3;                      // K ring
-    static constexpr int kRing = 4;                         // V ring = P buffers
-    static constexpr int kS = 2 * kGroups < 6 ? 2 * kGroups : 6;   // S buffers in TMEM
+    static constexpr int kVStages = 2;                      // V ring
+    static constexpr int kS = kGroups;                      // S (and P) buffers in TMEM
     static constexpr int kQBytes = kSub * kTile * 128;
-    static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
-    static constexpr int kPBytes = kTile * 128;
+    static constexpr int kPanel = kSB * 128;                // 128 keys x 64 channels
+    static constexpr int kStageBytes = kSub * kPanel;       // K or V of one superblock
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kQBytes;
-    static constexpr int oV = oK + kKStages * kKBytes;
-    static constexpr int oP = oV + kRing * kKBytes;
-    static constexpr int oList = oP + kRing * kPBytes;      // int32 [kMaxList]
+    static constexpr int oV = oK + kKStages * kStageBytes;
+    static constexpr int oList = oV + kVStages * kStageBytes;   // int32 [kMaxList]
     static constexpr int oRed = oList + kMaxList * 4;       // float [2][kGroups][kTile]
     static constexpr int oBar = oRed + 2 * kGroups * kTile * 4;
     enum {
@@ -71,22 +75,25 @@ struct SCfg {
         bKFull = 1,
         bKEmpty = bKFull + kKStages,
         bVFull = bKEmpty + kKStages,
-        bVEmpty = bVFull + kRing,
-        bSFull = bVEmpty + kRing,
-        bSFree = bSFull + kS,
-        bPFull = bSFree + kS,
-        bPFree = bPFull + kRing,
-        bOFull = bPFree + kRing,
+        bVEmpty = bVFull + kVStages,
+        bSFull = bVEmpty + kVStages,
+        bSFree = bSFull + kS,           // pass-0 scores read
+        bPFull = bSFree + kS,           // pass-1 P written over its scores
+        bPvDone = bPFull + kS,          // pass-1 P.V done: the buffer is free
+        bOFull = bPvDone + kS,
         bCount = bOFull + 1
     };
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
-    static constexpr uint32_t kTmemCols = 512;              // S[kS] from 0; O after them
-    static constexpr uint32_t cO = kS * kB;
+    static constexpr uint32_t kTmemCols = 512;              // S[3] (P in the first 64 columns) from 0; O after them
+    static constexpr uint32_t cO = kS * kSB;
 };
 static_assert(SCfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
 static_assert(SCfg<128>::cO + 128 <= SCfg<128>::kTmemCols, "tensor memory (d = 128)");
-static_assert(kGroups >= 1 && kGroups <= 4, "softmax warpgroups");
+static_assert(kLag < kGroups, "an S buffer is reused only after its P.V was issued");
+
+// Pass-0 stage-uses (u < ns) that fall on S buffer j of ks.
+__device__ __forceinline__ int pass0_uses(int ns, int j, int ks) { return (ns - j + ks - 1) / ks; }
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -223,15 +230,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             tc::mbar_init(bars + C::bKFull + s, 1);
             tc::mbar_init(bars + C::bKEmpty + s, 1);
         }
-        for (int j = 0; j < C::kRing; ++j) {
-            tc::mbar_init(bars + C::bVFull + j, 1);
-            tc::mbar_init(bars + C::bVEmpty + j, 1);
-            tc::mbar_init(bars + C::bPFull + j, kTile);     // one warpgroup per stage-use
-            tc::mbar_init(bars + C::bPFree + j, 1);
+        for (int r = 0; r < C::kVStages; ++r) {
+            tc::mbar_init(bars + C::bVFull + r, 1);
+            tc::mbar_init(bars + C::bVEmpty + r, 1);
         }
         for (int j = 0; j < C::kS; ++j) {
             tc::mbar_init(bars + C::bSFull + j, 1);
-            tc::mbar_init(bars + C::bSFree + j, kTile);
+            tc::mbar_init(bars + C::bSFree + j, kTile);     // one warpgroup per stage-use
+            tc::mbar_init(bars + C::bPFull + j, kTile);
+            tc::mbar_init(bars + C::bPvDone + j, 1);
         }
         tc::mbar_init(bars + C::bOFull, 1);
         tc::fence_barrier_init();
@@ -248,88 +255,105 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int nl = *nlist_s;
+    const int ns = (nl + 1) >> 1;                     // superblocks
+    // first key of block `blk` of the list; past the end: keys beyond the
+    // sequence (loaded as zeros, never admitted)
+    auto block_key0 = [&](int blk) -> int64_t {
+        return blk < nl ? int64_t(list_s[blk]) * kB : a.nb * kB;
+    };
 
     if (warp == 0) {
-        // ------------------------------------------------------- producer
+        // ------------------------------------------------- producer of Q, K
         if (lane == 0) {
             tc::mbar_arrive_expect_tx(bars + C::bQFull, C::kQBytes);
 #pragma unroll
             for (int sub = 0; sub < C::kSub; ++sub)
                 tc::tma_load_3d(sm + C::oQ + sub * kTile * 128, &tm_q, bars + C::bQFull, sub * 64,
                                 int32_t(i0), int32_t(h));
-            for (int u = 0; u < 2 * nl; ++u) {
-                const int jb = u >= nl ? u - nl : u, s = u % C::kKStages;
+            for (int u = 0; u < 2 * ns; ++u) {
+                const int sb = u >= ns ? u - ns : u, s = u % C::kKStages;
                 if (u >= C::kKStages &&
                     !tc::mbar_wait(bars + C::bKEmpty + s, ((u / C::kKStages) - 1) & 1, status))
                     break;
-                const int32_t key0 = list_s[jb] * kB;
-                tc::mbar_arrive_expect_tx(bars + C::bKFull + s, C::kKBytes);
+                tc::mbar_arrive_expect_tx(bars + C::bKFull + s, C::kStageBytes);
 #pragma unroll
-                for (int sub = 0; sub < C::kSub; ++sub)
-                    tc::tma_load_3d(sm + C::oK + s * C::kKBytes + sub * kB * 128, &tm_k,
-                                    bars + C::bKFull + s, sub * 64, key0, int32_t(h));
+                for (int half = 0; half < 2; ++half) {
+                    const int32_t key0 = int32_t(block_key0(2 * sb + half));
+#pragma unroll
+                    for (int sub = 0; sub < C::kSub; ++sub)
+                        tc::tma_load_3d(sm + C::oK + s * C::kStageBytes + sub * C::kPanel + half * kB * 128,
+                                        &tm_k, bars + C::bKFull + s, sub * 64, key0, int32_t(h));
+                }
             }
         }
         __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------------------ producer of V
         if (lane == 0) {
-            for (int jb = 0; jb < nl; ++jb) {
-                const int r = jb % C::kRing;
-                if (jb >= C::kRing &&
-                    !tc::mbar_wait(bars + C::bVEmpty + r, ((jb / C::kRing) - 1) & 1, status))
+            for (int sb = 0; sb < ns; ++sb) {
+                const int r = sb % C::kVStages;
+                if (sb >= C::kVStages &&
+                    !tc::mbar_wait(bars + C::bVEmpty + r, ((sb / C::kVStages) - 1) & 1, status))
                     break;
-                tc::mbar_arrive_expect_tx(bars + C::bVFull + r, C::kKBytes);
+                tc::mbar_arrive_expect_tx(bars + C::bVFull + r, C::kStageBytes);
 #pragma unroll
-                for (int sub = 0; sub < C::kSub; ++sub)
-                    tc::tma_load_3d(sm + C::oV + r * C::kKBytes + sub * kB * 128, &tm_v,
-                                    bars + C::bVFull + r, sub * 64, list_s[jb] * kB, int32_t(h));
+                for (int half = 0; half < 2; ++half) {
+                    const int32_t key0 = int32_t(block_key0(2 * sb + half));
+#pragma unroll
+                    for (int sub = 0; sub < C::kSub; ++sub)
+                        tc::tma_load_3d(sm + C::oV + r * C::kStageBytes + sub * C::kPanel + half * kB * 128,
+                                        &tm_v, bars + C::bVFull + r, sub * 64, key0, int32_t(h));
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA
-        constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
+        constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kSB);
         constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
         bool ok = __all_sync(kFull, tc::mbar_wait(bars + C::bQFull, 0, status));
         const uint32_t aq = tc::smem_u32(sm + C::oQ);
-        auto issue_pv = [&](int jb) {         // O += P_jb V_jb
-            const int r = jb % C::kRing, ph = (jb / C::kRing) & 1;
-            bool w = tc::mbar_wait(bars + C::bVFull + r, ph, status);
-            w = w && tc::mbar_wait(bars + C::bPFull + r, ph, status);
+        // O += P_sb V_sb, P (bf16) in the first 64 columns of the superblock's S buffer
+        auto issue_pv = [&](int sb) {
+            const int u = sb + ns, j = u % C::kS, r = sb % C::kVStages;
+            bool w = tc::mbar_wait(bars + C::bVFull + r, (sb / C::kVStages) & 1, status);
+            w = w && tc::mbar_wait(bars + C::bPFull + j, (u / C::kS - pass0_uses(ns, j, C::kS)) & 1,
+                                   status);
             ok = __all_sync(kFull, w);
             if (!ok) return;
             tc::tc_fence_after();
             if (tc::elect_one()) {
-                const uint32_t ap = tc::smem_u32(sm + C::oP + r * C::kPBytes);
-                const uint32_t av = tc::smem_u32(sm + C::oV + r * C::kKBytes);
+                const uint32_t av = tc::smem_u32(sm + C::oV + r * C::kStageBytes);
 #pragma unroll
-                for (int kk = 0; kk < kB / 16; ++kk)
-                    tc::mma_bf16(tmem + C::cO, tc::smem_desc_sw128(ap + kk * 32, 1024),
-                                 tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
-                                 (jb > 0 || kk > 0) ? 1u : 0u);
-                tc::mma_commit(bars + C::bPFree + r);
+                for (int kk = 0; kk < kSB / 16; ++kk)
+                    tc::mma_bf16_ts(tmem + C::cO, tmem + uint32_t(j * kSB + kk * 8),
+                                    tc::smem_desc_sw128_mn(av + kk * 2048, C::kPanel, 1024), idesc_o,
+                                    (sb > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(bars + C::bPvDone + j);
                 tc::mma_commit(bars + C::bVEmpty + r);
-                if (jb == nl - 1) tc::mma_commit(bars + C::bOFull);
+                if (sb == ns - 1) tc::mma_commit(bars + C::bOFull);
             }
             __syncwarp();
         };
-        for (int u = 0; ok && u < 2 * nl + kLag; ++u) {
-            if (u < 2 * nl) {
-                const int s = u % C::kKStages, j = u % C::kS;
+        for (int u = 0; ok && u < 2 * ns + kLag; ++u) {
+            if (u < 2 * ns) {
+                const int s = u % C::kKStages, j = u % C::kS, prev = u - C::kS;
                 bool w = tc::mbar_wait(bars + C::bKFull + s, (u / C::kKStages) & 1, status);
-                if (w && u >= C::kS)
-                    w = tc::mbar_wait(bars + C::bSFree + j, ((u / C::kS) - 1) & 1, status);
+                // the buffer's last use: pass-0 scores read, or the P.V of its P done
+                if (w && prev >= 0)
+                    w = prev < ns ? tc::mbar_wait(bars + C::bSFree + j, (prev / C::kS) & 1, status)
+                                  : tc::mbar_wait(bars + C::bPvDone + j,
+                                                  (prev / C::kS - pass0_uses(ns, j, C::kS)) & 1, status);
                 ok = __all_sync(kFull, w);
                 if (!ok) break;
                 tc::tc_fence_after();
                 if (tc::elect_one()) {
-                    const uint32_t ak = tc::smem_u32(sm + C::oK + s * C::kKBytes);
+                    const uint32_t ak = tc::smem_u32(sm + C::oK + s * C::kStageBytes);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
-                        const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
-                        tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
+                        const uint32_t off_k = uint32_t((kk >> 2) * C::kPanel + (kk & 3) * 32);
+                        tc::mma_bf16(tmem + uint32_t(j * kSB), tc::smem_desc_sw128(aq + off_q, 1024),
                                      tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
                     }
                     tc::mma_commit(bars + C::bSFull + j);
@@ -338,35 +362,38 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 __syncwarp();
             }
             // P.V kLag stage-uses behind the scores
-            if (u - kLag >= nl) issue_pv(u - kLag - nl);
+            if (u - kLag >= ns) issue_pv(u - kLag - ns);
         }
     } else {
         // ----------------------------------------- softmax and epilogue
-        const int g = (warp - kWarpSoftmax) >> 2;                 // warpgroup: stage-uses u = g mod kGroups
+        const int g = (warp - kWarpSoftmax) >> 2;      // warpgroup: stage-uses u = g mod kGroups
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int64_t i = i0 + row;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
-        // pass 0: masked row maxima of this group's blocks
-        for (int u = g; ok && u < nl; u += kGroups) {
+        // pass 0: masked row maxima of this group's superblocks
+        for (int u = g; ok && u < ns; u += kGroups) {
             const int j = u % C::kS;
             if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kS) & 1, status)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
-            const int64_t j0 = int64_t(list_s[u]) * kB;
-            const bool full = block_full(a, i0, j0);
+            const int64_t j0a = block_key0(2 * u), j0b = block_key0(2 * u + 1);
+            const bool fa = 2 * u < nl && block_full(a, i0, j0a);
+            const bool fb = 2 * u + 1 < nl && block_full(a, i0, j0b);
             float mraw = -INFINITY;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kB; c0 += 32) {
+            for (int c = 0; c < kSB / 32; ++c) {
                 uint32_t sv[32];
-                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                tc::tmem_ld32(tmem + uint32_t(j * kSB + c * 32) + lane_off, sv);
                 tc::tmem_ld_wait();
+                const bool full = c < 2 ? fa : fb;
+                const int64_t jc = (c < 2 ? j0a : j0b) + (c & 1) * 32;
                 mraw = fmaxf(mraw, full ? chunk_max<false>(sv, 0u)
-                                        : chunk_max<true>(sv, admitted_bits(a, i, j0 + c0)));
+                                        : chunk_max<true>(sv, admitted_bits(a, i, jc)));
             }
             tc::tc_fence_before();
             tc::mbar_arrive(bars + C::bSFree + j);
@@ -378,44 +405,33 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
 #pragma unroll
         for (int o = 0; o < kGroups; ++o) m2 = fmaxf(m2, m_part[o * kTile + row]);
         const float mm = m2 == -INFINITY ? 0.f : m2;                  // a row with no admitted key
-        // pass 1: p, l and P of this group's blocks
-        for (int u = nl + (g + kGroups - nl % kGroups) % kGroups; ok && u < 2 * nl; u += kGroups) {
-            const int jb = u - nl, j = u % C::kS, r = jb % C::kRing;
+        // pass 1: p, l and P of this group's superblocks
+        for (int u = ns + (g + kGroups - ns % kGroups) % kGroups; ok && u < 2 * ns; u += kGroups) {
+            const int sb = u - ns, j = u % C::kS;
             if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kS) & 1, status)) {
                 ok = false;
                 break;
             }
             tc::tc_fence_after();
-            const int64_t j0 = int64_t(list_s[jb]) * kB;
-            const bool full = block_full(a, i0, j0);
-            uint8_t *sP = sm + C::oP + r * C::kPBytes + row * 128;
+            const int64_t j0a = block_key0(2 * sb), j0b = block_key0(2 * sb + 1);
+            const bool fa = 2 * sb < nl && block_full(a, i0, j0a);
+            const bool fb = 2 * sb + 1 < nl && block_full(a, i0, j0b);
 #pragma unroll 1
-            for (int c0 = 0; c0 < kB; c0 += 32) {
+            for (int c = 0; c < kSB / 32; ++c) {
                 uint32_t sv[32];
-                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
+                tc::tmem_ld32(tmem + uint32_t(j * kSB + c * 32) + lane_off, sv);
                 tc::tmem_ld_wait();
-                if (c0 + 32 == kB) {
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(bars + C::bSFree + j);
-                }
+                const bool full = c < 2 ? fa : fb;
+                const int64_t jc = (c < 2 ? j0a : j0b) + (c & 1) * 32;
                 uint32_t pk[16];
                 l += full ? chunk_exp<false>(sv, 0u, a.scale_log2, mm, pk)
-                          : chunk_exp<true>(sv, admitted_bits(a, i, j0 + c0), a.scale_log2, mm, pk);
-                if (c0 == 0 && jb >= C::kRing &&
-                    !tc::mbar_wait(bars + C::bPFree + r, ((jb / C::kRing) - 1) & 1, status)) {
-                    ok = false;
-                    break;
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int chunk = (c0 >> 3) + c;
-                    *reinterpret_cast<uint4 *>(sP + ((chunk ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                }
+                          : chunk_exp<true>(sv, admitted_bits(a, i, jc), a.scale_log2, mm, pk);
+                // P over scores already read: columns [16 c, 16 c + 16) of the buffer
+                tc::tmem_st16(tmem + uint32_t(j * kSB + c * 16) + lane_off, pk);
             }
-            if (!ok) break;
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(bars + C::bPFull + r);
+            tc::tmem_st_wait();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bars + C::bPFull + j);
         }
         // the row sum over the groups
         l_part[g * kTile + row] = l;
