@@ -1,8 +1,9 @@
 #!/usr/bin/env python3
 """Benchmark of the content-dependent block-sparse attention forward.
 
-One step = one ``bsa_forward`` (block mean-pool -> coarse scoring + top-k ->
-fine attention over the selected blocks) on the 32k-token workload:
+One step = one forward (block mean-pool -> coarse scoring + top-k -> fine
+attention over the selected blocks), replayed as one captured CUDA graph of
+``bsa_forward_ex`` (``--no-graph``: one direct call) on the 32k-token workload:
 bh = 8 heads, n = 32768, d = 64, bf16, key block 64, top-16, planted block
 centres; inputs resident in HBM, L2 flushed (a 256 MiB write) before every
 timed step.  Prints ONE JSON line (rank 0):
@@ -17,6 +18,9 @@ timed step.  Prints ONE JSON line (rank 0):
   cpu_baseline  the fp64 oracle on a bounded row sample, host cores (rank 0)
 
 ``--impl reference`` times the oracle itself as the reference arm.
+``--workload`` selects another workload: the selection-option, skewed-list
+and smaller dynamic ones time the same forward; the sliding-window one times
+the static-list fine stage alone.
 Multi-GPU (torchrun): every rank runs its own independent problem (weak
 scaling, no collective on the data path); the barrier and max-over-ranks
 timing use torch.distributed.
@@ -58,6 +62,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", dest="graph", action="store_false",
+                   help="call bsa_forward_ex for every forward instead of replaying one "
+                        "captured CUDA graph (bsa_forward_graph_create / bsa_graph_launch)")
     p.add_argument("--profile-forwards", type=int, default=0, metavar="N",
                    help="run N untimed forwards of the workload and exit (a fixed launch "
                         "sequence for profilers: 6 kernels per forward); prints no JSON")
@@ -315,10 +322,10 @@ def reference_arm(args, rank, world, w):
     return 0
 
 
-def profile_static(args, w, device, dist):
-    """--profile-forwards N on a sliding-window workload: N untimed calls of
-    the static-list fine stage on the tensors of the dynamic workload of the
-    same shape (one launch each)."""
+def run_static(args, w, device, dist):
+    """A sliding-window workload: the static-list fine stage on the tensors
+    of the dynamic workload of the same shape (one launch per step); with
+    --profile-forwards N, N untimed calls, else a timed run and one JSON line."""
     import torch
     from content_dependent_block_gb300 import bsa
     base = next(x for x in workloads.WORKLOADS.values()
@@ -330,13 +337,46 @@ def profile_static(args, w, device, dist):
     lst, _, _ = bsa.static_blocks(w.n, w.q_group, w.key_block, m)
     dl = torch.from_numpy(lst).to(device)
     out = torch.empty_like(q)
-    for _ in range(args.profile_forwards):
+    def run():
         bsa.fine_attention(q, k, v, dl, key_block=w.key_block, q_group=w.q_group,
                            per_head=False, mask=m, out=out)
+
+    if args.profile_forwards > 0:
+        for _ in range(args.profile_forwards):
+            run()
+        torch.cuda.synchronize(device)
+        status = bsa.device_status()
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0 if status == 0 else 1
+    # timed: the static-list fine stage alone (one launch per step)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        run()
     torch.cuda.synchronize(device)
+    evs = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(device)
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    pairs = metrics.sliding_pairs(w.n, w.sliding) * w.bh
     status = bsa.device_status()
     if dist is not None:
         dist.destroy_process_group()
+    print(json.dumps({
+        "metric": "static sliding-window fine stage, effective TFLOP/s on admitted pairs",
+        "value": metrics.pairs_flops(pairs, w.d) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "sliding": w.sliding,
+                   "key_block": w.key_block, "q_group": w.q_group, "inputs": w.note,
+                   "timing": "median of CUDA-event times; inputs (805 MB) larger than L2"},
+        "admitted_pairs": pairs, "device_status": status}), flush=True)
     return 0 if status == 0 else 1
 
 
@@ -373,14 +413,15 @@ def main(argv=None):
     barrier(dist, device)
     bsa.lib()
 
-    if args.profile_forwards > 0 and w.kind == "sliding":
-        return profile_static(args, w, device, dist)
+    if w.kind == "sliding":
+        return run_static(args, w, device, dist)
     t = workloads.generate(w, seed=w.seed + rank)
     torch.cuda.reset_peak_memory_stats(device)
     mem0 = torch.cuda.memory_allocated(device)
     q, k, v = (torch.from_numpy(getattr(t, x).view("int16")).view(torch.bfloat16).to(device)
                for x in "qkv")
-    fwd = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk, device=device, **select_args(w, device))
+    fwd = bsa.Forward(w.bh, w.n, w.d, w.key_block, w.topk, device=device, graph=args.graph,
+                      **select_args(w, device))
     fwd(q, k, v)
     torch.cuda.synchronize(device)
     if args.profile_forwards > 0:
@@ -496,11 +537,14 @@ def main(argv=None):
     peaks = measured_peaks()
     tc_peak = peaks["bf16_tflops"]
     achieved = fine_flops / (fine_ms * 1e-3) / 1e12
+    cfg = config_of(w)
+    cfg["launch"] = ("one CUDA-graph replay per forward" if args.graph
+                     else "one bsa_forward_ex call per forward")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+        "dtype": "bf16", "data": "synthetic", "config": cfg,
         "roofline": {"kernel": "fine attention stage: one bsa_fine_attention call over the top-k "
                                "list (list inversion + fine_ws_kernel)",
                      "bound": "tensor", "achieved": achieved, "peak": tc_peak,

@@ -28,7 +28,7 @@ EXPORTS = (
     "bsa_pool_blocks", "bsa_coarse_topk_workspace_size", "bsa_coarse_topk",
     "bsa_coarse_topk_ex", "bsa_fine_attention_workspace_size", "bsa_fine_attention",
     "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_ex", "bsa_forward_noalloc",
-    "bsa_forward_launches",
+    "bsa_forward_launches", "bsa_forward_graph_create", "bsa_graph_launch", "bsa_graph_destroy",
     "bsa_static_max_blocks",
     "bsa_static_blocks", "bsa_get_device_status", "bsa_status_string",
     "bsa_last_error", "bsa_version",
@@ -94,6 +94,10 @@ def lib():
         "bsa_forward_ex": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp, vp, vp,
                             sz, vp], i32),
         "bsa_forward_noalloc": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp], i32),
+        "bsa_forward_graph_create": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp,
+                                      vp, vp, sz, ctypes.POINTER(vp)], i32),
+        "bsa_graph_launch": ([vp, vp], i32),
+        "bsa_graph_destroy": ([vp], i32),
         "bsa_forward_launches": ([Shape, i32, i32], i32),
         "bsa_static_max_blocks": ([i64, i32, i32, Mask], i32),
         "bsa_static_blocks": ([i64, i32, i32, Mask, vp, i32, vp, vp], i32),
@@ -212,16 +216,21 @@ def fine_attention(q, k, v, block_list=None, *, key_block: int, q_group: int = 1
 
 class Forward:
     """Reusable forward: owns the output, selection and workspace buffers for
-    one shape so repeated calls allocate nothing."""
+    one shape so repeated calls allocate nothing.  With ``graph=True`` the
+    forward is captured once as a CUDA graph (bsa_forward_graph_create) for
+    the q, k, v buffers of the first call and replayed with one launch; a
+    call with other buffers captures again."""
 
     def __init__(self, bh: int, n: int, d: int, key_block: int, topk: int, device="cuda",
                  scale: float = 0.0, *, head_topk=None, causal: bool = False,
-                 local_block: bool = False):
+                 local_block: bool = False, graph: bool = False):
         torch = _torch()
         self.shape = Shape(bh, n, d, BF16)
         self.key_block, self.topk, self.scale = key_block, topk, scale
         self.head_topk = head_topk            # kept alive: the library reads it on every call
         self.sel = _select(head_topk, causal, local_block)
+        self.use_graph = graph
+        self._graph = None                    # (handle, (q, k, v) pointers, keep_idx)
         self.ws_bytes = lib().bsa_forward_workspace_size(self.shape, key_block, topk)
         self.ws = _workspace(self.ws_bytes, device)
         self.out = torch.empty((bh, n, d), dtype=torch.bfloat16, device=device)
@@ -236,12 +245,36 @@ class Forward:
         s = _shape(q)
         if (s.bh, s.n, s.d) != (self.shape.bh, self.shape.n, self.shape.d):
             raise ValueError("shape differs from the one this Forward was built for")
-        _check(lib().bsa_forward_ex(self.shape, _ptr(q), _ptr(k), _ptr(v), self.key_block,
-                                    self.topk, None if self.sel is None else ctypes.byref(self.sel),
-                                    float(self.scale), _ptr(self.out),
-                                    _ptr(self.idx if keep_idx else None), _ptr(self.ws),
-                                    self.ws_bytes, _stream()))
+        sel = None if self.sel is None else ctypes.byref(self.sel)
+        if not self.use_graph:
+            _check(lib().bsa_forward_ex(self.shape, _ptr(q), _ptr(k), _ptr(v), self.key_block,
+                                        self.topk, sel, float(self.scale), _ptr(self.out),
+                                        _ptr(self.idx if keep_idx else None), _ptr(self.ws),
+                                        self.ws_bytes, _stream()))
+            return self.out
+        key = ((q.data_ptr(), k.data_ptr(), v.data_ptr()), keep_idx)
+        if self._graph is None or self._graph[1] != key:
+            self.close()
+            h = ctypes.c_void_p()
+            _check(lib().bsa_forward_graph_create(
+                self.shape, _ptr(q), _ptr(k), _ptr(v), self.key_block, self.topk, sel,
+                float(self.scale), _ptr(self.out), _ptr(self.idx if keep_idx else None),
+                _ptr(self.ws), self.ws_bytes, ctypes.byref(h)))
+            self._graph = (h, key)
+        _check(lib().bsa_graph_launch(self._graph[0], _stream()))
         return self.out
+
+    def close(self):
+        """Release the captured graph, if any."""
+        if self._graph is not None:
+            lib().bsa_graph_destroy(self._graph[0])
+            self._graph = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def forward(q, k, v, key_block: int, topk: int, scale: float = 0.0, *, head_topk=None,

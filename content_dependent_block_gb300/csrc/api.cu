@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
 
 #include "bsa.h"
 #include "bsa_internal.h"
@@ -514,6 +515,69 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
     if (bsa::fine_static_tc_supported(a, shape.dtype))
         return launched(bsa::launch_fine_static_tc(a, st), "fine attention (tensor-core tiles) launch");
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
+}
+
+// ------------------------------------------------------------ CUDA graphs
+struct bsa_graph_s {
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+bsa_status bsa_forward_graph_create(bsa_shape shape, const void *q, const void *k, const void *v,
+                                    int32_t key_block, int32_t topk, const bsa_select *sel,
+                                    float scale, void *out, int32_t *idx_out, void *ws,
+                                    size_t ws_bytes, bsa_graph *graph) {
+    if (graph == nullptr) return fail(BSA_ERR_INVALID_ARG, "graph is NULL");
+    *graph = nullptr;
+    if (device_status_ptr() == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    cudaStream_t cs = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "capture stream: %s", cudaGetErrorString(e));
+    e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(cs);
+        return fail(BSA_ERR_CUDA, "begin capture: %s", cudaGetErrorString(e));
+    }
+    const bsa_status st = bsa_forward_ex(shape, q, k, v, key_block, topk, sel, scale, out, idx_out,
+                                         ws, ws_bytes, cs);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(cs, &g);
+    cudaStreamDestroy(cs);
+    if (st != BSA_OK) {                       // the reason is already recorded
+        if (g != nullptr) cudaGraphDestroy(g);
+        return st;
+    }
+    if (e != cudaSuccess || g == nullptr)
+        return fail(BSA_ERR_CUDA, "end capture: %s", cudaGetErrorString(e));
+    cudaGraphExec_t x = nullptr;
+    e = cudaGraphInstantiate(&x, g, 0);
+    if (e != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return fail(BSA_ERR_CUDA, "instantiate: %s", cudaGetErrorString(e));
+    }
+    bsa_graph h = new (std::nothrow) bsa_graph_s{g, x};
+    if (h == nullptr) {
+        cudaGraphExecDestroy(x);
+        cudaGraphDestroy(g);
+        return fail(BSA_ERR_CUDA, "out of host memory");
+    }
+    *graph = h;
+    return ok();
+}
+
+bsa_status bsa_graph_launch(bsa_graph graph, void *stream) {
+    if (graph == nullptr) return fail(BSA_ERR_INVALID_ARG, "graph is NULL");
+    const cudaError_t e = cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "graph launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+bsa_status bsa_graph_destroy(bsa_graph graph) {
+    if (graph == nullptr) return ok();
+    cudaGraphExecDestroy(graph->exec);
+    cudaGraphDestroy(graph->graph);
+    delete graph;
+    return ok();
 }
 
 }  // extern "C"

@@ -220,6 +220,32 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k,
                           void *stream);
 
 /*
+ * The whole forward as one CUDA graph (page "sparse-attention-triton-bench",
+ * The Triton kernel: the forward as a few fused launches instead of the
+ * hundreds of a Python loop; here every launch of bsa_forward_ex is captured
+ * once and the caller replays them with one host call).
+ *   bsa_forward_graph_create  captures bsa_forward_ex for these exact
+ *       pointers and arguments (same validation and errors) on a private
+ *       stream and instantiates it; *graph receives the handle (NULL on
+ *       error).  Nothing runs at creation.
+ *   bsa_graph_launch  enqueues one replay on `stream`: it reads whatever the
+ *       captured q, k, v (and head_topk) buffers hold at that time and writes
+ *       out (and idx_out); the workspace must stay allocated and unshared
+ *       while replays can run.
+ *   bsa_graph_destroy  releases the handle (NULL is a no-op); replays already
+ *       enqueued complete.
+ */
+typedef struct bsa_graph_s *bsa_graph;
+bsa_status bsa_forward_graph_create(bsa_shape shape, const void *q,
+                                    const void *k, const void *v,
+                                    int32_t key_block, int32_t topk,
+                                    const bsa_select *sel, float scale,
+                                    void *out, int32_t *idx_out, void *ws,
+                                    size_t ws_bytes, bsa_graph *graph);
+bsa_status bsa_graph_launch(bsa_graph graph, void *stream);
+bsa_status bsa_graph_destroy(bsa_graph graph);
+
+/*
  * bsa_forward without a workspace argument, for callers that must not
  * allocate device memory at call time (e.g. a plugin inside an application
  * whose memory manager owns the device, or a latency-bound loop that cannot

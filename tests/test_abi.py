@@ -96,6 +96,13 @@ def test_pool_and_coarse_reject_fp32(L):
     assert L.bsa_coarse_topk_ex(s, FAKE, FAKE, 64, 4, None, FAKE, None, 0, None) == 2
 
 
+def test_graph_handles_are_checked(L):
+    assert L.bsa_forward_graph_create(_shape(), FAKE, FAKE, FAKE, 64, 4, None, 0.0, FAKE, None,
+                                      FAKE, 1 << 30, None) == 1
+    assert L.bsa_graph_launch(None, None) == 1
+    assert L.bsa_graph_destroy(None) == 0
+
+
 def test_select_options_are_checked(L):
     s = _shape()
     bad = bsa.Select(0x10002, 1, 0)                   # head_topk not 4-byte aligned

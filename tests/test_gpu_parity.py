@@ -108,6 +108,25 @@ def test_forward_matches_oracle(name):
     assert bsa.device_status() == 0
 
 
+def test_forward_skewed_lists():
+    """Planted popular blocks that nearly every query selects: a popular
+    (head, range, block) bin holds ~30x the mean number of pairs; the work
+    items split it and the persistent CTAs share it."""
+    w, t, (q, k, v) = tensors("dyn_n32768_skew", bh=2, n=8192)
+    f = bsa.Forward(2, 8192, w.d, w.key_block, w.topk)
+    out = f(q, k, v)
+    rows = oracle.all_rows(2, 8192)
+    s = oracle.scores(t.q, oracle.pool(t.k, w.key_block), rows)
+    oidx, kth = oracle.topk(s, w.topk)
+    gidx = f.idx.cpu().numpy().reshape(-1, w.topk)
+    parity.check_selection(gidx, oidx, s, kth, 8192 // w.key_block)
+    pop = np.linspace(0, 8192 // w.key_block - 1, w.popular).round().astype(int)
+    assert np.isin(gidx, pop).sum(1).mean() > 6          # the lists really are skewed
+    o_ref, _, _ = oracle.fine(t.q, t.k, t.v, w.key_block, gidx, rows)
+    parity.assert_close(parity.from_device(out).reshape(-1, w.d), o_ref, "bf16", "skewed lists")
+    assert bsa.device_status() == 0
+
+
 @pytest.mark.parametrize("name", ["local_global_n4096", "local_global_n4100"])
 def test_static_local_global_fp32(name):
     w, t, (q, k, v) = tensors(name)

@@ -177,3 +177,27 @@ def test_static_tc_causal(n, d):
     got = parity.from_device(out).reshape(-1, d)[rows]
     parity.assert_close(got, ref, "bf16", f"static causal n={n} d={d}")
     assert bsa.device_status() == 0
+
+
+@pytest.mark.parametrize("opt", [dict(), dict(causal=True, local=True, budgets=True)],
+                         ids=["plain", "options"])
+def test_graph_replay_matches_direct_calls(opt):
+    """The captured forward reads its input buffers at every replay."""
+    import torch
+    bh, n, d, k = 2, 3000, 64, 8
+    t, (q, kk, v) = _inputs(bh, n, d, seed=31)
+    hk = torch.from_numpy(_budgets(bh, k)).cuda() if opt.get("budgets") else None
+    kw = dict(head_topk=hk, causal=opt.get("causal", False), local_block=opt.get("local", False))
+    direct = bsa.Forward(bh, n, d, 64, k, **kw)
+    graph = bsa.Forward(bh, n, d, 64, k, graph=True, **kw)
+    for step in range(3):
+        if step:
+            q.copy_(q.roll(1, dims=1))                  # new inputs, same buffers
+            v.mul_(-1)
+        o1 = direct(q, kk, v).clone()
+        i1 = direct.idx.clone()
+        o2 = graph(q, kk, v)
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o2) and torch.equal(i1, graph.idx), f"step {step}"
+    graph.close()
+    assert bsa.device_status() == 0

@@ -48,6 +48,10 @@ class Workload:
     causal: bool = False
     local_block: bool = False
     head_topk: tuple = ()
+    # skewed lists: `popular` blocks spread over the sequence that nearly
+    # every query selects (keys of those blocks shifted along channel 0,
+    # queries shifted the same way); 0 = none
+    popular: int = 0
 
     @property
     def has_options(self) -> bool:
@@ -89,6 +93,11 @@ WORKLOADS = {
         "dyn_n32768_budgets", bh=8, n=32768, d=64, dtype="bf16", kind="dynamic",
         key_block=64, topk=16, centre_sigma=0.5, head_topk=(16, 12, 8, 4, 16, 12, 8, 4),
         note="as dyn_n32768; per-head budgets 16/12/8/4 (twice)"),
+    "dyn_n32768_skew": Workload(
+        "dyn_n32768_skew", bh=8, n=32768, d=64, dtype="bf16", kind="dynamic",
+        key_block=64, topk=16, centre_sigma=0.5, popular=8,
+        note="as dyn_n32768 plus 8 popular blocks nearly every query selects: "
+             "skewed lists, a popular (head, range, block) bin holds ~30x the mean"),
     "dyn_n131072": Workload(
         "dyn_n131072", bh=8, n=131072, d=128, dtype="bf16", kind="dynamic",
         key_block=64, topk=32, centre_sigma=0.5,
@@ -159,6 +168,12 @@ def generate(w: Workload, *, bh: Optional[int] = None, n: Optional[int] = None,
         tok_block = np.arange(n) // w.key_block
         k += centres[:, tok_block, :]
     v = rng.standard_normal(shape, dtype=np.float32)
+    if w.popular > 0:
+        # no extra draws: the other workloads' streams stay as they are
+        q[:, :, 0] += np.float32(3.0)
+        pop = np.linspace(0, nb - 1, w.popular).round().astype(np.int64)
+        for b in pop:
+            k[:, b * w.key_block:(b + 1) * w.key_block, 0] += np.float32(6.0)
     if w.dtype == "bf16":
         return Tensors(bf16_bits_rne(q), bf16_bits_rne(k), bf16_bits_rne(v),
                        "bf16", {"seed": seed})
