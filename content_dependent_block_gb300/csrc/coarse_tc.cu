@@ -18,10 +18,12 @@
 //               every chunk, so each thread scans half of its query's scores
 //               and keeps a running top-k in registers; the two lists are
 //               merged at the end
-// Selection: every 16 scores of a thread are sorted by a bitonic network and
-// merged into its running top-k (element-wise max against the reversed batch,
-// then a bitonic merge): the same compare-exchanges on every lane, no
-// data-dependent branches.
+// Selection: a thread compares each score's key with its current k-th key
+// and queues the ones that beat it in shared memory (no branches); when a
+// lane of the warp has 16 queued, every lane sorts its first 16 by a bitonic
+// network and merges them into its running top-k (element-wise max against
+// the reversed batch, then a bitonic merge).  The sorting work follows the
+// scores that can still enter the top-k, not all of them.
 // Precision: Kbar enters as a bf16 pair (hi = bf16(Kbar), lo = bf16(Kbar -
 // hi)); S = Q.hi + Q.lo accumulates in fp32, i.e. about 2^-16 relative to
 // the fp32 mean -- far inside the 1e-3 relative tie band of the selection.
@@ -51,7 +53,8 @@ constexpr int kGroups = 2;         // epilogue warpgroups (column split)
 constexpr int kEpi = kGroups * kTileM;
 constexpr int kThreads = 64 + kEpi;
 constexpr int kTmemCols = 2 * kChunk;
-constexpr int kQueue = 16;         // scores filtered per drain (divides 32)
+constexpr int kSlice = 8;          // scores filtered between drain checks (divides 32)
+constexpr int kQueue = 16 + kSlice;   // queued keys per thread: < 16 after a drain, + one slice
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>
@@ -245,6 +248,24 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
         uint32_t L[KMAX];
 #pragma unroll
         for (int t = 0; t < KMAX; ++t) L[t] = 0u;  // 0 = empty (below every real key)
+        // Selection: keys that beat the thread's current k-th key wait in a
+        // small shared-memory queue (this thread's column of it); whenever a
+        // lane of the warp has 16 queued, every lane sorts its first 16
+        // (bitonic, padded with empty keys) and merges them into L.  Most
+        // scores stop at one compare; the sort runs on the few that pass.
+        uint32_t *qu = queue + eg * kTileM + r;    // [kQueue][kEpi]
+        int cnt = 0;
+        auto drain = [&]() {
+            uint32_t B[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) B[t] = t < cnt ? qu[t * kEpi] : 0u;
+            sort16_desc(B);
+            merge_sorted<KMAX, 16>(L, B);
+#pragma unroll
+            for (int t = 0; t < kQueue - 16; ++t)
+                if (16 + t < cnt) qu[t * kEpi] = qu[(16 + t) * kEpi];
+            cnt = max(cnt - 16, 0);
+        };
         bool ok = true;
         for (int c = 0; c < nchunks; ++c) {
             const int buf = c & 1;
@@ -264,24 +285,25 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
                     uint32_t v[32];
                     tc::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kChunk + j * 32), v);
                     tc::tmem_ld_wait();
-#pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        // 16 keys: sort them, merge them into the running top-k
-                        uint32_t B[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int x = hf * 16 + e;
-                            const uint32_t vx = hf ? v[16 + e] : v[e];
-                            B[e] = x < lim ? score_key(__uint_as_float(vx), col0 + x, key_mask) : 0u;
+                    for (int hf = 0; hf < 32 / kSlice; ++hf) {
+                        // queue the keys that beat the current k-th key (no branches)
+                        const uint32_t thr = L[KMAX - 1];
+#pragma unroll
+                        for (int e = 0; e < kSlice; ++e) {
+                            const int x = hf * kSlice + e;
+                            const uint32_t key = score_key(__uint_as_float(v[x]), col0 + x, key_mask);
+                            qu[cnt * kEpi] = key;
+                            cnt += (x < lim && key > thr) ? 1 : 0;
                         }
-                        sort16_desc(B);
-                        merge_sorted<KMAX, 16>(L, B);
+                        if (__any_sync(kFull, cnt >= 16)) drain();
                     }
                 }
             }
             tc::tc_fence_before();
             tc::mbar_arrive(acc_empty + buf);
         }
+        while (__any_sync(kFull, cnt > 0)) drain();
         // group 1 hands its list to group 0, which merges and writes
         static_assert(KMAX * kTileM <= S::kQueueWords, "merge lists fit the queue region");
         tc::named_bar_sync(1, kEpi);               // every queue drained
