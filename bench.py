@@ -178,16 +178,17 @@ def measured_peaks():
     return d
 
 
-def kernel_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's
-    source has not changed since it was captured; else None."""
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was
+    captured on this workload and the kernel's source has not changed since;
+    else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         table = json.load(f)
     ent = table.get(kernel)
-    if not ent:
+    if not ent or ent.get("workload") != workload:
         return None
     sources = ent.get("sources") or {ent["source"]: ent.get("source_sha")}
     for rel, want in sources.items():
@@ -550,7 +551,8 @@ def main(argv=None):
                      "bound": "tensor", "achieved": achieved, "peak": tc_peak,
                      "unit": "TFLOP/s", "frac": achieved / tc_peak,
                      "peak_source": f"bf16_tflops burst, {peaks['source']}",
-                     "traffic": kernel_traffic("fine_stage" if fwd.launches == 6 else "fine_query_major"),
+                     "traffic": kernel_traffic("fine_stage" if fwd.launches == 6 else "fine_query_major",
+                                               w.name),
                      "algorithmic_flops_per_launch": fine_flops,
                      "launch_ms": fine_ms},
         "e2e": {"value": flops * world / (e2e_total / args.steps * 1e-3) / 1e12,
