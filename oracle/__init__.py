@@ -59,6 +59,8 @@ def _load():
         lib.orc_select.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, i32, i32, vp]
         lib.orc_fine.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, vp, i64,
                                  vp, i64, i32, dbl, vp, vp, vp]
+        lib.orc_fine_backward.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, i64, i32,
+                                          dbl, vp, vp, vp]
         lib.orc_mask.argtypes = [i32, i64, i64, i64, i64, i64]
         lib.orc_mask.restype = ctypes.c_int
         lib.orc_masked.argtypes = [vp, vp, vp, i32, i64, i64, i64, i32, i64,
@@ -176,6 +178,21 @@ def fine(q, k, v, key_block: int, idx: np.ndarray, rows: np.ndarray,
                      key_block, _ptr(idx), kk, _ptr(rows), rows.size, int(causal),
                      ctypes.c_double(scale), _ptr(o), _ptr(lse), _ptr(psum))
     return o, lse, psum
+
+
+def fine_backward(q, k, v, do, key_block: int, idx: np.ndarray,
+                  scale: Optional[float] = None, causal: bool = False):
+    """Gradients (dQ, dK, dV) [bh, n, d] float64 of the fine stage with the
+    selection fixed (page "sparse-attention-triton-bench", What's next:
+    backward pass).  ``idx`` holds the lists of every row, [bh*n, kmax]."""
+    bh, n, d = _check3(q, k, v, do)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    idx = np.ascontiguousarray(idx, dtype=np.int32).reshape(bh * n, -1)
+    out = [np.empty((bh, n, d), dtype=np.float64) for _ in range(3)]
+    _load().orc_fine_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _dtype_code(q), bh, n, d,
+                              key_block, _ptr(idx), idx.shape[1], int(causal),
+                              ctypes.c_double(scale), *(_ptr(a) for a in out))
+    return tuple(out)
 
 
 def mask(kind: int, i: int, j: int, w: int = -1, s: int = 0, W: int = 0) -> bool:

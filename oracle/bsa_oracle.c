@@ -311,6 +311,84 @@ void orc_fine(const void *Q, const void *K, const void *V, int dtype,
  *  [P3] sliding window, causal, W tokens including i:  i-W < j <= i.
  *  [P3] section 1, causal (lower triangle):  j <= i.
  */
+/*
+ * [P1] What's next, backward pass: gradients of the fine stage through the
+ * sparse softmax-weighted sum, with the selection held fixed (it is a
+ * discrete choice).  For row i of head bh with token set T_i (the listed
+ * blocks' keys; only j <= i when causal), s_ij = scale q_i.k_j,
+ * p_ij = softmax over T_i, o_i = sum_j p_ij v_j, and a given dO:
+ *   dv_j += p_ij do_i
+ *   dp_ij = do_i . v_j
+ *   ds_ij = p_ij (dp_ij - sum_t p_it dp_it)
+ *   dq_i  = scale sum_j ds_ij k_j
+ *   dk_j += scale ds_ij q_i
+ * idx holds the lists of every row [BH*N][k]; every row is processed, one
+ * head per thread (dK, dV gather over a head's rows).  dQ, dK, dV are
+ * [BH][N][d] doubles.  A row with no token contributes nothing.
+ */
+void orc_fine_backward(const void *Q, const void *K, const void *V, const void *dO,
+                       int dtype, int64_t BH, int64_t N, int64_t d, int64_t B,
+                       const int32_t *idx, int64_t k, int causal, double scale,
+                       double *dQ, double *dK, double *dV) {
+    memset(dQ, 0, sizeof(double) * (size_t)(BH * N * d));
+    memset(dK, 0, sizeof(double) * (size_t)(BH * N * d));
+    memset(dV, 0, sizeof(double) * (size_t)(BH * N * d));
+#pragma omp parallel
+    {
+        int64_t *tok = (int64_t *)malloc(sizeof(int64_t) * (size_t)(k * B + 1));
+        double *p = (double *)malloc(sizeof(double) * (size_t)(k * B + 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(k * B + 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < BH; ++bh) {
+            for (int64_t i = 0; i < N; ++i) {
+                const int64_t r = bh * N + i;
+                int64_t nt = 0;
+                for (int64_t t = 0; t < k; ++t) {
+                    int32_t b = idx[r * k + t];
+                    if (b < 0) continue;
+                    for (int64_t j = (int64_t)b * B; j < ((int64_t)b + 1) * B && j < N; ++j)
+                        if (!causal || j <= i) tok[nt++] = j;
+                }
+                if (nt == 0) continue;
+                double m = -INFINITY;
+                for (int64_t t = 0; t < nt; ++t) {
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += widen(Q, dtype, r * d + c) * widen(K, dtype, (bh * N + tok[t]) * d + c);
+                    p[t] = scale * dot;
+                    if (p[t] > m) m = p[t];
+                }
+                double l = 0.0;
+                for (int64_t t = 0; t < nt; ++t) {
+                    p[t] = exp(p[t] - m);
+                    l += p[t];
+                }
+                double rowsum = 0.0;                 /* sum_t p_it dp_it */
+                for (int64_t t = 0; t < nt; ++t) {
+                    p[t] /= l;
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c)
+                        dot += widen(dO, dtype, r * d + c) * widen(V, dtype, (bh * N + tok[t]) * d + c);
+                    dp[t] = dot;
+                    rowsum += p[t] * dot;
+                }
+                for (int64_t t = 0; t < nt; ++t) {
+                    const int64_t jr = bh * N + tok[t];
+                    const double ds = p[t] * (dp[t] - rowsum);
+                    for (int64_t c = 0; c < d; ++c) {
+                        dV[jr * d + c] += p[t] * widen(dO, dtype, r * d + c);
+                        dQ[r * d + c] += scale * ds * widen(K, dtype, jr * d + c);
+                        dK[jr * d + c] += scale * ds * widen(Q, dtype, r * d + c);
+                    }
+                }
+            }
+        }
+        free(tok);
+        free(p);
+        free(dp);
+    }
+}
+
 int orc_mask(int kind, int64_t w, int64_t s, int64_t W, int64_t i, int64_t j) {
     if (kind == ORC_MASK_LOCAL_GLOBAL) {
         int64_t dist = i > j ? i - j : j - i;

@@ -129,3 +129,42 @@ def test_mask_kind_causal_is_causal_attention():
     o, _, psum = oracle.masked(q, k, v, oracle.MASK_CAUSAL, rows)
     np.testing.assert_allclose(o, _sdpa(q, k, v, causal=True).reshape(-1, 64), rtol=0, atol=1e-12)
     assert oracle.mask(oracle.MASK_CAUSAL, 5, 5) and not oracle.mask(oracle.MASK_CAUSAL, 5, 6)
+
+
+# ------------------------------------------------------------ backward pass
+def _random_lists(bh, n, B, k, seed, causal):
+    rng = np.random.default_rng(seed)
+    nb = -(-n // B)
+    idx = np.full((bh * n, k), -1, np.int32)
+    for r in range(bh * n):
+        i = r % n
+        last = i // B if causal else nb - 1
+        m = rng.integers(0, min(k, last + 1) + 1)           # some rows get no block
+        idx[r, :m] = np.sort(rng.choice(last + 1, size=m, replace=False))
+    return idx
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_equals_autograd_of_masked_attention(causal):
+    """The fine stage with its lists fixed is masked softmax attention; torch
+    autograd of that (float64) gives the gradients."""
+    bh, n, d, B, k = 2, 150, 64, 16, 4                     # ragged last block (6 tokens)
+    q, kk, v = _qkv(bh, n, d, seed=40 + causal)
+    do = _qkv(bh, n, d, seed=50 + causal)[0]
+    idx = _random_lists(bh, n, B, k, seed=3, causal=causal)
+    dq, dk, dv = oracle.fine_backward(q, kk, v, do, B, idx, causal=causal)
+    mask = np.zeros((bh, n, n), dtype=bool)
+    for r in range(bh * n):
+        h, i = divmod(r, n)
+        for b in idx[r]:
+            if b >= 0:
+                j = np.arange(b * B, min(n, (b + 1) * B))
+                mask[h, i, j[(j <= i) if causal else slice(None)]] = True
+    Q, K, V = (_f64(x).requires_grad_() for x in (q, kk, v))
+    s = (Q @ K.transpose(-1, -2)) / np.sqrt(d)
+    s = s.masked_fill(~torch.from_numpy(mask), float("-inf"))
+    p = torch.softmax(s, dim=-1).nan_to_num(0.0)           # rows with no key: zero
+    (p @ V).backward(_f64(do))
+    for got, ref in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
+        np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-11)
+    assert (dq.reshape(-1, d)[(idx < 0).all(1)] == 0).all()  # empty rows: no gradient
