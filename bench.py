@@ -62,6 +62,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     p.add_argument("--workload", default=WORKLOAD, choices=sorted(workloads.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--backward", action="store_true",
+                   help="time the fine stage's backward pass (bsa_fine_backward) over the "
+                        "forward's lists instead of the forward; prints its own JSON line")
     p.add_argument("--no-graph", dest="graph", action="store_false",
                    help="call bsa_forward_ex for every forward instead of replaying one "
                         "captured CUDA graph (bsa_forward_graph_create / bsa_graph_launch)")
@@ -381,6 +384,66 @@ def run_static(args, w, device, dist):
     return 0 if status == 0 else 1
 
 
+def run_backward(args, w, fwd, q, k, v, device, dist):
+    """The fine stage's backward pass over the lists (and output) of one
+    forward: bsa_fine_backward timed alone, CUDA events, L2 flushed before
+    every step; one JSON line.  It runs on the CUDA cores, so the roofline is
+    the FP32 peak."""
+    import torch
+    from content_dependent_block_gb300 import bsa
+    gen = torch.Generator(device="cpu").manual_seed(1)
+    dout = torch.randn(q.shape, generator=gen).to(torch.bfloat16).to(device)
+    L = bsa.lib()
+    ld = bsa.ListDesc(1, w.key_block, w.topk, 1)
+    m = bsa.mask_struct(bsa.MASK_CAUSAL if w.causal else bsa.MASK_NONE)
+    dq, dk, dv = (torch.empty(q.shape, dtype=torch.float32, device=device) for _ in range(3))
+    ws_n = L.bsa_fine_backward_workspace_size(fwd.shape, ld)
+    ws = bsa._workspace(ws_n, device)
+    P = bsa._ptr
+
+    def step():
+        bsa._check(L.bsa_fine_backward(fwd.shape, P(q), P(k), P(v), P(fwd.out), P(dout),
+                                       P(fwd.idx), ld, m, 0.0, P(dq), P(dk), P(dv), P(ws), ws_n,
+                                       bsa._stream()))
+
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    evs = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize(device)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    pairs = admitted_pairs(fwd.idx, w)
+    # per admitted (query, key) pair: q.k, dO.v, dQ, dK and dV updates (2d each) + softmax ops
+    flops = pairs * (10 * w.d + 5)
+    peaks = measured_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    p_fp32 = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+    achieved = flops / (ms * 1e-3) / 1e12
+    status = bsa.device_status()
+    if dist is not None:
+        dist.destroy_process_group()
+    print(json.dumps({
+        "metric": "fine-stage backward pass (dQ, dK, dV over the forward's lists), effective TFLOP/s",
+        "value": achieved, "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps,
+        "warmup": args.warmup, "n_gpus": 1, "higher_is_better": True, "dtype": "bf16 in, fp32",
+        "data": "synthetic", "config": config_of(w),
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": p_fp32 / 1e12,
+                     "unit": "TFLOP/s", "frac": achieved * 1e12 / p_fp32,
+                     "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x max clock"},
+        "admitted_pairs": pairs, "flops_per_step": flops, "device_status": status}), flush=True)
+    return 0 if status == 0 else 1
+
+
 def config_of(w):
     c = {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "key_block": w.key_block,
          "topk": w.topk, "dtype": w.dtype, "inputs": w.note,
@@ -425,6 +488,8 @@ def main(argv=None):
                       **select_args(w, device))
     fwd(q, k, v)
     torch.cuda.synchronize(device)
+    if args.backward:
+        return run_backward(args, w, fwd, q, k, v, device, dist)
     if args.profile_forwards > 0:
         for _ in range(args.profile_forwards - 1):
             fwd(q, k, v)

@@ -517,6 +517,102 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }
 
+// ---------------------------------------------------------- backward pass
+struct BwdLayout {
+    size_t lse = 0, dsum = 0, counts = 0, cursors = 0, offsets = 0, qlist = 0, total = 0;
+};
+
+BwdLayout bwd_layout(const bsa_shape &s, int32_t kb, int32_t k) {
+    BwdLayout L;
+    const size_t rows = size_t(s.bh) * size_t(s.n), bins = size_t(s.bh) * size_t(ceil_div(s.n, kb));
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = at;
+        at += round_up(bytes, 256);
+        return o;
+    };
+    L.lse = take(rows * 4);
+    L.dsum = take(rows * 4);
+    L.counts = take(bins * 4);
+    L.cursors = take(bins * 4);
+    L.offsets = take((bins + 1) * 4);
+    L.qlist = take(rows * size_t(k) * 4);
+    L.total = at;
+    return L;
+}
+
+bool bwd_lists_ok(const bsa_list_desc &ld) {
+    return ld.q_group == 1 && ld.per_head && ld.max_blocks >= 1 && ld.max_blocks <= 64;
+}
+
+size_t bsa_fine_backward_workspace_size(bsa_shape shape, bsa_list_desc ld) {
+    if (check_shape(shape) != BSA_OK || check_key_block(ld.key_block) != BSA_OK || !bwd_lists_ok(ld))
+        return 0;
+    return bwd_layout(shape, ld.key_block, ld.max_blocks).total;
+}
+
+bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, const void *v,
+                             const void *out, const void *dout, const int32_t *list,
+                             bsa_list_desc ld, bsa_mask mask, float scale, float *dq, float *dk,
+                             float *dv, void *ws, size_t ws_bytes, void *stream) {
+    BSA_TRY(check_shape(shape));
+    if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "the backward pass takes bf16");
+    BSA_TRY(check_key_block(ld.key_block));
+    if (!bwd_lists_ok(ld))
+        return fail(BSA_ERR_UNSUPPORTED,
+                    "the backward pass takes per-query lists (q_group 1, per head, 1..64 blocks)");
+    if (mask.kind != BSA_MASK_NONE && mask.kind != BSA_MASK_CAUSAL)
+        return fail(BSA_ERR_UNSUPPORTED, "the backward pass takes no mask or the causal one");
+    if (!bsa::fine_backward_supported(shape.d, ld.key_block))
+        return fail(BSA_ERR_UNSUPPORTED, "the backward pass takes d 64 or 128 and key_block * d <= 8192");
+    BSA_TRY(check_ptr(q, "q"));
+    BSA_TRY(check_ptr(k, "k"));
+    BSA_TRY(check_ptr(v, "v"));
+    BSA_TRY(check_ptr(out, "out"));
+    BSA_TRY(check_ptr(dout, "dout"));
+    BSA_TRY(check_ptr(dq, "dq"));
+    BSA_TRY(check_ptr(dk, "dk"));
+    BSA_TRY(check_ptr(dv, "dv"));
+    if (list == nullptr) return fail(BSA_ERR_INVALID_ARG, "list is NULL");
+    if (!aligned(list, 4)) return fail(BSA_ERR_ALIGNMENT, "list is not 4-byte aligned");
+    const BwdLayout L = bwd_layout(shape, ld.key_block, ld.max_blocks);
+    BSA_TRY(check_ws(ws, ws_bytes, L.total));
+    int32_t *status = device_status_ptr();
+    if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(ws);
+    // counts and cursors are adjacent: one memset
+    cudaError_t e = cudaMemsetAsync(base + L.counts, 0, L.offsets - L.counts, st);
+    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    bsa::BwdArgs a{};
+    a.q = static_cast<const uint16_t *>(q);
+    a.kp = static_cast<const uint16_t *>(k);
+    a.vp = static_cast<const uint16_t *>(v);
+    a.out = static_cast<const uint16_t *>(out);
+    a.dout = static_cast<const uint16_t *>(dout);
+    a.list = list;
+    a.bh = shape.bh;
+    a.n = shape.n;
+    a.nb = ceil_div(shape.n, ld.key_block);
+    a.d = shape.d;
+    a.k = ld.max_blocks;
+    a.kb = ld.key_block;
+    a.causal = mask.kind == BSA_MASK_CAUSAL ? 1 : 0;
+    a.scale = scale > 0.f ? scale : 1.0f / std::sqrt(float(shape.d));
+    a.scale_log2 = softmax_scale_log2(scale, shape.d);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.lse = reinterpret_cast<float *>(base + L.lse);
+    a.dsum = reinterpret_cast<float *>(base + L.dsum);
+    a.counts = reinterpret_cast<int32_t *>(base + L.counts);
+    a.cursors = reinterpret_cast<int32_t *>(base + L.cursors);
+    a.offsets = reinterpret_cast<int32_t *>(base + L.offsets);
+    a.qlist = reinterpret_cast<int32_t *>(base + L.qlist);
+    a.status = status;
+    return launched(bsa::launch_fine_backward(a, st), "backward launch");
+}
+
 // ------------------------------------------------------------ CUDA graphs
 struct bsa_graph_s {
     cudaGraph_t graph;

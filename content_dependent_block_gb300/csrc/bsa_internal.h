@@ -39,6 +39,23 @@ struct SelectOpts {
     int32_t local = 0;                 // the own block is always selected
 };
 
+// Backward pass of the fine stage over per-query lists (bf16 in, fp32 out).
+struct BwdArgs {
+    const uint16_t *q, *kp, *vp, *out, *dout;
+    const int32_t *list;          // [bh][n][k]
+    int64_t bh, n, nb;
+    int32_t d, k, kb, causal;
+    float scale, scale_log2;      // softmax scale, and times log2(e)
+    float *dq, *dk, *dv;          // [bh][n][d]
+    float *lse, *dsum;            // [bh * n] workspace: log2-sum-exp, dO . O
+    int32_t *counts, *cursors;    // [bh * nb] workspace, zeroed
+    int32_t *offsets;             // [bh * nb + 1] workspace
+    int32_t *qlist;               // [bh * n * k] workspace: queries by (head, block)
+    int32_t *status;
+};
+bool fine_backward_supported(int32_t d, int32_t kb);   // one CTA of kb * d / 16 <= 512 threads
+cudaError_t launch_fine_backward(const BwdArgs &a, cudaStream_t st);
+
 // Records the one-line reason bsa_last_error() reports on this thread.
 void set_last_error(const char *msg);
 

@@ -192,6 +192,39 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k,
                               void *stream);
 
 /*
+ * Backward pass of the fine stage (page "sparse-attention-triton-bench",
+ * What's next: a backward pass through the sparse softmax-weighted sum over
+ * the selected blocks).  The selection is a discrete choice and is held
+ * fixed: the gradients flow through the fine stage only.  For query i with
+ * token set T_i (its listed blocks' keys; only j <= i under
+ * BSA_MASK_CAUSAL) and the output gradient dO:
+ *   D_i = dO_i . O_i,  dS_ij = p_ij (dO_i . v_j - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ *   dV_j = sum_i p_ij dO_i.
+ * The row statistics of the softmax are recomputed from q, k and the list.
+ *   q, k, v   [bh][n][d] bf16 (device), as given to the forward.
+ *   out       [bh][n][d] bf16: the forward's output O for this list.
+ *   dout      [bh][n][d] bf16: dO.
+ *   list, ld  per-query lists as the forward took them (q_group 1,
+ *             per_head 1, max_blocks <= 64; ascending ids, -1 padding).
+ *   mask      BSA_MASK_NONE or BSA_MASK_CAUSAL.
+ *   scale     softmax scale; <= 0 selects 1/sqrt(d).
+ *   dq, dk, dv  [bh][n][d] fp32 outputs (device); every element is written
+ *             (keys no query listed get zeros).
+ *   ws        device workspace of bsa_fine_backward_workspace_size() bytes.
+ * d in {64, 128}, key_block * d <= 8192; bf16 only.  Listed ids outside
+ * [0, nb) are skipped and
+ * reported as BSA_ERR_BAD_INDEX through bsa_get_device_status().
+ */
+size_t bsa_fine_backward_workspace_size(bsa_shape shape, bsa_list_desc ld);
+bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k,
+                             const void *v, const void *out, const void *dout,
+                             const int32_t *list, bsa_list_desc ld,
+                             bsa_mask mask, float scale, float *dq, float *dk,
+                             float *dv, void *ws, size_t ws_bytes,
+                             void *stream);
+
+/*
  * The whole dynamic forward: pool -> score + top-k -> fine attention, all
  * enqueued on `stream` (page "sparse-attention-triton-bench", Two-stage
  * block indexer).  bf16 only, non-causal (bsa_forward_ex below takes the causal and
