@@ -39,19 +39,24 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ float bf(uint16_t x) { return __uint_as_float(uint32_t(x) << 16); }
 
 // q . row for a bf16 row of D channels (16-byte loads) against fp32 q in
-// shared memory (every lane reads the same q: broadcast).
+// shared memory, read four channels at a time (every lane reads the same q:
+// broadcast).
 template <int D>
 __device__ __forceinline__ float dot_row(const float *q, const uint16_t *row) {
     float s = 0.f;
+    const float4 *q4 = reinterpret_cast<const float4 *>(q);
 #pragma unroll
     for (int c = 0; c < D; c += 8) {
         const uint4 u = __ldg(reinterpret_cast<const uint4 *>(row + c));
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            s = fmaf(q[c + 2 * e], bf16_low_half(w[e]), s);
-            s = fmaf(q[c + 2 * e + 1], bf16_high_half(w[e]), s);
-        }
+        const float4 qa = q4[c / 4], qb = q4[c / 4 + 1];
+        s = fmaf(qa.x, bf16_low_half(u.x), s);
+        s = fmaf(qa.y, bf16_high_half(u.x), s);
+        s = fmaf(qa.z, bf16_low_half(u.y), s);
+        s = fmaf(qa.w, bf16_high_half(u.y), s);
+        s = fmaf(qb.x, bf16_low_half(u.z), s);
+        s = fmaf(qb.y, bf16_high_half(u.z), s);
+        s = fmaf(qb.z, bf16_low_half(u.w), s);
+        s = fmaf(qb.w, bf16_high_half(u.w), s);
     }
     return s;
 }
@@ -66,7 +71,8 @@ __device__ __forceinline__ void block_keys(const BwdArgs &a, int32_t b, int64_t 
 
 template <int D>
 __global__ void __launch_bounds__(kQWarps * 32) bwd_query_kernel(const BwdArgs a) {
-    __shared__ float sq[kQWarps][D], sdo[kQWarps][D];
+    __shared__ __align__(16) float sq[kQWarps][D];
+    __shared__ __align__(16) float sdo[kQWarps][D];
     constexpr int CPL = D / 32;                        // channels per lane
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t h = blockIdx.y;
@@ -121,7 +127,8 @@ __global__ void __launch_bounds__(kQWarps * 32) bwd_query_kernel(const BwdArgs a
         a.lse[row] = lse;
         a.dsum[row] = dsum;
     }
-    // pass 2: dS per key (lanes over keys), dQ accumulated with lanes over channels
+    // pass 2: dS per key (lanes over keys), dQ accumulated with lanes over
+    // channels: lane owns channels [CPL lane, CPL lane + CPL)
     float dq[CPL];
 #pragma unroll
     for (int e = 0; e < CPL; ++e) dq[e] = 0.f;
@@ -141,15 +148,20 @@ __global__ void __launch_bounds__(kQWarps * 32) bwd_query_kernel(const BwdArgs a
                 const int cnt = int(i64min(32, jend - jb));
                 for (int u = 0; u < cnt; ++u) {
                     const float dsu = __shfl_sync(kFull, ds, u);
-                    const uint16_t *kr = kh + (jb + u) * D;
+                    const uint32_t *kr = reinterpret_cast<const uint32_t *>(kh + (jb + u) * D) +
+                                         lane * (CPL / 2);
 #pragma unroll
-                    for (int e = 0; e < CPL; ++e) dq[e] = fmaf(dsu, bf(kr[lane + 32 * e]), dq[e]);
+                    for (int e = 0; e < CPL / 2; ++e) {
+                        const uint32_t w = __ldg(kr + e);
+                        dq[2 * e] = fmaf(dsu, bf16_low_half(w), dq[2 * e]);
+                        dq[2 * e + 1] = fmaf(dsu, bf16_high_half(w), dq[2 * e + 1]);
+                    }
                 }
             }
         }
     }
 #pragma unroll
-    for (int e = 0; e < CPL; ++e) a.dq[row * D + lane + 32 * e] = dq[e] * a.scale;
+    for (int e = 0; e < CPL; ++e) a.dq[row * D + lane * CPL + e] = dq[e] * a.scale;
 }
 
 // grid: (ceil(n * k / 256), bh)
