@@ -98,6 +98,7 @@ struct Cfg {
     static constexpr int kNQ = D == 64 ? 3 : 2;            // Q stages
     static constexpr int kNKV = D == 64 ? 3 : 2;           // K/V buffers (items in flight)
     static constexpr int kMS = D == 64 ? 2 : 1;            // merge stages per merge warp
+    static constexpr int kNO = D == 64 ? 4 : 2;            // O and P buffers in TMEM
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int oQ = 0;
@@ -118,10 +119,10 @@ struct Cfg {
         bSFull = bKvFree + kNKV,
         bSFree = bSFull + 2,
         bPFull = bSFree + 2,
-        bPFree = bPFull + 2,
-        bOFull = bPFree + 2,
-        bOFree = bOFull + 2,
-        bMlFull = bOFree + 2,
+        bPFree = bPFull + kNO,
+        bOFull = bPFree + kNO,
+        bOFree = bOFull + kNO,
+        bMlFull = bOFree + kNO,
         bTiFull = bMlFull + kNT,
         bTiFree = bTiFull + kNT,
         bItFull = bTiFree + kNT,
@@ -133,7 +134,8 @@ struct Cfg {
     static constexpr int kTotal = oMisc + 64 + 1024;
     static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t cO = 2 * kB;                 // O[j] at cO + j*D; S[j] at j*64
-    static constexpr uint32_t cP = 2 * kB + 2 * D;         // P[j] (bf16 pairs) at cP + j*32
+    static constexpr uint32_t cP = 2 * kB + kNO * D;       // P[j] (bf16 pairs) at cP + j*32
+    static_assert(cP + kNO * 32 <= kTmemCols, "tensor memory");
 };
 static_assert(Cfg<64>::kTotal <= 227 * 1024, "shared memory (d = 64)");
 static_assert(Cfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
@@ -292,6 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bars + C::bSFull + i, 1);
             tc::mbar_init(bars + C::bSFree + i, kTile);
+        }
+        for (int i = 0; i < C::kNO; ++i) {
             tc::mbar_init(bars + C::bPFull + i, kTile);
             tc::mbar_init(bars + C::bPFree + i, 1);
             tc::mbar_init(bars + C::bOFull + i, 1);
@@ -526,9 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         for (uint32_t spin = 0;; ++spin) {
             bool progressed = false;
             if (g2 < g1) {
-                const int j = g2 & 1;
-                if (probe(bars + C::bPFull + j, (g2 >> 1) & 1) &&
-                    (g2 < 2 || probe(bars + C::bOFree + j, ((g2 >> 1) - 1) & 1))) {
+                const int j = g2 % C::kNO;                // P and O buffer of tile g2
+                if (probe(bars + C::bPFull + j, (g2 / C::kNO) & 1) &&
+                    (g2 < C::kNO || probe(bars + C::bOFree + j, ((g2 / C::kNO) - 1) & 1))) {
                     tc::tc_fence_after();
                     const int ib = t_ib[g2 & 3];
                     if (tc::elect_one()) {
@@ -614,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         const int row = quad * 32 + lane;
         const uint32_t lane_off = uint32_t(quad * 32) << 16;
         for (int g = 0;; ++g) {
-            const int slot = g % kNT, j = g & 1;
+            const int slot = g % kNT, j = g & 1, jp = g % C::kNO;   // S buffer, P buffer
             if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
             const int32_t end_flag = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
             if (end_flag) break;
@@ -657,11 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     l += p0 + p1;
                     pk[c >> 1] = pack_bf16x2(p0, p1);
                 }
-                if (c0 == 0 && g >= 2 && !tc::mbar_wait(bars + C::bPFree + j, ((g >> 1) - 1) & 1, status)) {
+                if (c0 == 0 && g >= C::kNO &&
+                    !tc::mbar_wait(bars + C::bPFree + jp, ((g / C::kNO) - 1) & 1, status)) {
                     ok = false;
                     break;
                 }
-                tc::tmem_st16(tmem + C::cP + uint32_t(j * 32 + (c0 >> 1)) + lane_off, pk);
+                tc::tmem_st16(tmem + C::cP + uint32_t(jp * 32 + (c0 >> 1)) + lane_off, pk);
             }
             if (!ok) break;
             // (m, l) live with the tile slot, which the gather group reuses
@@ -670,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::mbar_arrive(bars + C::bMlFull + slot);
             tc::tmem_st_wait();
             tc::tc_fence_before();
-            tc::mbar_arrive(bars + C::bPFull + j);
+            tc::mbar_arrive(bars + C::bPFull + jp);
         }
     } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
         // ------------------------------------------------------- epilogue
@@ -686,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         uint8_t *eb = sm + C::oEpi + (warp - kWarpEpi) * 2048;
         const int srow = lane >> 2, spiece = lane & 3;      // store phase: rows 8i + srow
         for (int g = 0;; ++g) {
-            const int slot = g % kNT, j = g & 1;
+            const int slot = g % kNT, jo = g % C::kNO;             // O buffer
             if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
             const int32_t x_end = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
             if (x_end) break;
@@ -694,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const int32_t x_rg = reinterpret_cast<volatile TileInfo *>(ti + slot)->rg;
             const int32_t x_qbase = reinterpret_cast<volatile TileInfo *>(ti + slot)->qbase;
             const int32_t x_roff = reinterpret_cast<volatile TileInfo *>(ti + slot)->roff;
-            if (!tc::mbar_wait(bars + C::bOFull + j, (g >> 1) & 1, status)) break;
+            if (!tc::mbar_wait(bars + C::bOFull + jo, (g / C::kNO) & 1, status)) break;
             if (!tc::mbar_wait(bars + C::bMlFull + slot, (g / kNT) & 1, status)) break;
             tc::tc_fence_after();
             const float2 mlv = ml[slot * kTile + row];
@@ -715,12 +720,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 64) {
                 uint32_t ov[2][32];
-                tc::tmem_ld32(tmem + C::cO + uint32_t(j * D + c0) + lane_off, ov[0]);
-                tc::tmem_ld32(tmem + C::cO + uint32_t(j * D + c0 + 32) + lane_off, ov[1]);
+                tc::tmem_ld32(tmem + C::cO + uint32_t(jo * D + c0) + lane_off, ov[0]);
+                tc::tmem_ld32(tmem + C::cO + uint32_t(jo * D + c0 + 32) + lane_off, ov[1]);
                 tc::tmem_ld_wait();
                 if (c0 + 64 == D) {
                     tc::tc_fence_before();
-                    tc::mbar_arrive(bars + C::bOFree + j);
+                    tc::mbar_arrive(bars + C::bOFree + jo);
                 }
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
