@@ -368,9 +368,13 @@ bool fine_uses_bm(const bsa_shape &shape, const int32_t *list, const bsa_list_de
 
 size_t bsa_fine_attention_workspace_size(bsa_shape shape, bsa_list_desc ld, bsa_mask mask) {
     if (check_shape(shape) != BSA_OK || check_key_block(ld.key_block) != BSA_OK) return 0;
-    // a non-null list is assumed; the query-major path needs no workspace
-    if (!bm_lists(shape, ld, mask)) return 0;
-    return bm_layout(shape, ld.key_block, ld.max_blocks, 0).total;
+    // a non-null list is assumed (max_blocks 0 stands for no list)
+    if (bm_lists(shape, ld, mask)) return bm_layout(shape, ld.key_block, ld.max_blocks, 0).total;
+    // static tile lists on the tensor cores: optional, lets them run one pass
+    if (shape.dtype == BSA_BF16 && (shape.d == 64 || shape.d == 128) && ld.key_block == 64 &&
+        (ld.q_group == 128 || ld.max_blocks == 0) && ld.max_blocks <= 512 && shape.bh <= 65535)
+        return bsa::fine_static_tc_workspace(shape.bh, shape.n, ld.key_block);
+    return 0;   // the query-major path needs none
 }
 
 bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, const void *v,
@@ -426,8 +430,16 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
     a.sliding = mask.sliding;
     a.scale_log2 = sl2;
     a.status = status;
-    if (bsa::fine_static_tc_supported(a, shape.dtype))
+    if (bsa::fine_static_tc_supported(a, shape.dtype)) {
+        // with the optional workspace: block key norms, then one pass with a score bound
+        const size_t need_s = bsa::fine_static_tc_workspace(shape.bh, shape.n, ld.key_block);
+        if (ws != nullptr && ws_bytes >= need_s && aligned(ws, 256)) {
+            a.kmax = static_cast<float *>(ws);
+            a.flags = reinterpret_cast<int32_t *>(static_cast<char *>(ws) +
+                                                  round_up(size_t(shape.bh) * size_t(a.nb) * 4, 256));
+        }
         return launched(bsa::launch_fine_static_tc(a, st), "fine attention (tensor-core tiles) launch");
+    }
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
 }
 

@@ -29,6 +29,11 @@ struct FineArgs {
     int32_t sliding;
     float scale_log2;      // softmax scale * log2(e)
     int32_t *status;       // device status word
+    // tensor-core static path, optional workspace: with both set, one pass
+    // with a per-row bound on the scores, then the exact two passes only for
+    // the tiles the bound did not serve
+    float *kmax;           // [bh][nb] largest key norm of each block
+    int32_t *flags;        // [bh][ceil(n / 128)] tiles to redo
 };
 
 // Options of the dynamic selection (bsa_select in bsa.h).
@@ -148,6 +153,8 @@ cudaError_t launch_fine_query_major(const FineArgs &a, int32_t dtype,
 // 64-key blocks, one list row per 128-query tile (or no list), at most 512
 // listed blocks per row.
 bool fine_static_tc_supported(const FineArgs &a, int32_t dtype);
+// Workspace (bytes) that lets the static tensor-core path run one pass.
+size_t fine_static_tc_workspace(int64_t bh, int64_t n, int32_t kb);
 cudaError_t launch_fine_static_tc(const FineArgs &a, cudaStream_t st);
 
 }  // namespace bsa

@@ -16,7 +16,16 @@
 // softmax is exact and two-pass: pass 0 computes the row maxima over all
 // listed blocks, pass 1 recomputes the scores, forms p = exp2(s * scale *
 // log2 e - m) once, accumulates l and O += P V in tensor memory.  O is never
-// rescaled, at the price of computing Q K^T twice.  Stage-use u runs over
+// rescaled, at the price of computing Q K^T twice.
+//
+// With a workspace the first pass is skipped: any m >= the row maximum gives
+// the same softmax, so each row takes the bound m = |q_i| max_j |k_j| scale
+// log2 e over the tile's listed blocks (the key norms come from a small
+// kernel run first) and does pass 1 only.  That is exact up to rounding while
+// the bound exceeds the true maximum by less than ~100 (p stays far above
+// the smallest fp32 and bf16 normals); a tile with a row beyond that is
+// flagged and recomputed by the two-pass kernel in a second launch whose
+// other CTAs return at once.  Stage-use u runs over
 // u < ns (pass 0, superblock u) and ns <= u < 2 ns (pass 1, superblock
 // u - ns), ns = ceil(listed / 2).
 //
@@ -176,7 +185,34 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&sv)[32], uint32_t ad
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
+// Largest key norm of each 64-key block: one CTA of 64 threads per (block, head).
 template <int D>
+__global__ void __launch_bounds__(64) key_norm_kernel(const uint16_t *__restrict__ k, int64_t n,
+                                                       int64_t nb, float *__restrict__ kmax) {
+    const int64_t h = blockIdx.y, b = blockIdx.x, j = b * kB + threadIdx.x;
+    float s = 0.f;
+    if (j < n) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(k + (h * n + j) * D);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 u = __ldg(row + c);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+                s = fmaf(lo, lo, fmaf(hi, hi, s));
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(kFull, s, o));
+    __shared__ float wmax[2];
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) kmax[h * nb + b] = sqrtf(fmaxf(wmax[0], wmax[1]));
+}
+
+template <int D, bool kOnePass>
 __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const FineArgs a) {
@@ -192,10 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t *status = a.status;
-    // A wait elsewhere already ran out: the whole CTA leaves together.
-    if (__syncthreads_or(*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout)) return;
+    const int64_t tile = int64_t(blockIdx.y) * gridDim.x + blockIdx.x;
+    // A wait elsewhere already ran out, or (second launch) the one-pass launch
+    // served this tile: the whole CTA leaves together.
+    if (__syncthreads_or(*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout ||
+                         (!kOnePass && a.flags != nullptr && a.flags[tile] == 0)))
+        return;
     const int64_t h = blockIdx.y;
     const int64_t i0 = int64_t(blockIdx.x) * kTile;
+    float *kmax_s = reinterpret_cast<float *>(sm + C::oMisc + 32);   // largest key norm of the list
 
     // the tile's list, compacted to valid ids (padding and bad ids dropped)
     if (warp == 0) {
@@ -223,6 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             cnt = min(cnt, kMaxList);
         }
         if (lane == 0) *nlist_s = cnt;
+        if (kOnePass) {
+            __syncwarp();
+            float km = 0.f;
+            for (int t = lane; t < cnt; t += 32) km = fmaxf(km, __ldg(a.kmax + h * a.nb + list_s[t]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) km = fmaxf(km, __shfl_xor_sync(kFull, km, o));
+            if (lane == 0) *kmax_s = km;
+        }
     }
     if (threadIdx.x == 0) {
         tc::mbar_init(bars + C::bQFull, 1);
@@ -256,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
     const uint32_t tmem = *tmem_slot;
     const int nl = *nlist_s;
     const int ns = (nl + 1) >> 1;                     // superblocks
+    const int np0 = kOnePass ? 0 : ns;                // pass-0 stage-uses
     // first key of block `blk` of the list; past the end: keys beyond the
     // sequence (loaded as zeros, never admitted)
     auto block_key0 = [&](int blk) -> int64_t {
@@ -270,8 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             for (int sub = 0; sub < C::kSub; ++sub)
                 tc::tma_load_3d(sm + C::oQ + sub * kTile * 128, &tm_q, bars + C::bQFull, sub * 64,
                                 int32_t(i0), int32_t(h));
-            for (int u = 0; u < 2 * ns; ++u) {
-                const int sb = u >= ns ? u - ns : u, s = u % C::kKStages;
+            for (int u = 0; u < np0 + ns; ++u) {
+                const int sb = u >= np0 ? u - np0 : u, s = u % C::kKStages;
                 if (u >= C::kKStages &&
                     !tc::mbar_wait(bars + C::bKEmpty + s, ((u / C::kKStages) - 1) & 1, status))
                     break;
@@ -315,9 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
         const uint32_t aq = tc::smem_u32(sm + C::oQ);
         // O += P_sb V_sb, P (bf16) in the first 64 columns of the superblock's S buffer
         auto issue_pv = [&](int sb) {
-            const int u = sb + ns, j = u % C::kS, r = sb % C::kVStages;
+            const int u = sb + np0, j = u % C::kS, r = sb % C::kVStages;
             bool w = tc::mbar_wait(bars + C::bVFull + r, (sb / C::kVStages) & 1, status);
-            w = w && tc::mbar_wait(bars + C::bPFull + j, (u / C::kS - pass0_uses(ns, j, C::kS)) & 1,
+            w = w && tc::mbar_wait(bars + C::bPFull + j, (u / C::kS - pass0_uses(np0, j, C::kS)) & 1,
                                    status);
             ok = __all_sync(kFull, w);
             if (!ok) return;
@@ -335,15 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             }
             __syncwarp();
         };
-        for (int u = 0; ok && u < 2 * ns + kLag; ++u) {
-            if (u < 2 * ns) {
+        for (int u = 0; ok && u < np0 + ns + kLag; ++u) {
+            if (u < np0 + ns) {
                 const int s = u % C::kKStages, j = u % C::kS, prev = u - C::kS;
                 bool w = tc::mbar_wait(bars + C::bKFull + s, (u / C::kKStages) & 1, status);
                 // the buffer's last use: pass-0 scores read, or the P.V of its P done
                 if (w && prev >= 0)
-                    w = prev < ns ? tc::mbar_wait(bars + C::bSFree + j, (prev / C::kS) & 1, status)
-                                  : tc::mbar_wait(bars + C::bPvDone + j,
-                                                  (prev / C::kS - pass0_uses(ns, j, C::kS)) & 1, status);
+                    w = prev < np0 ? tc::mbar_wait(bars + C::bSFree + j, (prev / C::kS) & 1, status)
+                                   : tc::mbar_wait(bars + C::bPvDone + j,
+                                                   (prev / C::kS - pass0_uses(np0, j, C::kS)) & 1, status);
                 ok = __all_sync(kFull, w);
                 if (!ok) break;
                 tc::tc_fence_after();
@@ -362,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 __syncwarp();
             }
             // P.V kLag stage-uses behind the scores
-            if (u - kLag >= ns) issue_pv(u - kLag - ns);
+            if (u - kLag >= np0) issue_pv(u - kLag - np0);
         }
     } else {
         // ----------------------------------------- softmax and epilogue
@@ -374,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
         float m2 = -INFINITY, l = 0.f;
         bool ok = true;
         // pass 0: masked row maxima of this group's superblocks
-        for (int u = g; ok && u < ns; u += kGroups) {
+        for (int u = g; ok && u < np0; u += kGroups) {
             const int j = u % C::kS;
             if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kS) & 1, status)) {
                 ok = false;
@@ -399,15 +449,37 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
             tc::mbar_arrive(bars + C::bSFree + j);
             m2 = fmaxf(m2, mraw * a.scale_log2);                     // scale > 0 keeps the order
         }
-        // the row maximum over the groups (every group thread passes here once)
-        m_part[g * kTile + row] = m2;
-        tc::named_bar_sync(kBarGroups, kGroups * 128);
+        float mm;
+        if (kOnePass) {
+            // the row's bound |q_i| max |k| scale log2 e on every admitted score
+            float qq = 0.f;
+            if (i < a.n) {
+                const uint4 *qr = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.q) +
+                                                                  (h * a.n + i) * D);
+#pragma unroll 4
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 u = __ldg(qr + c);
+                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-        for (int o = 0; o < kGroups; ++o) m2 = fmaxf(m2, m_part[o * kTile + row]);
-        const float mm = m2 == -INFINITY ? 0.f : m2;                  // a row with no admitted key
+                    for (int e = 0; e < 4; ++e) {
+                        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+                        qq = fmaf(lo, lo, fmaf(hi, hi, qq));
+                    }
+                }
+            }
+            mm = sqrtf(qq) * *kmax_s * a.scale_log2;
+        } else {
+            // the row maximum over the groups (every group thread passes here once)
+            m_part[g * kTile + row] = m2;
+            tc::named_bar_sync(kBarGroups, kGroups * 128);
+#pragma unroll
+            for (int o = 0; o < kGroups; ++o) m2 = fmaxf(m2, m_part[o * kTile + row]);
+            mm = m2 == -INFINITY ? 0.f : m2;                          // a row with no admitted key
+        }
+        float mtrue = -INFINITY;                                      // one pass: the actual maximum (raw)
         // pass 1: p, l and P of this group's superblocks
-        for (int u = ns + (g + kGroups - ns % kGroups) % kGroups; ok && u < 2 * ns; u += kGroups) {
-            const int sb = u - ns, j = u % C::kS;
+        for (int u = np0 + (g + kGroups - np0 % kGroups) % kGroups; ok && u < np0 + ns; u += kGroups) {
+            const int sb = u - np0, j = u % C::kS;
             if (!tc::mbar_wait(bars + C::bSFull + j, (u / C::kS) & 1, status)) {
                 ok = false;
                 break;
@@ -424,8 +496,11 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
                 const bool full = c < 2 ? fa : fb;
                 const int64_t jc = (c < 2 ? j0a : j0b) + (c & 1) * 32;
                 uint32_t pk[16];
+                const uint32_t adm = full ? 0xffffffffu : admitted_bits(a, i, jc);
+                if (kOnePass)
+                    mtrue = fmaxf(mtrue, full ? chunk_max<false>(sv, 0u) : chunk_max<true>(sv, adm));
                 l += full ? chunk_exp<false>(sv, 0u, a.scale_log2, mm, pk)
-                          : chunk_exp<true>(sv, admitted_bits(a, i, jc), a.scale_log2, mm, pk);
+                          : chunk_exp<true>(sv, adm, a.scale_log2, mm, pk);
                 // P over scores already read: columns [16 c, 16 c + 16) of the buffer
                 tc::tmem_st16(tmem + uint32_t(j * kSB + c * 16) + lane_off, pk);
             }
@@ -439,6 +514,16 @@ __global__ void __launch_bounds__(kThreads, 1) fine_static_tc_kernel(
         l = 0.f;
 #pragma unroll
         for (int o = 0; o < kGroups; ++o) l += l_part[o * kTile + row];
+        if (kOnePass) {
+            // did the bound serve every row?  Else the second launch redoes the tile.
+            m_part[g * kTile + row] = mtrue;
+            tc::named_bar_sync(kBarGroups, kGroups * 128);
+#pragma unroll
+            for (int o = 0; o < kGroups; ++o) mtrue = fmaxf(mtrue, m_part[o * kTile + row]);
+            const float gap = mm - mtrue * a.scale_log2;
+            const bool bad_row = i < a.n && mtrue > -INFINITY && !(gap <= 100.f && l > 0.f && l < INFINITY);
+            if (g == 0 && __any_sync(kFull, bad_row) && lane == 0) a.flags[tile] = 1;
+        }
         // epilogue: O / l; group g writes the 32-column chunks c = g mod kGroups
         if (ok && nl > 0 && tc::mbar_wait(bars + C::bOFull, 0, status)) {
             tc::tc_fence_after();
@@ -502,16 +587,34 @@ bool make_map(CUtensorMap *m, const void *base, int64_t bh, int64_t n, int d, in
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-cudaError_t launch_d(const FineArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, cudaStream_t st) {
+template <int D, bool kOnePass>
+cudaError_t launch_kernel(const FineArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                          const CUtensorMap &mv, cudaStream_t st) {
     using C = SCfg<D>;
-    auto kern = fine_static_tc_kernel<D>;
+    auto kern = fine_static_tc_kernel<D, kOnePass>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kTotal);
     if (e != cudaSuccess) return e;
     const dim3 grid(unsigned((a.n + kTile - 1) / kTile), unsigned(a.bh));
     kern<<<grid, kThreads, C::kTotal, st>>>(mq, mk, mv, a);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const FineArgs &a, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, cudaStream_t st) {
+    if (a.kmax == nullptr || a.flags == nullptr) {
+        FineArgs b = a;
+        b.flags = nullptr;                   // every tile, two passes
+        return launch_kernel<D, false>(b, mq, mk, mv, st);
+    }
+    key_norm_kernel<D><<<dim3(unsigned(a.nb), unsigned(a.bh)), kB, 0, st>>>(
+        static_cast<const uint16_t *>(a.k), a.n, a.nb, a.kmax);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = a.bh * ((a.n + kTile - 1) / kTile);
+    if ((e = cudaMemsetAsync(a.flags, 0, size_t(tiles) * sizeof(int32_t), st)) != cudaSuccess) return e;
+    if ((e = launch_kernel<D, true>(a, mq, mk, mv, st)) != cudaSuccess) return e;
+    return launch_kernel<D, false>(a, mq, mk, mv, st);      // flagged tiles only
 }
 
 }  // namespace
@@ -520,6 +623,11 @@ bool fine_static_tc_supported(const FineArgs &a, int32_t dtype) {
     return dtype == 0 /*bf16*/ && (a.d == 64 || a.d == 128) && a.kb == kB &&
            (a.list == nullptr || a.q_group == kTile) && a.bh <= 65535 &&
            (a.list == nullptr ? a.nb <= kMaxList : a.max_blocks <= kMaxList);
+}
+
+size_t fine_static_tc_workspace(int64_t bh, int64_t n, int32_t kb) {
+    const int64_t nb = (n + kb - 1) / kb, tiles = (n + kTile - 1) / kTile;
+    return size_t(bh) * size_t(nb) * 4 + 256 + size_t(bh) * size_t(tiles) * 4;
 }
 
 cudaError_t launch_fine_static_tc(const FineArgs &a, cudaStream_t st) {

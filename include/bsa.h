@@ -180,6 +180,13 @@ bsa_status bsa_coarse_topk_ex(bsa_shape shape, const void *q, const float *kbar,
  *   out      [bh][n][d] of shape.dtype (device); a query whose list admits
  *            no key gets zeros.
  *   ws       device workspace of bsa_fine_attention_workspace_size() bytes.
+ *            Per-query lists need it.  For static tile lists (and no list)
+ *            of bf16 inputs on the tensor-core path it is optional: with it
+ *            the kernel first takes each block's largest key norm and runs
+ *            one pass with a per-row bound on the scores (the exact two-pass
+ *            kernel redoes only the tiles the bound does not serve); without
+ *            it (NULL) every tile runs two passes.  The results agree to
+ *            rounding.
  * A listed id outside [0, nb) is skipped and reported as BSA_ERR_BAD_INDEX
  * through bsa_get_device_status().
  */

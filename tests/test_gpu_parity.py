@@ -270,6 +270,56 @@ def test_static_tc_sliding_bf16(n, d, win):
     assert bsa.device_status() == 0
 
 
+def test_static_tc_bound_fallback_bf16():
+    """Rows whose score bound |q| max|k| overshoots the true maximum by far
+    (a large query component on a channel where every key is zero) are
+    redone by the exact two-pass launch; the other tiles keep the one-pass
+    result."""
+    import torch
+    n, d, W = 1000, 64, 300
+    w = workloads.Workload("fb", bh=2, n=n, d=d, dtype="bf16", kind="dynamic", key_block=64,
+                           topk=4, seed=17)
+    t = workloads.generate(w)
+    qf = workloads.bf16_bits_to_f32(t.q).copy()
+    kf = workloads.bf16_bits_to_f32(t.k).copy()
+    qf[0, 128:384, 0] = 400.0          # two tiles of head 0: bound ~ 400 x 8 / 8 x log2 e above
+    kf[:, :, 0] = 0.0
+    t.q[...] = workloads.bf16_bits_rne(qf)
+    t.k[...] = workloads.bf16_bits_rne(kf)
+    q, k, v = (parity.to_device(getattr(t, x), "bf16") for x in "qkv")
+    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=W)
+    lst, _, _ = bsa.static_blocks(n, 128, 64, m)
+    out = bsa.fine_attention(q, k, v, torch.from_numpy(lst).cuda(), key_block=64, q_group=128,
+                             per_head=False, mask=m)
+    rows = oracle.all_rows(2, n)
+    ref, _, _ = oracle.masked(t.q, t.k, t.v, oracle.MASK_SLIDING, rows, W=W)
+    parity.assert_close(parity.from_device(out).reshape(-1, d), ref, "bf16", "bound fallback")
+    assert bsa.device_status() == 0
+
+
+def test_static_tc_without_workspace_runs_two_passes_bf16():
+    import ctypes
+    import torch
+    n, d = 1100, 128
+    t, (q, k, v) = _small(1, n, d, seed=23)
+    m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, 40, 300)
+    lst, _, _ = bsa.static_blocks(n, 128, 64, m)
+    dl = torch.from_numpy(lst).cuda()
+    out = torch.empty_like(q)
+    L = bsa.lib()
+    ld = bsa.ListDesc(128, 64, lst.shape[1], 0)
+    assert L.bsa_fine_attention_workspace_size(bsa._shape(q), ld, m) > 0
+    bsa._check(L.bsa_fine_attention(bsa._shape(q), bsa._ptr(q), bsa._ptr(k), bsa._ptr(v),
+                                    bsa._ptr(dl), ld, m, 0.0, bsa._ptr(out), None, 0,
+                                    bsa._stream()))
+    one = bsa.fine_attention(q, k, v, dl, key_block=64, q_group=128, per_head=False, mask=m)
+    rows = oracle.all_rows(1, n)
+    ref, _, _ = oracle.masked(t.q, t.k, t.v, oracle.MASK_LOCAL_GLOBAL, rows, w=40, s=300)
+    parity.assert_close(parity.from_device(out).reshape(-1, d), ref, "bf16", "two passes")
+    parity.assert_close(parity.from_device(one).reshape(-1, d), ref, "bf16", "one pass")
+    assert bsa.device_status() == 0
+
+
 def test_static_tc_null_list_is_dense_bf16():
     t, (q, k, v) = _small(2, 700, 64, seed=11)
     out = bsa.fine_attention(q, k, v, None, key_block=64)
