@@ -36,6 +36,7 @@
 // so two blocks can only swap when their scores agree to that precision.
 // The register list is kept sorted by a compare-exchange pass (min/max).
 #include <climits>
+#include <type_traits>
 
 #include <cudaTypedefs.h>
 
@@ -285,19 +286,24 @@ __global__ void __launch_bounds__(kThreads, 2) coarse_topk_tc_kernel(
                     uint32_t v[32];
                     tc::tmem_ld32(tmem + (uint32_t(quad * 32) << 16) + uint32_t(buf * kChunk + j * 32), v);
                     tc::tmem_ld_wait();
+                    // queue the keys that beat the current k-th key (no branches); a
+                    // group of 32 valid columns (the common case) skips the bound check
+                    auto filter = [&](auto whole) {
 #pragma unroll
-                    for (int hf = 0; hf < 32 / kSlice; ++hf) {
-                        // queue the keys that beat the current k-th key (no branches)
-                        const uint32_t thr = L[KMAX - 1];
+                        for (int hf = 0; hf < 32 / kSlice; ++hf) {
+                            const uint32_t thr = L[KMAX - 1];
 #pragma unroll
-                        for (int e = 0; e < kSlice; ++e) {
-                            const int x = hf * kSlice + e;
-                            const uint32_t key = score_key(__uint_as_float(v[x]), col0 + x, key_mask);
-                            qu[cnt * kEpi] = key;
-                            cnt += (x < lim && key > thr) ? 1 : 0;
+                            for (int e = 0; e < kSlice; ++e) {
+                                const int x = hf * kSlice + e;
+                                const uint32_t key = score_key(__uint_as_float(v[x]), col0 + x, key_mask);
+                                qu[cnt * kEpi] = key;
+                                cnt += ((decltype(whole)::value || x < lim) && key > thr) ? 1 : 0;
+                            }
+                            if (__any_sync(kFull, cnt >= 16)) drain();
                         }
-                        if (__any_sync(kFull, cnt >= 16)) drain();
-                    }
+                    };
+                    if (__all_sync(kFull, lim >= 32)) filter(std::true_type{});
+                    else filter(std::false_type{});
                 }
             }
             tc::tc_fence_before();
