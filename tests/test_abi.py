@@ -118,6 +118,37 @@ def test_select_options_are_checked(L):
     assert L.bsa_forward_workspace_size(s, 64, 4) == need
 
 
+def test_backward_rejects_bad_arguments(L):
+    s = _shape(n=256)
+    ld = bsa.ListDesc(1, 64, 4, 1)
+    need = L.bsa_fine_backward_workspace_size(s, ld)
+    assert need > 0
+    none = bsa.mask_struct()
+    args = lambda **kw: [kw.get("shape", s), FAKE, FAKE, FAKE, FAKE, FAKE, kw.get("lst", FAKE),
+                         kw.get("ld", ld), kw.get("mask", none), 0.0, kw.get("dq", FAKE), FAKE,
+                         FAKE, kw.get("ws", FAKE), kw.get("wsn", need), None]
+    assert L.bsa_fine_backward(*args(shape=_shape(n=256, dtype=bsa.FP32))) == 2
+    assert L.bsa_fine_backward(*args(shape=_shape(n=256, d=96))) == 2
+    assert L.bsa_fine_backward(*args(ld=bsa.ListDesc(128, 64, 4, 0))) == 2      # static lists
+    assert L.bsa_fine_backward(*args(mask=bsa.mask_struct(bsa.MASK_SLIDING, sliding=8))) == 2
+    assert L.bsa_fine_backward(*args(lst=None)) == 1
+    assert L.bsa_fine_backward(*args(dq=MISALIGNED)) == 7
+    assert L.bsa_fine_backward(*args(wsn=need - 1)) == 4
+    assert L.bsa_fine_backward(*args(shape=_shape(n=256, d=128), ld=bsa.ListDesc(1, 128, 4, 1))) == 2
+    assert L.bsa_fine_backward_workspace_size(s, bsa.ListDesc(128, 64, 4, 0)) == 0
+
+
+def test_static_path_workspace_is_optional_and_sized(L):
+    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=256)
+    s = _shape(bh=2, n=1000, d=128)
+    tiles, nb = -(-1000 // 128), -(-1000 // 64)
+    need = L.bsa_fine_attention_workspace_size(s, bsa.ListDesc(128, 64, 9, 0), m)
+    assert need >= 2 * nb * 4 + 2 * tiles * 4
+    # fp32 and other tile heights take the query-major kernel: no workspace
+    assert L.bsa_fine_attention_workspace_size(_shape(dtype=bsa.FP32), bsa.ListDesc(128, 64, 9, 0), m) == 0
+    assert L.bsa_fine_attention_workspace_size(s, bsa.ListDesc(16, 64, 9, 0), m) == 0
+
+
 def test_static_blocks_rejects_bad_arguments(L):
     m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=0)
     assert L.bsa_static_max_blocks(100, 16, 16, m) < 0
