@@ -168,3 +168,12 @@ def test_backward_equals_autograd_of_masked_attention(causal):
     for got, ref in ((dq, Q.grad), (dk, K.grad), (dv, V.grad)):
         np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-11)
     assert (dq.reshape(-1, d)[(idx < 0).all(1)] == 0).all()  # empty rows: no gradient
+
+
+def test_budgets_outside_the_list_width_are_clamped():
+    rng = np.random.default_rng(3)
+    s = rng.standard_normal((2 * 50, 7))
+    rows = np.arange(100, dtype=np.int64)
+    got = oracle.select(s, rows, 50, 8, 4, head_k=np.array([-2, 9], dtype=np.int32))
+    assert (got[:50] == -1).all()                                   # clamped to 0
+    np.testing.assert_array_equal(got[50:], oracle.topk(s[50:], 4)[0])   # clamped to k
