@@ -369,12 +369,20 @@ def run_static(args, w, device, dist):
     torch.cuda.synchronize(device)
     ms = statistics.median(a.elapsed_time(b) for a, b in evs)
     pairs = metrics.sliding_pairs(w.n, w.sliding) * w.bh
+    achieved = metrics.pairs_flops(pairs, w.d) / (ms * 1e-3) / 1e12
+    peaks = measured_peaks()
     status = bsa.device_status()
     if dist is not None:
         dist.destroy_process_group()
     print(json.dumps({
         "metric": "static sliding-window fine stage, effective TFLOP/s on admitted pairs",
-        "value": metrics.pairs_flops(pairs, w.d) / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "value": achieved, "unit": "TFLOP/s",
+        "roofline": {"kernel": "static fine stage: block key norms + one-pass tensor-core kernel "
+                               "(+ the two-pass relaunch for flagged tiles)",
+                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": f"bf16_tflops burst, {peaks['source']}",
+                     "traffic": kernel_traffic("fine_static_tc", w.name)},
         "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
         "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "sliding": w.sliding,
