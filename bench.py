@@ -326,6 +326,36 @@ def reference_arm(args, rank, world, w):
     return 0
 
 
+def static_oracle_sample(w, t, seconds: float):
+    """The oracle's sliding-window attention (plain masked definition) on a
+    seeded row sample, repeated until about `seconds` of CPU time; returns
+    (TFLOP/s on admitted pairs, rows per pass, seconds, cores, description)."""
+    import numpy as np
+    import oracle
+    cores = oracle.num_threads()
+
+    def run(count):
+        rows = workloads.sample_rows(w.bh, w.n, max(1, count // w.bh), seed=7)
+        t0 = time.perf_counter()
+        oracle.masked(t.q, t.k, t.v, oracle.MASK_SLIDING, rows, W=w.sliding)
+        keys = np.minimum(rows % w.n + 1, w.sliding)
+        return rows.size, time.perf_counter() - t0, metrics.pairs_flops(int(keys.sum()), w.d)
+
+    r0, t0, _ = run(16 * w.bh)
+    count = int(min(w.bh * w.n, 8192, max(r0, r0 * seconds / max(t0, 1e-3))))
+    rows = secs = flops = 0
+    passes = 0
+    while passes == 0 or (secs < seconds and passes < 64):
+        r, dt, fl = run(count)
+        rows += r
+        secs += dt
+        flops += fl
+        passes += 1
+    desc = (f"{rows // passes} of {w.bh * w.n} query rows (seeded sample) x {passes} passes, "
+            f"dense masked attention over i-W < j <= i per row, fp64, {cores} threads")
+    return flops / secs / 1e12, rows // passes, secs, cores, desc
+
+
 def run_static(args, w, device, dist):
     """A sliding-window workload: the static-list fine stage on the tensors
     of the dynamic workload of the same shape (one launch per step); with
@@ -388,7 +418,11 @@ def run_static(args, w, device, dist):
         "config": {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "sliding": w.sliding,
                    "key_block": w.key_block, "q_group": w.q_group, "inputs": w.note,
                    "timing": "median of CUDA-event times; inputs (805 MB) larger than L2"},
-        "admitted_pairs": pairs, "device_status": status}), flush=True)
+        "admitted_pairs": pairs, "device_status": status,
+        **({} if args.no_cpu_baseline else {"cpu_baseline": dict(zip(
+            ("value", "rows", "seconds", "cores", "sample"),
+            static_oracle_sample(w, t, args.cpu_seconds)), unit="TFLOP/s", kind="oracle")})}),
+        flush=True)
     return 0 if status == 0 else 1
 
 

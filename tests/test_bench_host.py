@@ -69,3 +69,11 @@ def test_skewed_workload_plants_popular_blocks_without_changing_other_draws():
     ks = workloads.bf16_bits_to_f32(skew.k)[0, :, 0]
     shifted = np.unique(np.nonzero(np.abs(ks - kb_) > 1.0)[0] // 64)
     assert shifted.size == 8 and shifted[0] == 0 and shifted[-1] == 4096 // 64 - 1
+
+
+def test_static_oracle_sample_counts_admitted_pairs():
+    w = workloads.Workload("s", bh=2, n=1024, d=64, dtype="bf16", kind="sliding", key_block=64,
+                           q_group=128, sliding=300)
+    t = workloads.generate(w)
+    tf, rows, secs, cores, desc = bench.static_oracle_sample(w, t, 0.2)
+    assert tf > 0 and rows > 0 and secs > 0 and cores >= 1 and "fp64" in desc
