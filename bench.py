@@ -358,8 +358,10 @@ def static_oracle_sample(w, t, seconds: float):
 
 def run_static(args, w, device, dist):
     """A sliding-window workload: the static-list fine stage on the tensors
-    of the dynamic workload of the same shape (one launch per step); with
-    --profile-forwards N, N untimed calls, else a timed run and one JSON line."""
+    of the dynamic workload of the same shape (one bsa_fine_attention call
+    per step: block key norms, the one-pass kernel, the relaunch for flagged
+    tiles); with --profile-forwards N, N untimed calls, else a timed run and
+    one JSON line."""
     import torch
     from content_dependent_block_gb300 import bsa
     base = next(x for x in workloads.WORKLOADS.values()
@@ -383,7 +385,7 @@ def run_static(args, w, device, dist):
         if dist is not None:
             dist.destroy_process_group()
         return 0 if status == 0 else 1
-    # timed: the static-list fine stage alone (one launch per step)
+    # timed: the static-list fine stage alone (one call per step)
     stream = torch.cuda.current_stream(device)
     for _ in range(args.warmup):
         run()
