@@ -8,7 +8,7 @@
 // selected the block.  One persistent CTA per SM runs six warp roles that
 // hand work to each other through mbarrier rings in shared memory:
 //
-//   prefetch  (warp 12)     takes fine items (one bin, <= 512 pairs) from a
+//   prefetch  (warp 15)     takes fine items (one bin, <= 512 pairs) from a
 //                           global queue and stages each item's descriptor
 //                           and pair ids in a shared-memory ring
 //   gather    (4 warps)     per staged item: loads K_b, V_b by TMA (128-byte
@@ -23,11 +23,14 @@
 //                           of two TMEM outputs;
 //                           an event loop that issues whichever is ready
 //   softmax   (warps 4-7)   one thread per row: m = max s, p = exp2(s - m),
-//                           l = sum p; P (bf16 pairs) to TMEM, (m, l) aside
+//                           l = sum p; P (bf16 pairs) to TMEM, (m, l) aside;
+//                           a full 64-key block takes a short path (one
+//                           load of all 64 scores, S released at once,
+//                           three-input max tree, no per-key predicates)
 //   epilogue  (warps 8-11)  reads O, stores the pair's partial state
 //                           o = O / l (bf16) and lse = m + log2 l into a ring
 //                           of query ranges, counts the range's finished pairs
-//   merge     (2 warps)     each takes merge items (256 queries of one range)
+//   merge     (2 warps)     each takes merge items (32 queries of one range)
 //                           from a second queue once the range's pairs are all
 //                           done, pulls the queries' partial states into
 //                           shared-memory stages with bulk copies and merges
@@ -40,6 +43,7 @@
 // deadlock, and every wait is bounded.  Results do not depend on scheduling:
 // partial states are per pair and merged in slot order.
 #include <cmath>
+#include <type_traits>
 
 #include <cudaTypedefs.h>
 
@@ -58,18 +62,20 @@ constexpr int kItemMax = 512;            // pairs per fine item (kFineBmItemPair
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 // Warp w runs on SM sub-partition w % 4.  Softmax and epilogue need one warp
-// per TMEM lane quadrant (w % 4 = 0..3); the other roles are placed so that
-// no sub-partition runs more than three different role code paths:
-//   partition 0: MMA (0), softmax, epilogue, prefetch (12)
+// per TMEM lane quadrant (w % 4 = 0..3).  The two merge warps sit on
+// different sub-partitions: with both on one, that partition's softmax warp
+// finished its quarter of every tile ~2000 cycles after the other three
+// (clock64 trace), and the P.V of the tile waited for it.
+//   partition 0: MMA (0), softmax, epilogue, merge (12)
 //   partitions 1, 2: gather (1, 13 and 2, 14), softmax, epilogue
-//   partition 3: merge (3, 15), softmax, epilogue
-constexpr int kWarpMma = 0, kWarpFetch = 12;
+//   partition 3: merge (3), softmax, epilogue, prefetch (15)
+constexpr int kWarpMma = 0, kWarpFetch = 15;
 constexpr int kWarpSoftmax = 4, kWarpEpi = 8;            // 4-7, 8-11
 __device__ __forceinline__ int gather_index(int w) {     // warps 1, 13, 2, 14 -> 0..3
     return w == 1 ? 0 : w == 13 ? 1 : w == 2 ? 2 : w == 14 ? 3 : -1;
 }
-__device__ __forceinline__ int merge_index(int w) {      // warps 3, 15 -> 0, 1
-    return w == 3 ? 0 : w == 15 ? 1 : -1;
+__device__ __forceinline__ int merge_index(int w) {      // warps 3, 12 -> 0, 1
+    return w == 3 ? 0 : w == 12 ? 1 : -1;
 }
 constexpr int kGather = 128;             // gather threads (warps 0-3)
 constexpr int kMergeWarps = 2;
@@ -140,36 +146,14 @@ struct Cfg {
 static_assert(Cfg<64>::kTotal <= 227 * 1024, "shared memory (d = 64)");
 static_assert(Cfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
 
-__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
-    int32_t v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Bounded wait until *p >= target (acquire).  False on timeout, or when
-// another wait in the grid already timed out.  The (slow) global timer is read
-// only every 64 polls.
-__device__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status) {
-    if (ld_acquire(p) >= target) return true;
-    uint64_t t0 = 0;
-    for (uint32_t spin = 1;; ++spin) {
-        __nanosleep(64);
-        if (ld_acquire(p) >= target) return true;
-        if ((spin & 63u) == 0) {
-            if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return false;
-            const uint64_t now = tc::global_ns();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > tc::kWaitLimitNs) {
-                report_status(status, kStatusTimeout);
-                return false;
-            }
-        }
-    }
-}
-
 __device__ __forceinline__ void red_add_release(int32_t *p, int32_t v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -419,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     flush();
                     int got = 1;
                     if (lane == 0)
-                        got = wait_counter(a.merge_done + (rg - kPartialRing),
+                        got = tc::wait_counter(a.merge_done + (rg - kPartialRing),
                                            a.w.range_merges[rg - kPartialRing], status);
                     if (!__shfl_sync(kFull, got, 0)) {
                         ok = false;
@@ -631,47 +615,65 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             }
             if (!tc::mbar_wait(bars + C::bSFull + j, (g >> 1) & 1, status)) break;
             tc::tc_fence_after();
-            float mraw = -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                uint32_t sv[32];
-                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
-                tc::tmem_ld_wait();
+            // All 64 scores of the row in one load; the S buffer is released at
+            // once.  Keys past `keys_valid` (a ragged last block, or the causal
+            // limit) are masked out; a warp whose rows are all full skips the
+            // masks.  Both forms do the same arithmetic in the same order (a
+            // masked key adds an exact zero), so a row's result does not depend
+            // on which other rows share its tile.
+            uint32_t s0[32], s1[32];
+            tc::tmem_ld32(tmem + uint32_t(j * kB) + lane_off, s0);
+            tc::tmem_ld32(tmem + uint32_t(j * kB + 32) + lane_off, s1);
+            tc::tmem_ld_wait();
+            tc::tc_fence_before();
+            tc::mbar_arrive(bars + C::bSFree + j);
+            const bool full = __all_sync(kFull, keys_valid == kB);
+            auto row_softmax = [&](auto masked) {
+                constexpr bool kMasked = decltype(masked)::value;
+                auto sc = [&](int c) -> float {       // score of key c, -inf when masked
+                    const float x = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+                    return (!kMasked || c < keys_valid) ? x : -INFINITY;
+                };
+                float mx[4];
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    if (c0 + c < keys_valid) mraw = fmaxf(mraw, __uint_as_float(sv[c]));
-            }
-            const float m2 = mraw * a.scale_log2;     // scale > 0 keeps the argmax
-            float l = 0.f;
-            bool ok = true;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                uint32_t sv[32];
-                tc::tmem_ld32(tmem + uint32_t(j * kB + c0) + lane_off, sv);
-                tc::tmem_ld_wait();
-                if (c0 == 32) {
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(bars + C::bSFree + j);
+                for (int u = 0; u < 4; ++u) {
+                    // 16 scores per chain, four independent chains
+                    float x[16];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        x[e] = sc(8 * u + e);
+                        x[8 + e] = sc(32 + 8 * u + e);
+                    }
+                    float m = fmax3(x[0], x[1], x[2]);
+#pragma unroll
+                    for (int e = 3; e < 15; e += 2) m = fmax3(m, x[e], x[e + 1]);
+                    mx[u] = fmaxf(m, x[15]);
                 }
-                uint32_t pk[16];
+                const float m2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                auto pr = [&](int c) -> float {       // p of key c, exactly 0 when masked
+                    const float x = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+                    return (!kMasked || c < keys_valid) ? ex2(fmaf(x, a.scale_log2, -m2)) : 0.f;
+                };
+                float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk0[16], pk1[16];
 #pragma unroll
                 for (int c = 0; c < 32; c += 2) {
-                    const float p0 = c0 + c < keys_valid ? ex2(fmaf(__uint_as_float(sv[c]), a.scale_log2, -m2)) : 0.f;
-                    const float p1 = c0 + c + 1 < keys_valid ? ex2(fmaf(__uint_as_float(sv[c + 1]), a.scale_log2, -m2)) : 0.f;
-                    l += p0 + p1;
-                    pk[c >> 1] = pack_bf16x2(p0, p1);
+                    const float p0 = pr(c), p1 = pr(c + 1), p2 = pr(c + 32), p3 = pr(c + 33);
+                    lsum[(c >> 1) & 3] += (p0 + p1) + (p2 + p3);
+                    pk0[c >> 1] = pack_bf16x2(p0, p1);
+                    pk1[c >> 1] = pack_bf16x2(p2, p3);
                 }
-                if (c0 == 0 && g >= C::kNO &&
-                    !tc::mbar_wait(bars + C::bPFree + jp, ((g / C::kNO) - 1) & 1, status)) {
-                    ok = false;
-                    break;
-                }
-                tc::tmem_st16(tmem + C::cP + uint32_t(jp * 32 + (c0 >> 1)) + lane_off, pk);
-            }
+                if (g >= C::kNO && !tc::mbar_wait(bars + C::bPFree + jp, ((g / C::kNO) - 1) & 1, status))
+                    return false;
+                tc::tmem_st16(tmem + C::cP + uint32_t(jp * 32) + lane_off, pk0);
+                tc::tmem_st16(tmem + C::cP + uint32_t(jp * 32 + 16) + lane_off, pk1);
+                // (m, l) live with the tile slot, which the gather group reuses
+                // only after this tile's epilogue is done
+                ml[slot * kTile + row] = make_float2(m2, (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
+                return true;
+            };
+            const bool ok = full ? row_softmax(std::false_type{}) : row_softmax(std::true_type{});
             if (!ok) break;
-            // (m, l) live with the tile slot, which the gather group reuses
-            // only after this tile's epilogue is done
-            ml[slot * kTile + row] = make_float2(m2, l);
             tc::mbar_arrive(bars + C::bMlFull + slot);
             tc::tmem_st_wait();
             tc::tc_fence_before();
@@ -787,7 +789,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const int64_t rg = item.x;
             int got = 1;
             if (lane == 0) {
-                got = wait_counter(a.range_done + rg, a.w.range_total[rg], status);
+                got = tc::wait_counter(a.range_done + rg, a.w.range_total[rg], status);
                 tc::fence_proxy_async_global();      // partials were written by generic stores
             }
             if (!__shfl_sync(kFull, got, 0)) break;
