@@ -31,7 +31,7 @@ EXPORTS = (
     "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_ex", "bsa_forward_noalloc",
     "bsa_forward_launches", "bsa_forward_graph_create", "bsa_graph_launch", "bsa_graph_destroy",
     "bsa_static_max_blocks",
-    "bsa_static_blocks", "bsa_get_device_status", "bsa_status_string",
+    "bsa_static_blocks", "bsa_get_device_status", "bsa_selftest_wait_timeout", "bsa_status_string",
     "bsa_last_error", "bsa_version",
 )
 
@@ -106,6 +106,7 @@ def lib():
         "bsa_static_max_blocks": ([i64, i32, i32, Mask], i32),
         "bsa_static_blocks": ([i64, i32, i32, Mask, vp, i32, vp, vp], i32),
         "bsa_get_device_status": ([vp, vp], i32),
+        "bsa_selftest_wait_timeout": ([i32, ctypes.c_uint64, vp], i32),
         "bsa_status_string": ([i32], ctypes.c_char_p),
         "bsa_last_error": ([], ctypes.c_char_p),
         "bsa_version": ([], i32),
@@ -345,3 +346,10 @@ def device_status() -> int:
     v = ctypes.c_int32(0)
     _check(lib().bsa_get_device_status(ctypes.byref(v), _stream()))
     return int(v.value)
+
+
+def selftest_wait_timeout(kind: int, limit_ns: int) -> None:
+    """Enqueue the bounded-wait self-test (bsa_selftest_wait_timeout): a wait
+    nothing completes gives up after about limit_ns and records
+    BSA_ERR_TIMEOUT; read it with device_status()."""
+    _check(lib().bsa_selftest_wait_timeout(int(kind), int(limit_ns), _stream()))

@@ -625,6 +625,17 @@ bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, cons
     return launched(bsa::launch_fine_backward(a, st), "backward launch");
 }
 
+// ------------------------------------------------------- failure path
+bsa_status bsa_selftest_wait_timeout(int32_t kind, uint64_t limit_ns, void *stream) {
+    if (kind != 0 && kind != 1) return fail(BSA_ERR_INVALID_ARG, "kind must be 0 or 1 (got %d)", kind);
+    if (limit_ns < 1000 || limit_ns > 2000000000ull)
+        return fail(BSA_ERR_INVALID_ARG, "limit_ns must be in [1e3, 2e9]");
+    int32_t *status = device_status_ptr();
+    if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    return launched(bsa::launch_wait_selftest(kind, limit_ns, status, static_cast<cudaStream_t>(stream)),
+                    "self-test launch");
+}
+
 // ------------------------------------------------------------ CUDA graphs
 struct bsa_graph_s {
     cudaGraph_t graph;

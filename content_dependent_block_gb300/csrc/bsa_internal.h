@@ -61,6 +61,11 @@ struct BwdArgs {
 bool fine_backward_supported(int32_t d, int32_t kb);   // one CTA of kb * d / 16 <= 512 threads
 cudaError_t launch_fine_backward(const BwdArgs &a, cudaStream_t st);
 
+// One small kernel whose bounded wait nothing completes (kind 0: an mbarrier,
+// 1: a global counter); it records BSA_ERR_TIMEOUT after about limit_ns.
+cudaError_t launch_wait_selftest(int32_t kind, uint64_t limit_ns, int32_t *status,
+                                 cudaStream_t st);
+
 // Records the one-line reason bsa_last_error() reports on this thread.
 void set_last_error(const char *msg);
 

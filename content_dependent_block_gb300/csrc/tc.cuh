@@ -91,13 +91,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Gives up
-// after about kWaitLimitNs, or as soon as another wait in the grid has (the
-// status word then already holds BSA_ERR_TIMEOUT).  The global timer is slow
-// to read, so it is read only every 1024 probes: a wait that ends within the
-// first probes costs no timer read at all.
+// after about `limit_ns` (kWaitLimitNs in every kernel; the self-test passes
+// a short one), or as soon as another wait in the grid has (the status word
+// then already holds BSA_ERR_TIMEOUT).  The global timer is slow to read, so
+// it is read only every 1024 probes: a wait that ends within the first
+// probes costs no timer read at all.
 // The polling loop is kept out of line: the wait sites are many and the
 // instruction cache is shared by every warp role of an SM sub-partition.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int32_t *status) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, int32_t *status,
+                                                   uint64_t limit_ns) {
     uint64_t t0 = 0;
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -107,7 +109,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parit
             const uint64_t now = global_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
+            } else if (now - t0 > limit_ns) {
                 report_status(status, kStatusTimeout);
                 return false;
             }
@@ -115,9 +117,41 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parit
     }
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, status);
+    return mbar_wait_slow(bar, parity, status, limit_ns);
+}
+
+__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until the global counter *p >= target (acquire at GPU
+// scope: what was written before the release that raised it is visible
+// afterwards).  False after about `limit_ns`, or at once when another wait
+// in the grid already ran out.  The (slow) global timer is read only every
+// 64 polls.
+static __device__ __noinline__ bool wait_counter(const int32_t *p, int32_t target, int32_t *status,
+                                                 uint64_t limit_ns = kWaitLimitNs) {
+    if (ld_acquire(p) >= target) return true;
+    uint64_t t0 = 0;
+    for (uint32_t spin = 1;; ++spin) {
+        __nanosleep(64);
+        if (ld_acquire(p) >= target) return true;
+        if ((spin & 63u) == 0) {
+            if (*reinterpret_cast<volatile int32_t *>(status) == kStatusTimeout) return false;
+            const uint64_t now = global_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > limit_ns) {
+                report_status(status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
 }
 
 // Named barrier among `count` threads (a multiple of 32) of the CTA.

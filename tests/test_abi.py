@@ -164,3 +164,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(bsa, "library_path", lambda: str(tmp_path / "absent.so"))
     with pytest.raises(bsa.BsaError):
         bsa.lib()
+
+
+@pytest.mark.parametrize("kind,limit", [(2, 1_000_000), (-1, 1_000_000), (0, 999), (1, 2_000_000_001)])
+def test_wait_selftest_rejects_bad_arguments(L, kind, limit):
+    assert L.bsa_selftest_wait_timeout(kind, limit, None) == 1
+    assert b"kind" in L.bsa_last_error() or b"limit" in L.bsa_last_error()
