@@ -301,7 +301,10 @@ bsa_status bsa_graph_destroy(bsa_graph graph);
  *   - Allocates nothing: no cudaMalloc/cudaFree and no allocating library
  *     call.  The first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The address is kept for the
+ *     life of the process (like the status word's, see
+ *     bsa_get_device_status): calls after a cudaDeviceReset of that device
+ *     are not supported.
  *   - Every call on a device shares the one array: calls whose work can
  *     overlap on the GPU (different streams, or different host threads)
  *     race on it and must be serialised by the caller.
@@ -337,9 +340,28 @@ bsa_status bsa_static_blocks(int64_t n, int32_t q_group, int32_t key_block,
 
 /*
  * Reads the device status word into *status (a bsa_status value), then
- * clears it.  Synchronises `stream` first.
+ * clears it.  Synchronises `stream` first.  The word is a static device
+ * variable of the library, one per device; its address is looked up on the
+ * first call that needs it on a device and kept for the life of the process
+ * (a cudaDeviceReset of that device is not supported afterwards).
  */
 bsa_status bsa_get_device_status(int32_t *status, void *stream);
+
+/*
+ * Failure-path self-test (the pages have no counterpart; it tests this
+ * library's own error handling).  Enqueues one small kernel that runs the
+ * library's bounded wait on something nothing will ever complete -- kind 0:
+ * an mbarrier no thread arrives on (the wait every TMA / MMA hand-off of the
+ * tensor-core kernels uses); kind 1: a counter in global memory no thread
+ * raises (the wait the block-major fine stage uses between its query ranges
+ * and merges).  After about limit_ns (1e3 .. 2e9 ns; the kernels use 2e9)
+ * the wait gives up, records BSA_ERR_TIMEOUT in the device status word and
+ * the kernel returns; the CUDA context stays usable.  If the status word
+ * already holds BSA_ERR_TIMEOUT the wait gives up at once.  Read (and clear)
+ * the result with bsa_get_device_status().  BSA_ERR_INVALID_ARG for another
+ * kind or a limit outside the range.
+ */
+bsa_status bsa_selftest_wait_timeout(int32_t kind, uint64_t limit_ns, void *stream);
 
 /* Static description of a status code. */
 const char *bsa_status_string(int32_t status);

@@ -3,8 +3,9 @@ memory at call time (its scratch is a static array inside the library).
 
 Called through the C ABI and compared with bsa_forward (caller workspace) on
 two consecutive calls with different inputs, so that leftovers of the first
-call in the shared static scratch would show up in the second.  Kept in a
-file of its own that is collected last.
+call in the shared static scratch would show up in the second; the device's
+free memory is the same before and after the second call.  Kept in a file of
+its own that is collected last.
 """
 import ctypes
 
@@ -34,11 +35,17 @@ def test_noalloc_matches_workspace_forward_on_two_calls():
         shape = bsa.Shape(w.bh, w.n, w.d, bsa.BF16)
         out = torch.full_like(q, float("nan"))
         idx = torch.full((w.bh, w.n, w.topk), -7, dtype=torch.int32, device=q.device)
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         rc = L.bsa_forward_noalloc(shape, bsa._ptr(q), bsa._ptr(k), bsa._ptr(v), w.key_block,
                                    w.topk, ctypes.c_float(0.0), bsa._ptr(out), bsa._ptr(idx),
                                    bsa._stream())
         assert rc == 0, L.bsa_last_error()
         torch.cuda.synchronize()
+        if seed == 1:
+            # after the first call (which may load the module holding the
+            # static array), a call takes no device memory at all
+            assert torch.cuda.mem_get_info()[0] == free_before
         assert bsa.device_status() == 0
         assert torch.equal(idx, ref_idx)
         got = parity.from_device(out).reshape(-1, w.d)
