@@ -73,6 +73,9 @@ def parse_args(argv=None):
                         "sequence for profilers: 6 kernels per forward); prints no JSON")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU seconds of the oracle sample")
+    p.add_argument("--preroll-s", type=float, default=1.5,
+                   help="seconds of untimed calls inside the clock-sampling window, "
+                        "before the warm-up and the timed steps")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -179,6 +182,59 @@ def measured_peaks():
     d = dict(FALLBACK_PEAKS)
     d["source"] = "fallback"
     return d
+
+
+def fp32_peak(peaks, sms: int) -> float:
+    """FP32 FLOP/s derived from unit counts and clocks: SMs x 128 FP32
+    lanes x 2 FLOP (one FMA) x the maximum SM clock."""
+    return sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+
+
+def roofline(f_mma: float, f_alu: float, nbytes: float, t_ms: float, peaks, sms: int,
+             kernel: str, traffic, tc_key: str = "bf16_tflops"):
+    """Roofline object of the scope table (d): the bound is
+    t_roof = max(F_mma / P_tensor + F_alu / P_fp32, bytes / BW_hbm), with the
+    measured tensor peak and HBM bandwidth and the derived FP32 peak.
+    `achieved` is the algorithmic FLOPs over the measured time, `peak` the
+    same FLOPs over t_roof, so that frac = achieved / peak = t_roof / t."""
+    p_tc = peaks[tc_key] * 1e12
+    p_fp32 = fp32_peak(peaks, sms)
+    bw = peaks["hbm_gbs"] * 1e9
+    t_mma, t_alu, t_hbm = f_mma / p_tc, f_alu / p_fp32, nbytes / bw
+    t_roof = max(t_mma + t_alu, t_hbm)
+    flops = f_mma + f_alu
+    achieved = flops / (t_ms * 1e-3) / 1e12
+    peak = flops / t_roof / 1e12
+    if t_hbm >= t_mma + t_alu:
+        bound = "hbm"
+    elif t_mma >= t_alu:
+        bound = "tensor"
+    else:
+        bound = "alu"
+    return {"kernel": kernel, "bound": bound, "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+            "t_roof_us": t_roof * 1e6, "launch_ms": t_ms,
+            "terms_us": {"mma_at_tensor_peak": t_mma * 1e6, "softmax_at_fp32_peak": t_alu * 1e6,
+                         "bytes_at_hbm_bw": t_hbm * 1e6},
+            "algorithmic": {"mma_flops": f_mma, "alu_flops": f_alu, "unique_bytes": nbytes},
+            "peaks": {"tensor_tflops": p_tc / 1e12, "tensor_source": f"{tc_key}, {peaks['source']}",
+                      "fp32_tflops": p_fp32 / 1e12,
+                      "fp32_source": f"{sms} SMs x 128 lanes x 2 x max clock (derived)",
+                      "hbm_gbs": bw / 1e9, "hbm_source": f"hbm_gbs, {peaks['source']}"},
+            "formula": "peak = F / max(F_mma/P_tensor + F_alu/P_fp32, bytes/BW_hbm)"}
+
+
+def preroll(fn, seconds: float, sync):
+    """Untimed calls for about `seconds` (so that clock samplers see the
+    GPU under steady load before the timed region)."""
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(8):
+            fn()
+        sync()
+        n += 8
+    return n
 
 
 def kernel_traffic(kernel: str, workload: str):
@@ -327,19 +383,31 @@ def reference_arm(args, rank, world, w):
 
 
 def static_oracle_sample(w, t, seconds: float):
-    """The oracle's sliding-window attention (plain masked definition) on a
-    seeded row sample, repeated until about `seconds` of CPU time; returns
-    (TFLOP/s on admitted pairs, rows per pass, seconds, cores, description)."""
+    """The oracle's static-pattern attention (plain masked definition: the
+    sliding window or the local+global mask) on a seeded row sample,
+    repeated until about `seconds` of CPU time; returns (TFLOP/s on admitted
+    pairs, rows per pass, seconds, cores, description)."""
     import numpy as np
     import oracle
     cores = oracle.num_threads()
+    if w.kind == "sliding":
+        kind, kw, what = oracle.MASK_SLIDING, dict(W=w.sliding), "i-W < j <= i"
+    else:
+        kind, kw, what = oracle.MASK_LOCAL_GLOBAL, dict(w=w.window, s=w.stride), \
+            f"|i-j| <= {w.window} or j % {w.stride} == 0"
+
+    def keys_of(rows):
+        i = rows % w.n
+        if w.kind == "sliding":
+            return int(np.minimum(i + 1, w.sliding).sum())
+        j = np.arange(w.n)
+        return int(sum(int(((np.abs(ii - j) <= w.window) | (j % w.stride == 0)).sum()) for ii in i))
 
     def run(count):
         rows = workloads.sample_rows(w.bh, w.n, max(1, count // w.bh), seed=7)
         t0 = time.perf_counter()
-        oracle.masked(t.q, t.k, t.v, oracle.MASK_SLIDING, rows, W=w.sliding)
-        keys = np.minimum(rows % w.n + 1, w.sliding)
-        return rows.size, time.perf_counter() - t0, metrics.pairs_flops(int(keys.sum()), w.d)
+        oracle.masked(t.q, t.k, t.v, kind, rows, **kw)
+        return rows.size, time.perf_counter() - t0, metrics.pairs_flops(keys_of(rows), w.d)
 
     r0, t0, _ = run(16 * w.bh)
     count = int(min(w.bh * w.n, 8192, max(r0, r0 * seconds / max(t0, 1e-3))))
@@ -352,27 +420,45 @@ def static_oracle_sample(w, t, seconds: float):
         flops += fl
         passes += 1
     desc = (f"{rows // passes} of {w.bh * w.n} query rows (seeded sample) x {passes} passes, "
-            f"dense masked attention over i-W < j <= i per row, fp64, {cores} threads")
+            f"dense masked attention over {what} per row, fp64, {cores} threads")
     return flops / secs / 1e12, rows // passes, secs, cores, desc
 
 
 def run_static(args, w, device, dist):
-    """A sliding-window workload: the static-list fine stage on the tensors
-    of the dynamic workload of the same shape (one bsa_fine_attention call
-    per step: block key norms, the one-pass kernel, the relaunch for flagged
-    tiles); with --profile-forwards N, N untimed calls, else a timed run and
-    one JSON line."""
+    """A static-pattern workload: one bsa_fine_attention call per step over
+    the host-built block lists (bsa_static_blocks).  The sliding window runs
+    on the tensors of the dynamic workload of the same shape (block key
+    norms, the one-pass tensor-core kernel, the relaunch for flagged tiles);
+    the local+global pattern is the fp32 16x16-tile workload of the
+    yayme/CUDA-kernel README (CUDA-core kernel).  With --profile-forwards N,
+    N untimed calls; else a timed run (clocks sampled around it, L2 flushed
+    before every step) and one JSON line."""
     import torch
     from content_dependent_block_gb300 import bsa
-    base = next(x for x in workloads.WORKLOADS.values()
-                if x.kind == "dynamic" and (x.bh, x.n, x.d) == (w.bh, w.n, w.d))
-    t = workloads.generate(base)
-    q, k, v = (torch.from_numpy(getattr(t, x).view("int16")).view(torch.bfloat16).to(device)
-               for x in "qkv")
-    m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=w.sliding)
+    if w.kind == "sliding":
+        base = next(x for x in workloads.WORKLOADS.values()
+                    if x.kind == "dynamic" and (x.bh, x.n, x.d) == (w.bh, w.n, w.d))
+        t = workloads.generate(base)
+        q, k, v = (torch.from_numpy(getattr(t, x).view("int16")).view(torch.bfloat16).to(device)
+                   for x in "qkv")
+        m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=w.sliding)
+        pairs = metrics.sliding_pairs(w.n, w.sliding) * w.bh
+        elem, dtype, tc_key = 2, "bf16", "bf16_tflops"
+        kernel = ("static fine stage: block key norms + one-pass tensor-core kernel "
+                  "(+ the two-pass relaunch for flagged tiles)")
+        metric = "static sliding-window fine stage, effective TFLOP/s on admitted pairs"
+    else:
+        t = workloads.generate(w)
+        q, k, v = (torch.from_numpy(getattr(t, x)).to(device) for x in "qkv")
+        m = bsa.mask_struct(bsa.MASK_LOCAL_GLOBAL, window=w.window, stride=w.stride)
+        pairs = metrics.local_global_pairs(w.n, w.window, w.stride) * w.bh
+        elem, dtype, tc_key = 4, "f32", "bf16_tflops"
+        kernel = "static fine stage, fp32 on the CUDA cores (query-major kernel over the tile lists)"
+        metric = "static local+global fine stage (fp32), effective TFLOP/s on admitted pairs"
     lst, _, _ = bsa.static_blocks(w.n, w.q_group, w.key_block, m)
     dl = torch.from_numpy(lst).to(device)
     out = torch.empty_like(q)
+
     def run():
         bsa.fine_attention(q, k, v, dl, key_block=w.key_block, q_group=w.q_group,
                            per_head=False, mask=m, out=out)
@@ -385,46 +471,63 @@ def run_static(args, w, device, dist):
         if dist is not None:
             dist.destroy_process_group()
         return 0 if status == 0 else 1
-    # timed: the static-list fine stage alone (one call per step)
     stream = torch.cuda.current_stream(device)
-    for _ in range(args.warmup):
-        run()
-    torch.cuda.synchronize(device)
-    evs = []
-    for _ in range(args.steps):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run()
-        e1.record(stream)
-        evs.append((e0, e1))
-    torch.cuda.synchronize(device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else device.index
+    with ClockSampler(gpu_index) as clocks:
+        preroll(run, args.preroll_s, lambda: torch.cuda.synchronize(device))
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            run()
+        torch.cuda.synchronize(device)
+        evs = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+    clk = clocks.summary()
     ms = statistics.median(a.elapsed_time(b) for a, b in evs)
-    pairs = metrics.sliding_pairs(w.n, w.sliding) * w.bh
     achieved = metrics.pairs_flops(pairs, w.d) / (ms * 1e-3) / 1e12
     peaks = measured_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    nbytes = metrics.unique_bytes(w.n, w.bh, w.d, elem)
+    if w.kind == "sliding":
+        rl = roofline(4 * w.d * pairs, 5 * pairs, nbytes, ms, peaks, sms, kernel,
+                      kernel_traffic("fine_static_tc", w.name), tc_key)
+    else:
+        # fp32 throughout: every FLOP at the FP32 peak (no tensor term)
+        rl = roofline(0, metrics.pairs_flops(pairs, w.d), nbytes, ms, peaks, sms, kernel, None,
+                      tc_key)
     status = bsa.device_status()
     if dist is not None:
         dist.destroy_process_group()
-    print(json.dumps({
-        "metric": "static sliding-window fine stage, effective TFLOP/s on admitted pairs",
-        "value": achieved, "unit": "TFLOP/s",
-        "roofline": {"kernel": "static fine stage: block key norms + one-pass tensor-core kernel "
-                               "(+ the two-pass relaunch for flagged tiles)",
-                     "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                     "peak_source": f"bf16_tflops burst, {peaks['source']}",
-                     "traffic": kernel_traffic("fine_static_tc", w.name)},
+    cfg = {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "key_block": w.key_block,
+           "q_group": w.q_group, "dtype": w.dtype, "inputs": w.note,
+           "timing": "median of CUDA-event times; L2 flushed (256 MiB write) before every step"}
+    if w.kind == "sliding":
+        cfg["sliding"] = w.sliding
+    else:
+        cfg.update(window=w.window, stride=w.stride)
+    line = {
+        "metric": metric, "value": achieved, "unit": "TFLOP/s",
+        "roofline": rl,
         "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "n_gpus": 1,
-        "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "bh": w.bh, "n": w.n, "d": w.d, "sliding": w.sliding,
-                   "key_block": w.key_block, "q_group": w.q_group, "inputs": w.note,
-                   "timing": "median of CUDA-event times; inputs (805 MB) larger than L2"},
-        "admitted_pairs": pairs, "device_status": status,
-        **({} if args.no_cpu_baseline else {"cpu_baseline": dict(zip(
-            ("value", "rows", "seconds", "cores", "sample"),
-            static_oracle_sample(w, t, args.cpu_seconds)), unit="TFLOP/s", kind="oracle")})}),
-        flush=True)
+        "higher_is_better": True, "dtype": dtype, "data": "synthetic", "config": cfg,
+        "clocks": clk, "admitted_pairs": pairs, "device_status": status,
+        # per call: sliding = block key norms, the one-pass kernel, the
+        # relaunch for flagged tiles (plus a memset); fp32 = one kernel
+        "gpu_launches": (3 if w.kind == "sliding" else 1) * args.steps}
+    if not args.no_cpu_baseline:
+        tf, rows, secs, cores, desc = static_oracle_sample(w, t, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": secs}
+    print(json.dumps(line), flush=True)
     return 0 if status == 0 else 1
 
 
@@ -521,7 +624,7 @@ def main(argv=None):
     barrier(dist, device)
     bsa.lib()
 
-    if w.kind == "sliding":
+    if w.kind in ("sliding", "local_global"):
         return run_static(args, w, device, dist)
     t = workloads.generate(w, seed=w.seed + rank)
     torch.cuda.reset_peak_memory_stats(device)
@@ -573,6 +676,7 @@ def main(argv=None):
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
     with ClockSampler(gpu_index) as clocks:
+        preroll(lambda: fwd(q, k, v), args.preroll_s, lambda: torch.cuda.synchronize(device))
         for _ in range(args.warmup):
             flush_l2()
             fwd(q, k, v)
@@ -646,7 +750,17 @@ def main(argv=None):
     value = total_flops / (total_ms * 1e-3) / 1e12
     peaks = measured_peaks()
     tc_peak = peaks["bf16_tflops"]
-    achieved = fine_flops / (fine_ms * 1e-3) / 1e12
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    # the dominant unit: one bsa_fine_attention call (list inversion + the
+    # fine kernel), timed alone; per admitted (query, key) pair 4d MMA FLOPs
+    # (q.k and p.v) and 5 softmax ops, compulsory bytes Q, K, V in and O out
+    fine_keys = fine_flops // (4 * w.d + 5)
+    fine_rl = roofline(4 * w.d * fine_keys, 5 * fine_keys, metrics.unique_bytes(w.n, w.bh, w.d, 2),
+                       fine_ms, peaks, sms,
+                       "fine attention stage: one bsa_fine_attention call over the top-k list "
+                       "(list inversion + fine_ws_kernel)",
+                       kernel_traffic("fine_stage" if fwd.launches == 6 else "fine_query_major",
+                                      w.name))
     cfg = config_of(w)
     cfg["launch"] = ("one CUDA-graph replay per forward" if args.graph
                      else "one bsa_forward_ex call per forward")
@@ -655,15 +769,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": cfg,
-        "roofline": {"kernel": "fine attention stage: one bsa_fine_attention call over the top-k "
-                               "list (list inversion + fine_ws_kernel)",
-                     "bound": "tensor", "achieved": achieved, "peak": tc_peak,
-                     "unit": "TFLOP/s", "frac": achieved / tc_peak,
-                     "peak_source": f"bf16_tflops burst, {peaks['source']}",
-                     "traffic": kernel_traffic("fine_stage" if fwd.launches == 6 else "fine_query_major",
-                                               w.name),
-                     "algorithmic_flops_per_launch": fine_flops,
-                     "launch_ms": fine_ms},
+        "roofline": fine_rl,
         "e2e": {"value": flops * world / (e2e_total / args.steps * 1e-3) / 1e12,
                 "unit": "TFLOP/s", "ms_per_step": e2e_total / args.steps,
                 "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
@@ -682,8 +788,7 @@ def main(argv=None):
     f_mma, f_alu = metrics.sparse_flops_split(w.n, w.bh, w.d, w.key_block, w.topk)
     if w.has_options:
         f_mma, f_alu = 4 * w.d * pairs + 2 * w.d * elig, 5 * pairs
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    p_fp32 = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
+    p_fp32 = fp32_peak(peaks, sms)
     bytes_fwd = metrics.unique_bytes(w.n, w.bh, w.d, 2)
     t_roof = max(f_mma / (tc_peak * 1e12) + f_alu / p_fp32, bytes_fwd / (peaks["hbm_gbs"] * 1e9))
     line["roofline_forward"] = {
