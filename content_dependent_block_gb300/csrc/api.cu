@@ -188,7 +188,7 @@ BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     off = round_up(off, 256);
     L.part_o = take(ring_slots * s.d * 2);
     off = round_up(off, 256);
-    L.part_lse = take(ring_slots * 4);
+    L.part_lse = take(ring_slots * 8);
     L.total = round_up(off, 256);
     return L;
 }
@@ -245,7 +245,7 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     a.head_k = sel != nullptr ? sel->head_k : nullptr;
     a.scale_log2 = scale_log2;
     a.part_o = reinterpret_cast<uint16_t *>(ws + L.part_o);
-    a.part_lse = reinterpret_cast<float *>(ws + L.part_lse);
+    a.part_ml = reinterpret_cast<float2 *>(ws + L.part_lse);
     a.out = static_cast<uint16_t *>(out);
     a.status = status;
     return bsa::launch_fine_bm(a, st);

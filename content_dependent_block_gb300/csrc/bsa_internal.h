@@ -145,7 +145,7 @@ struct FineBmArgs {
     const int32_t *head_k;
     float scale_log2;
     uint16_t *part_o;             // [ring][range * kpad][d] bf16
-    float *part_lse;              // [ring][range * kpad]
+    float2 *part_ml;              // [ring][range * kpad] (m, l) of each pair, log2 units
     uint16_t *out;
     int32_t *status;
 };

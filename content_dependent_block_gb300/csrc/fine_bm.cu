@@ -5,32 +5,33 @@
 //
 // Schedule.  The per-query lists are inverted (invert.cu) into bins
 // (head, query range, key block), each listing the (query, slot) pairs that
-// selected the block.  One persistent CTA per SM runs six warp roles that
-// hand work to each other through mbarrier rings in shared memory:
+// selected the block.  One persistent CTA per SM runs these warp roles,
+// handing work over mbarriers in shared memory:
 //
-//   prefetch  (warp 15)     takes fine items (one bin, <= 512 pairs) from a
-//                           global queue and stages each item's descriptor
-//                           and pair ids in a shared-memory ring
-//   gather    (4 warps)     per staged item: loads K_b, V_b by TMA (128-byte
-//                           swizzle, one buffer per item in flight); per tile
-//                           of 128 pairs, 128 threads copy the query rows
-//                           with cp.async straight into the swizzled operand
-//                           layout, and publish a tile once the next one is
-//                           in flight (or before any wait that may block)
-//   MMA       (warp 0)      S[j] = Q . K_b^T (tcgen05, M = 128, N = 64) into
-//                           one of two TMEM score buffers, then O[j] = P . V_b
-//                           (A = P read from TMEM, N = d, V MN-major) into one
-//                           of two TMEM outputs;
-//                           an event loop that issues whichever is ready
-//   softmax   (warps 4-7)   one thread per row: m = max s, p = exp2(s - m),
-//                           l = sum p; P (bf16 pairs) to TMEM, (m, l) aside;
-//                           a full 64-key block takes a short path (one
-//                           load of all 64 scores, S released at once,
-//                           three-input max tree, no per-key predicates)
-//   epilogue  (warps 8-11)  reads O, stores the pair's partial state
-//                           o = O / l (bf16) and lse = m + log2 l into a ring
-//                           of query ranges, counts the range's finished pairs
-//   merge     (2 warps)     each takes merge items (32 queries of one range)
+//   prefetch  (warp 12)     takes fine items (one bin, <= 512 pairs) from a
+//                           global queue, stages each item's descriptor and
+//                           pair ids in a shared-memory ring and starts the
+//                           TMA loads of its K_b and V_b (128-byte swizzle,
+//                           one buffer per item in flight)
+//   gather    (warps 8-11)  per tile of 128 pairs of a staged item, 128
+//                           threads copy the query rows with cp.async
+//                           straight into the swizzled operand layout; the
+//                           hardware arrives on the stage's barrier when the
+//                           copies land (no thread waits for them)
+//   owners    (warps 0-3,   fine items alternate between the two owner
+//              4-7)         warpgroups, and a group runs each tile of its
+//                           items from start to end: its first warp issues
+//                           S = Q . K_b^T (tcgen05, M = 128, N = 64) into the
+//                           group's TMEM columns; one thread per pair row
+//                           turns its row into P (bf16, back into TMEM) and
+//                           (m, l); the first warp issues O = P . V_b (A = P
+//                           from TMEM, N = d, V MN-major); every thread stores
+//                           its pair's unnormalised O (bf16) and (m, l) into
+//                           a ring of query ranges.  One group's softmax or
+//                           stores run while the other's MMAs do.  One
+//                           thread of the group counts finished pairs per
+//                           range, up to four tiles under one GPU-scope fence
+//   merge     (warps 13-15) each takes merge items (32 queries of one range)
 //                           from a second queue once the range's pairs are all
 //                           done, pulls the queries' partial states into
 //                           shared-memory stages with bulk copies and merges
@@ -39,9 +40,12 @@
 //
 // Partial states of a range live in ring entry (range mod kPartialRing); a
 // fine item of range r waits until range r - kPartialRing is merged.  Every
-// wait is on work taken from a queue earlier, so the schedule cannot
-// deadlock, and every wait is bounded.  Results do not depend on scheduling:
-// partial states are per pair and merged in slot order.
+// wait is on work taken from a queue earlier or on this CTA's own progress,
+// and a group counts its finished pairs before it waits for a tile that may
+// depend on other CTAs, so the schedule cannot deadlock; every wait is
+// bounded.  Results do not depend on scheduling: a row's arithmetic does not
+// depend on the other rows of its tile, and partial states are per pair and
+// merged in slot order.
 #include <cmath>
 #include <type_traits>
 
@@ -56,31 +60,24 @@ namespace {
 
 constexpr int kTile = 128;
 constexpr int kB = 64;                   // key block handled by this kernel
-constexpr int kNT = 8;                   // tile-info ring
+constexpr int kNTW = 4;                  // tile-info ring of each owner warpgroup
 constexpr int kNI = 2;                   // staged fine-item ring
 constexpr int kItemMax = 512;            // pairs per fine item (kFineBmItemPairs)
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-// Warp w runs on SM sub-partition w % 4.  Softmax and epilogue need one warp
-// per TMEM lane quadrant (w % 4 = 0..3).  The two merge warps sit on
-// different sub-partitions: with both on one, that partition's softmax warp
-// finished its quarter of every tile ~2000 cycles after the other three
-// (clock64 trace), and the P.V of the tile waited for it.
-//   partition 0: MMA (0), softmax, epilogue, merge (12)
-//   partitions 1, 2: gather (1, 13 and 2, 14), softmax, epilogue
-//   partition 3: merge (3), softmax, epilogue, prefetch (15)
-constexpr int kWarpMma = 0, kWarpFetch = 15;
-constexpr int kWarpSoftmax = 4, kWarpEpi = 8;            // 4-7, 8-11
-__device__ __forceinline__ int gather_index(int w) {     // warps 1, 13, 2, 14 -> 0..3
-    return w == 1 ? 0 : w == 13 ? 1 : w == 2 ? 2 : w == 14 ? 3 : -1;
-}
-__device__ __forceinline__ int merge_index(int w) {      // warps 3, 12 -> 0, 1
-    return w == 3 ? 0 : w == 12 ? 1 : -1;
-}
-constexpr int kGather = 128;             // gather threads (warps 0-3)
-constexpr int kMergeWarps = 2;
+// Warp w runs on SM sub-partition w % 4, and a warp reaches only the TMEM lane
+// quadrant w % 4.  Two owner warpgroups (warps 0-3 and 4-7) each run whole
+// tiles; the other roles spread over the four sub-partitions:
+//   0-3, 4-7   owner warpgroups (fine items alternate between them)
+//   8-11       gather
+//   12         prefetch
+//   13-15      merge
+constexpr int kWarpFetch = 12;
+__device__ __forceinline__ int gather_index(int w) { return w >= 8 && w < 12 ? w - 8 : -1; }
+__device__ __forceinline__ int merge_index(int w) { return w >= 13 ? w - 13 : -1; }
+constexpr int kGather = 128;             // gather threads (warps 8-11)
+constexpr int kMergeWarps = 3;
 constexpr int kStageBytes = 17408;       // one merge stage: >= 2 queries at d = 128, k = 32
-constexpr uint32_t kBarEpi = 1;
 constexpr unsigned kFull = 0xffffffffu;
 
 // Per-tile constants, computed once by the gather group: keys in the block
@@ -88,7 +85,7 @@ constexpr unsigned kFull = 0xffffffffu;
 // query (qbase), the range's offset in the partial-state ring (roff), the
 // range's first query index (ibase) and the block's first key (j0).
 struct TileInfo {
-    int32_t bin, p0, count, item, last, rg, end, kv, qbase, roff, ibase, j0;
+    int32_t bin, p0, count, item, last, rg, end, kv, qbase, roff, ibase, j0, g;
 };
 
 // A fine item staged by the prefetcher: descriptor plus all its pair ids
@@ -104,34 +101,27 @@ struct Cfg {
     static constexpr int kNQ = D == 64 ? 3 : 2;            // Q stages
     static constexpr int kNKV = D == 64 ? 3 : 2;           // K/V buffers (items in flight)
     static constexpr int kMS = D == 64 ? 2 : 1;            // merge stages per merge warp
-    static constexpr int kNO = D == 64 ? 4 : 2;            // O and P buffers in TMEM
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int oQ = 0;
     static constexpr int oK = oQ + kNQ * kQBytes;
     static constexpr int oV = oK + kNKV * kKBytes;
     static constexpr int oMs = oV + kNKV * kKBytes;        // merge stages
-    static constexpr int oEpi = oMs + kMergeWarps * kMS * kStageBytes;  // 4 warps x 32 rows x 64 B
-    static constexpr int oML = oEpi + 4 * 2048;            // float2 [kNT][128]
-    static constexpr int oPid = oML + kNT * kTile * 8;     // int32  [kNT][128]
-    static constexpr int oTi = oPid + kNT * kTile * 4;     // TileInfo [kNT]
-    static constexpr int oItem = oTi + kNT * int(sizeof(TileInfo));   // StagedItem [kNI]
+    static constexpr int oEpi = oMs + kMergeWarps * kMS * kStageBytes;  // 8 warps x 32 rows x 64 B
+    static constexpr int oPid = oEpi + 8 * 2048;           // int32  [2][kNTW][128]
+    static constexpr int oTi = oPid + 2 * kNTW * kTile * 4;     // TileInfo [2][kNTW]
+    static constexpr int oItem = oTi + 2 * kNTW * int(sizeof(TileInfo));   // StagedItem [kNI]
     static constexpr int oBar = oItem + kNI * int(sizeof(StagedItem));
     enum {
         bQFull = 0,
         bQFree = bQFull + kNQ,
         bKvFull = bQFree + kNQ,
         bKvFree = bKvFull + kNKV,
-        bSFull = bKvFree + kNKV,
-        bSFree = bSFull + 2,
-        bPFull = bSFree + 2,
-        bPFree = bPFull + kNO,
-        bOFull = bPFree + kNO,
-        bOFree = bOFull + kNO,
-        bMlFull = bOFree + kNO,
-        bTiFull = bMlFull + kNT,
-        bTiFree = bTiFull + kNT,
-        bItFull = bTiFree + kNT,
+        bTiFull = bKvFree + kNKV,          // [2][kNTW]
+        bTiFree = bTiFull + 2 * kNTW,      // [2][kNTW]
+        bSDone = bTiFree + 2 * kNTW,       // [2]
+        bODone = bSDone + 2,               // [2]
+        bItFull = bODone + 2,
         bItFree = bItFull + kNI,
         bMsFull = bItFree + kNI,
         bCount = bMsFull + kMergeWarps * kMS
@@ -139,12 +129,18 @@ struct Cfg {
     static constexpr int oMisc = oBar + bCount * 8;
     static constexpr int kTotal = oMisc + 64 + 1024;
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t cO = 2 * kB;                 // O[j] at cO + j*D; S[j] at j*64
-    static constexpr uint32_t cP = 2 * kB + kNO * D;       // P[j] (bf16 pairs) at cP + j*32
-    static_assert(cP + kNO * 32 <= kTmemCols, "tensor memory");
+    // each owner warpgroup: S (64 columns), P (bf16 pairs, 32), O (D)
+    static constexpr uint32_t kWgCols = 64 + 32 + D;
+    static_assert(2 * kWgCols <= kTmemCols, "tensor memory");
 };
 static_assert(Cfg<64>::kTotal <= 227 * 1024, "shared memory (d = 64)");
 static_assert(Cfg<128>::kTotal <= 227 * 1024, "shared memory (d = 128)");
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
 
 __device__ __forceinline__ void red_add_release(int32_t *p, int32_t v) {
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -162,31 +158,36 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Merge one query's partial states from a shared-memory stage.  The query
-// is owned by a group of LPQ = D/16 lanes; lane gl owns channels
-// [16 gl, 16 gl + 16), read as two 16-byte chunks per slot.  `po` points at
-// this lane's channels of slot 0 (slots D channels apart), `pl` at the
-// query's lse values, `vm` has bit s set for every listed slot s.  Slot s's
-// lse is read by lane s mod LPQ and the weights exp2(lse - max) are shared
-// by shuffles.  Neighbouring queries read their two chunks in opposite
-// order, so that a quarter warp touches all 32 banks once.  The slot loop
-// is rolled (four slots per trip) to keep the code small.  Returns false
-// when nothing is listed; else acc holds the merged channels.  kOpts: a
-// listed slot may hold a partial that admitted no key (lse = -inf, under the
+// Merge one query's partial states from a shared-memory stage.  Slot s
+// holds the unnormalised output O_s = sum_j 2^(s_j - m_s) v_j of its block
+// (bf16) and (m_s, l_s); the query's output is sum_s w_s O_s / sum_s w_s l_s
+// with w_s = 2^(m_s - M), M the largest m_s (the online-softmax merge of
+// (m, l, acc)).  The query is owned by a group of LPQ = D/16 lanes; lane gl
+// owns channels [16 gl, 16 gl + 16), read as two 16-byte chunks per slot.
+// `po` points at this lane's channels of slot 0 (slots D channels apart),
+// `pml` at the query's (m, l) pairs, `vm` has bit s set for every listed
+// slot s.  Slot s's (m, l) is read by lane s mod LPQ and the weights are
+// shared by shuffles.  Neighbouring queries read their two chunks in
+// opposite order, so that a quarter warp touches all 32 banks once.  The
+// slot loop is rolled (four slots per trip) to keep the code small.  Returns
+// false when nothing is listed; else acc holds the merged channels.  kOpts:
+// a listed slot may hold a partial that admitted no key (m = -inf, under the
 // causal mask); it weighs 0.
 template <int D, bool kOpts>
-__device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pl, uint32_t vm, int k,
+__device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pml, uint32_t vm, int k,
                                             int lane, float (&acc)[16]) {
     constexpr int LPQ = D / 16;
     constexpr int SPL = 32 / LPQ;              // slots per lane (k <= 32)
     const int gl = lane % LPQ, gbase = lane - gl;
     const int c0 = (lane / LPQ) & 1;           // chunk read first
-    float w[SPL];
+    float w[SPL], lv[SPL];
     float M = -INFINITY;
 #pragma unroll
     for (int t = 0; t < SPL; ++t) {
         const int s = gl + LPQ * t;
-        w[t] = ((vm >> s) & 1u) ? pl[s] : -INFINITY;
+        const bool listed = ((vm >> s) & 1u) != 0;
+        w[t] = listed ? pml[2 * s] : -INFINITY;
+        lv[t] = listed ? pml[2 * s + 1] : 0.f;
         M = fmaxf(M, w[t]);
     }
 #pragma unroll
@@ -198,7 +199,7 @@ __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pl,
         // unlisted slots hold -inf, and so does a partial that admitted no key
         const bool use = kOpts ? w[t] > -INFINITY : ((vm >> s) & 1u) != 0;
         w[t] = use ? ex2(w[t] - M) : 0.f;
-        L += w[t];
+        L += w[t] * lv[t];
     }
 #pragma unroll
     for (int o = 1; o < LPQ; o <<= 1) L += __shfl_xor_sync(kFull, L, o);
@@ -258,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
     TileInfo *ti = reinterpret_cast<TileInfo *>(sm + C::oTi);
     StagedItem *items = reinterpret_cast<StagedItem *>(sm + C::oItem);
     int32_t *pids = reinterpret_cast<int32_t *>(sm + C::oPid);
-    float2 *ml = reinterpret_cast<float2 *>(sm + C::oML);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::oMisc);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,20 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             tc::mbar_init(bars + C::bKvFull + i, 1);
             tc::mbar_init(bars + C::bKvFree + i, 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(bars + C::bSFull + i, 1);
-            tc::mbar_init(bars + C::bSFree + i, kTile);
-        }
-        for (int i = 0; i < C::kNO; ++i) {
-            tc::mbar_init(bars + C::bPFull + i, kTile);
-            tc::mbar_init(bars + C::bPFree + i, 1);
-            tc::mbar_init(bars + C::bOFull + i, 1);
-            tc::mbar_init(bars + C::bOFree + i, kTile);
-        }
-        for (int i = 0; i < kNT; ++i) tc::mbar_init(bars + C::bMlFull + i, kTile);
-        for (int i = 0; i < kNT; ++i) {
+        for (int i = 0; i < 2 * kNTW; ++i) {
             tc::mbar_init(bars + C::bTiFull + i, kGather);
             tc::mbar_init(bars + C::bTiFree + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bars + C::bSDone + i, 1);
+            tc::mbar_init(bars + C::bODone + i, 1);
         }
         for (int i = 0; i < kNI; ++i) {
             tc::mbar_init(bars + C::bItFull + i, 32);
@@ -299,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         tc::prefetch_tensormap(&tm_k);
         tc::prefetch_tensormap(&tm_v);
     }
-    if (warp == kWarpMma) {
+    if (warp == 0) {
         tc::tmem_alloc(tmem_slot, C::kTmemCols);
         tc::tmem_relinquish();
     }
@@ -356,63 +349,18 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 }
             }
             if (lane == 0) si->valid = valid ? 1 : 0;
-            __syncwarp();
-            tc::mbar_arrive(bars + C::bItFull + slot);
-            if (!valid) break;
-        }
-    } else if (gather_index(warp) >= 0) {
-        // --------------------------------------------------------- gather
-        // Thread gt owns pair row gt of each tile (its pid and query row);
-        // for the copies, lane l of warp gw moves 16-byte chunk (l & 7) of
-        // rows gw*32 + 4*i + (l >> 3), i < 8, taking the query row from the
-        // owning lane.  A tile's copies are published (wait, proxy fence,
-        // arrive) once kLag later tiles are in flight, or before any wait
-        // that may block.
-        constexpr int kLag = C::kNQ - 1;
-        const int gw = gather_index(warp), gt = gw * 32 + lane;
-        const int chunk = lane & 7, rsub = lane >> 3;
-        int g = 0, item_idx = 0, npend = 0;      // tiles g - npend .. g - 1 unpublished
-        bool ok = true;
-        auto flush = [&]() {
-            if (npend > 0) {
-                tc::cp_async_wait_pending<0>();
-                tc::fence_proxy_async_smem();
-                for (int t = g - npend; t < g; ++t) tc::mbar_arrive(bars + C::bQFull + t % C::kNQ);
-                npend = 0;
-            }
-        };
-        auto wait = [&](uint64_t *bar, uint32_t par) -> bool {
-            if (__all_sync(kFull, tc::mbar_test_wait(bar, par))) return true;
-            flush();
-            return __all_sync(kFull, tc::mbar_wait(bar, par, status));
-        };
-        for (int u = 0;; ++u) {
-            const int islot = u % kNI;
-            if (!wait(bars + C::bItFull + islot, (u / kNI) & 1)) {
-                ok = false;
-                break;
-            }
-            const StagedItem *si = items + islot;
-            if (!si->valid) break;
-            const int32_t first = si->first, end = si->end, bin = si->bin, rg = si->rg;
-            const int32_t kv = si->kv, qbase = si->qbase, roff = si->roff;
-            const int32_t ibase = si->ibase, j0 = si->j0;
-            if (gw == 0) {
-                if (rg >= kPartialRing) {
-                    // the ring entry must have been merged by its previous range
-                    flush();
-                    int got = 1;
-                    if (lane == 0)
-                        got = tc::wait_counter(a.merge_done + (rg - kPartialRing),
-                                           a.w.range_merges[rg - kPartialRing], status);
-                    if (!__shfl_sync(kFull, got, 0)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                const int ib = item_idx % C::kNKV;
-                if (item_idx >= C::kNKV && !wait(bars + C::bKvFree + ib, ((item_idx / C::kNKV) - 1) & 1)) {
-                    ok = false;
+            if (valid) {
+                // K_b and V_b into the item's buffer once the item three back is done
+                // with it (u counts valid items, as the gather's and owners' do)
+                const int ib = u % C::kNKV;
+                bool free_ok = true;
+                if (u >= C::kNKV)
+                    free_ok = __all_sync(kFull, tc::mbar_wait(bars + C::bKvFree + ib,
+                                                              ((u / C::kNKV) - 1) & 1, status));
+                if (!free_ok) {
+                    if (lane == 0) si->valid = 0;
+                    __syncwarp();
+                    tc::mbar_arrive(bars + C::bItFull + slot);
                     break;
                 }
                 if (lane == 0) {
@@ -427,13 +375,59 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     }
                 }
             }
+            __syncwarp();
+            tc::mbar_arrive(bars + C::bItFull + slot);
+            if (!valid) break;
+        }
+    } else if (gather_index(warp) >= 0) {
+        // --------------------------------------------------------- gather
+        // Thread gt owns pair row gt of each tile (its pid and query row);
+        // for the copies, lane l of warp gw moves 16-byte chunk (l & 7) of
+        // rows gw*32 + 4*i + (l >> 3), i < 8, taking the query row from the
+        // owning lane.  Each thread then arrives on the stage's barrier
+        // asynchronously: the arrival happens when its copies have landed,
+        // so a tile's Q rows are ready as soon as they are in shared memory
+        // and the gather never waits for its own copies.  (The K and V of an
+        // item are loaded by the prefetcher when it stages the item.)
+        const int gw = gather_index(warp), gt = gw * 32 + lane;
+        const int chunk = lane & 7, rsub = lane >> 3;
+        int g = 0, item_idx = 0;
+        int gx[2] = {0, 0};                      // tiles handed to each owner warpgroup
+        bool ok = true;
+        auto wait = [&](uint64_t *bar, uint32_t par) -> bool {
+            return __all_sync(kFull, tc::mbar_wait(bar, par, status));
+        };
+        for (int u = 0;; ++u) {
+            const int islot = u % kNI;
+            if (!wait(bars + C::bItFull + islot, (u / kNI) & 1)) {
+                ok = false;
+                break;
+            }
+            const StagedItem *si = items + islot;
+            if (!si->valid) break;
+            const int32_t first = si->first, end = si->end, bin = si->bin, rg = si->rg;
+            const int32_t kv = si->kv, qbase = si->qbase, roff = si->roff;
+            const int32_t ibase = si->ibase, j0 = si->j0;
+            if (gw == 0 && rg >= kPartialRing) {
+                // the ring entry must have been merged by its previous range
+                int got = 1;
+                if (lane == 0)
+                    got = tc::wait_counter(a.merge_done + (rg - kPartialRing),
+                                           a.w.range_merges[rg - kPartialRing], status);
+                if (!__shfl_sync(kFull, got, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            // every tile of an item goes to one owner warpgroup, items alternate
+            const int X = item_idx & 1;
             for (int32_t p0 = first; p0 < end; p0 += kTile) {
-                const int s = g % C::kNQ, slot = g % kNT;
+                const int s = g % C::kNQ, tx = gx[X], slot = X * kNTW + tx % kNTW;
                 if (g >= C::kNQ && !wait(bars + C::bQFree + s, ((g / C::kNQ) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                if (g >= kNT && !wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1)) {
+                if (tx >= kNTW && !wait(bars + C::bTiFree + slot, ((tx / kNTW) - 1) & 1)) {
                     ok = false;
                     break;
                 }
@@ -453,14 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     for (int sub = 0; sub < C::kSub; ++sub)   // rows past the pairs read as zeros
                         tc::cp_async16_zfill(dst + sub * kTile * 128, src + sub * 64, r < cnt);
                 }
-                tc::cp_async_commit();
-                if (npend == kLag) {
-                    tc::cp_async_wait_pending<kLag>();
-                    tc::fence_proxy_async_smem();
-                    tc::mbar_arrive(bars + C::bQFull + (g - kLag) % C::kNQ);
-                    --npend;
-                }
-                ++npend;
+                cp_async_arrive_noinc(bars + C::bQFull + s);
                 if (gt == 0) {
                     TileInfo x;
                     x.bin = bin;
@@ -475,291 +462,261 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     x.roff = roff;
                     x.ibase = ibase;
                     x.j0 = j0;
+                    x.g = g;
                     ti[slot] = x;
                 }
                 tc::mbar_arrive(bars + C::bTiFull + slot);
                 ++g;
+                ++gx[X];
             }
             if (!ok) break;
             tc::mbar_arrive(bars + C::bItFree + islot);
             ++item_idx;
         }
-        flush();
         if (ok) {
-            // end marker for the consumers
-            const int slot = g % kNT;
-            if (g < kNT || wait(bars + C::bTiFree + slot, ((g / kNT) - 1) & 1)) {
-                if (gt == 0) ti[slot].end = 1;
-                tc::mbar_arrive(bars + C::bTiFull + slot);
+            // an end marker for each owner warpgroup
+            for (int X = 0; X < 2; ++X) {
+                const int tx = gx[X], slot = X * kNTW + tx % kNTW;
+                if (tx < kNTW || wait(bars + C::bTiFree + slot, ((tx / kNTW) - 1) & 1)) {
+                    if (gt == 0) ti[slot].end = 1;
+                    tc::mbar_arrive(bars + C::bTiFull + slot);
+                }
             }
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------ MMA
-        // The whole warp runs an event loop with warp-uniform state (barrier
-        // probes are made by lane 0 and broadcast) and one elected lane
-        // issues: the S of the next tile or the P.V of the oldest tile whose
-        // P is in shared memory, whichever is ready first (both in tile
-        // order), so no P.V is ever held back.  Keeping the issuing code
-        // warp-uniform lets the MMAs issue back to back.
+    } else if (warp < 8) {
+        // ------------------------------------------------ owner warpgroups
+        // Warpgroup X (warps 4X .. 4X+3) runs every tile of its fine items
+        // from start to end, one thread per pair row: the issuing warp
+        // (the first of the group) waits for the tile's Q rows and its
+        // item's K_b, V_b and issues S = Q K_b^T into the group's S columns;
+        // every thread turns its row of S into P (bf16, into tensor memory)
+        // and (m, l); the issuing warp issues O = P V_b; every thread then
+        // stores its pair's partial state o = O / l (bf16) and
+        // lse = m + log2 l.  With two groups one runs its softmax or stores
+        // while the other's MMAs run.  Every wait's outcome is combined over
+        // the group at its named barriers, so the group leaves together.
+        // One thread counts the group's finished pairs per query range for
+        // the merges, up to four tiles under one GPU-scope fence; it counts
+        // at once whenever the group's next tile is not there yet, so that no
+        // count is held back while this CTA waits on others.
+        const int X = warp >> 2;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int wt = threadIdx.x & 127;        // thread within the group
+        const uint32_t bid = 2 + uint32_t(X);    // the group's named barrier
+        const uint32_t lane_off = uint32_t(quad * 32) << 16;
+        const uint32_t tS = tmem + uint32_t(X) * C::kWgCols, tP = tS + 64, tO = tS + 96;
+        uint64_t *b_tifull = bars + C::bTiFull + X * kNTW, *b_tifree = bars + C::bTiFree + X * kNTW;
+        uint64_t *b_sdone = bars + C::bSDone + X, *b_odone = bars + C::bODone + X;
+        uint8_t *eb = sm + C::oEpi + warp * 2048;
+        const int srow = lane >> 2, spiece = lane & 3;      // store phase: rows 8i + srow
         constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kTile, kB);
         constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kTile, D, /*b_mn_major=*/true);
-        int g1 = 0, g2 = 0;                       // next tile for S, next tile for P.V
-        int cur_item = -1, x_item = 0, x_last = 0;
-        int t_ib[4] = {0, 0, 0, 0}, t_last[4] = {0, 0, 0, 0};
-        bool end_seen = false, have_info = false;
-        uint64_t idle_since = 0;
-        auto probe = [&](uint64_t *bar, uint32_t par) -> bool {
-            return __shfl_sync(kFull, lane == 0 ? int(tc::mbar_test_wait(bar, par)) : 0, 0) != 0;
+        int cur_item = -1;                       // item whose K/V buffer is known to be full
+        int32_t pend_rg = -1, pend_cnt = 0, pend_rg2 = -1, pend_cnt2 = 0, pend_tiles = 0;
+        auto publish = [&]() {                   // thread wt == 32 only
+            if (pend_tiles > 0) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                if (pend_rg2 >= 0) atomicAdd(a.range_done + pend_rg2, pend_cnt2);
+                atomicAdd(a.range_done + pend_rg, pend_cnt);
+                pend_rg = pend_rg2 = -1;
+                pend_cnt = pend_cnt2 = pend_tiles = 0;
+            }
         };
-        for (uint32_t spin = 0;; ++spin) {
-            bool progressed = false;
-            if (g2 < g1) {
-                const int j = g2 % C::kNO;                // P and O buffer of tile g2
-                if (probe(bars + C::bPFull + j, (g2 / C::kNO) & 1) &&
-                    (g2 < C::kNO || probe(bars + C::bOFree + j, ((g2 / C::kNO) - 1) & 1))) {
+        for (int t = 0;; ++t) {
+            const int slot = t % kNTW;
+            const uint32_t par = (t / kNTW) & 1;
+            if (wt == 32 && pend_tiles > 0 && !tc::mbar_test_wait(b_tifull + slot, par)) publish();
+            bool ok = tc::mbar_wait(b_tifull + slot, par, status);
+            if (!tc::named_bar_and(bid, 128, ok)) break;
+            const volatile TileInfo *xi = ti + X * kNTW + slot;
+            if (xi->end) break;
+            const int32_t x_item = xi->item, x_g = xi->g, x_count = xi->count, x_last = xi->last;
+            const int32_t x_rg = xi->rg, x_qbase = xi->qbase, x_roff = xi->roff;
+            const int32_t *tpid = pids + (X * kNTW + slot) * kTile;
+            int keys_valid = xi->kv;                    // < 64: ragged last block
+            if (kOpts && a.causal && row < x_count) {
+                // causal: query i admits the keys j <= i of the block
+                const int32_t i = (tpid[row] >> 5) - x_qbase + xi->ibase;
+                keys_valid = min(keys_valid, i - xi->j0 + 1);   // <= 0: nothing admitted
+            }
+            const int s = x_g % C::kNQ, ib = x_item % C::kNKV;
+            // ---- S = Q K_b^T
+            bool issued = true;
+            if (quad == 0) {
+                if (x_item != cur_item)
+                    issued = tc::mbar_wait(bars + C::bKvFull + ib, (x_item / C::kNKV) & 1, status);
+                cur_item = x_item;
+                issued = issued && tc::mbar_wait(bars + C::bQFull + s, (x_g / C::kNQ) & 1, status);
+                issued = __all_sync(kFull, issued);
+                if (issued) {
+                    // the Q rows were written by cp.async (generic proxy); the MMA
+                    // reads them through the async proxy
+                    tc::fence_proxy_async_smem();
                     tc::tc_fence_after();
-                    const int ib = t_ib[g2 & 3];
                     if (tc::elect_one()) {
-                        const uint32_t av = tc::smem_u32(sm + C::oV + ib * C::kKBytes);
+                        const uint32_t aq = tc::smem_u32(sm + C::oQ + s * C::kQBytes);
+                        const uint32_t ak = tc::smem_u32(sm + C::oK + ib * C::kKBytes);
 #pragma unroll
-                        for (int kk = 0; kk < kB / 16; ++kk)
-                            tc::mma_bf16_ts(tmem + C::cO + uint32_t(j * D), tmem + C::cP + uint32_t(j * 32 + kk * 8),
-                                         tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
-                                         kk > 0);
-                        tc::mma_commit(bars + C::bOFull + j);
-                        tc::mma_commit(bars + C::bPFree + j);
-                        if (t_last[g2 & 3]) tc::mma_commit(bars + C::bKvFree + ib);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
+                            const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
+                            tc::mma_bf16(tS, tc::smem_desc_sw128(aq + off_q, 1024),
+                                         tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
+                        }
+                        tc::mma_commit(b_sdone);
+                        tc::mma_commit(bars + C::bQFree + s);
                     }
                     __syncwarp();
-                    ++g2;
-                    progressed = true;
                 }
             }
-            if (!end_seen && g1 - g2 < 3) {
-                const int slot = g1 % kNT;
-                if (!have_info && probe(bars + C::bTiFull + slot, (g1 / kNT) & 1)) {
-                    const volatile TileInfo *xi = ti + slot;
-                    if (xi->end) {
-                        end_seen = true;
-                    } else {
-                        have_info = true;
-                        x_item = xi->item;
-                        x_last = xi->last;
-                    }
-                    progressed = true;
-                }
-                if (have_info) {
-                    const int s = g1 % C::kNQ, j = g1 & 1, ib = x_item % C::kNKV;
-                    bool ready = x_item == cur_item || probe(bars + C::bKvFull + ib, (x_item / C::kNKV) & 1);
-                    ready = ready && probe(bars + C::bQFull + s, (g1 / C::kNQ) & 1);
-                    ready = ready && (g1 < 2 || probe(bars + C::bSFree + j, ((g1 >> 1) - 1) & 1));
-                    if (ready) {
-                        cur_item = x_item;
-                        tc::tc_fence_after();
-                        if (tc::elect_one()) {
-                            const uint32_t aq = tc::smem_u32(sm + C::oQ + s * C::kQBytes);
-                            const uint32_t ak = tc::smem_u32(sm + C::oK + ib * C::kKBytes);
+            // if the S was not issued, this wait runs out too
+            ok = tc::mbar_wait(b_sdone, uint32_t(t) & 1, status);
+            float m2 = -INFINITY, lrow = 0.f;
+            if (ok) {
+                // ---- softmax: all 64 scores of the row in one load.  Keys past
+                // `keys_valid` (a ragged last block, or the causal limit) are
+                // masked out; a warp whose rows are all full skips the masks.
+                // Both forms do the same arithmetic in the same order (a masked
+                // key adds an exact zero), so a row's result does not depend on
+                // which other rows share its tile.
+                tc::tc_fence_after();
+                uint32_t s0[32], s1[32];
+                tc::tmem_ld32(tS + lane_off, s0);
+                tc::tmem_ld32(tS + 32 + lane_off, s1);
+                tc::tmem_ld_wait();
+                const bool full = __all_sync(kFull, keys_valid == kB);
+                auto row_softmax = [&](auto masked) {
+                    constexpr bool kMasked = decltype(masked)::value;
+                    auto sc = [&](int c) -> float {       // score of key c, -inf when masked
+                        const float x = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+                        return (!kMasked || c < keys_valid) ? x : -INFINITY;
+                    };
+                    float mx[4];
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off_q = uint32_t((kk >> 2) * kTile * 128 + (kk & 3) * 32);
-                                const uint32_t off_k = uint32_t((kk >> 2) * kB * 128 + (kk & 3) * 32);
-                                tc::mma_bf16(tmem + uint32_t(j * kB), tc::smem_desc_sw128(aq + off_q, 1024),
-                                             tc::smem_desc_sw128(ak + off_k, 1024), idesc_s, kk > 0);
-                            }
-                            tc::mma_commit(bars + C::bSFull + j);
-                            tc::mma_commit(bars + C::bQFree + s);
+                    for (int u = 0; u < 4; ++u) {
+                        // 16 scores per chain, four independent chains
+                        float x[16];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            x[e] = sc(8 * u + e);
+                            x[8 + e] = sc(32 + 8 * u + e);
+                        }
+                        float m = fmax3(x[0], x[1], x[2]);
+#pragma unroll
+                        for (int e = 3; e < 15; e += 2) m = fmax3(m, x[e], x[e + 1]);
+                        mx[u] = fmaxf(m, x[15]);
+                    }
+                    m2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
+                    auto pr = [&](int c) -> float {       // p of key c, exactly 0 when masked
+                        const float x = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+                        return (!kMasked || c < keys_valid) ? ex2(fmaf(x, a.scale_log2, -m2)) : 0.f;
+                    };
+                    float lsum[4] = {0.f, 0.f, 0.f, 0.f};
+                    uint32_t pk0[16], pk1[16];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float p0 = pr(c), p1 = pr(c + 1), p2 = pr(c + 32), p3 = pr(c + 33);
+                        lsum[(c >> 1) & 3] += (p0 + p1) + (p2 + p3);
+                        pk0[c >> 1] = pack_bf16x2(p0, p1);
+                        pk1[c >> 1] = pack_bf16x2(p2, p3);
+                    }
+                    tc::tmem_st16(tP + lane_off, pk0);
+                    tc::tmem_st16(tP + 16 + lane_off, pk1);
+                    lrow = (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]);
+                };
+                if (full) row_softmax(std::false_type{});
+                else row_softmax(std::true_type{});
+                tc::tmem_st_wait();
+                tc::tc_fence_before();
+            }
+            // every row's P is in tensor memory
+            if (!tc::named_bar_and(bid, 128, ok && issued)) break;
+            // ---- O = P V_b
+            if (quad == 0) {
+                tc::tc_fence_after();
+                if (tc::elect_one()) {
+                    const uint32_t av = tc::smem_u32(sm + C::oV + ib * C::kKBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kB / 16; ++kk)
+                        tc::mma_bf16_ts(tO, tP + uint32_t(kk * 8),
+                                        tc::smem_desc_sw128_mn(av + kk * 2048, kB * 128, 1024), idesc_o,
+                                        kk > 0);
+                    tc::mma_commit(b_odone);
+                    if (x_last) tc::mma_commit(bars + C::bKvFree + ib);
+                }
+                __syncwarp();
+            }
+            ok = tc::mbar_wait(b_odone, uint32_t(t) & 1, status);
+            if (ok) {
+                // ---- epilogue: this row's pair state, the unnormalised O (bf16)
+                // and (m, l); the merge divides once per query.  O is read from
+                // TMEM 64 columns at a time;
+                // each 32-column chunk goes through a small swizzled shared
+                // buffer so that every store instruction writes 64 contiguous
+                // bytes of 8 rows instead of 16 bytes of 32 rows.
+                tc::tc_fence_after();
+                const bool has = row < x_count;
+                int32_t part = 0;                               // < kPartialRing * range * kpad
+                if (has) {
+                    const int32_t pid = tpid[row];
+                    part = x_roff + ((pid >> 5) - x_qbase) * int32_t(kpad) + (pid & 31);
+                }
+                int32_t sp[4];                                  // part of rows 8i + srow
+                bool sh[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sp[i] = __shfl_sync(kFull, part, 8 * i + srow);
+                    sh[i] = quad * 32 + 8 * i + srow < x_count;
+                }
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 64) {
+                    uint32_t ov[2][32];
+                    tc::tmem_ld32(tO + uint32_t(c0) + lane_off, ov[0]);
+                    tc::tmem_ld32(tO + uint32_t(c0 + 32) + lane_off, ov[1]);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 val = make_uint4(
+                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 0]), __uint_as_float(ov[hf][8 * v + 1])),
+                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 2]), __uint_as_float(ov[hf][8 * v + 3])),
+                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 4]), __uint_as_float(ov[hf][8 * v + 5])),
+                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 6]), __uint_as_float(ov[hf][8 * v + 7])));
+                            *reinterpret_cast<uint4 *>(eb + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
                         }
                         __syncwarp();
-                        t_ib[g1 & 3] = ib;
-                        t_last[g1 & 3] = x_last;
-                        ++g1;
-                        have_info = false;
-                        progressed = true;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int r = 8 * i + srow;
+                            const uint4 val =
+                                *reinterpret_cast<const uint4 *>(eb + r * 64 + ((spiece ^ ((r >> 1) & 3)) << 4));
+                            if (sh[i])
+                                *reinterpret_cast<uint4 *>(a.part_o + int64_t(sp[i]) * D + c0 + hf * 32 + spiece * 8) = val;
+                        }
+                        __syncwarp();
                     }
                 }
+                if (has) a.part_ml[part] = make_float2(m2, lrow);
+                tc::tc_fence_before();
             }
-            if (end_seen && g2 == g1) break;
-            if (progressed) {
-                idle_since = 0;
-            } else if ((spin & 63u) == 0) {
-                if (__shfl_sync(kFull, *reinterpret_cast<volatile int32_t *>(status), 0) == kStatusTimeout) break;
-                const uint64_t now = __shfl_sync(kFull, tc::global_ns(), 0);
-                if (idle_since == 0) {
-                    idle_since = now;
-                } else if (now - idle_since > tc::kWaitLimitNs) {
-                    if (lane == 0) report_status(status, kStatusTimeout);
-                    break;
+            // the group's stores are done and its tile slot is no longer read
+            if (!tc::named_bar_and(bid, 128, ok)) break;
+            if (wt == 0) tc::mbar_arrive(b_tifree + slot);
+            if (wt == 32) {
+                if (pend_tiles > 0 && x_rg != pend_rg && pend_rg2 >= 0) publish();
+                if (pend_tiles > 0 && x_rg != pend_rg) {
+                    pend_rg2 = pend_rg;
+                    pend_cnt2 = pend_cnt;
+                    pend_cnt = 0;
                 }
+                pend_rg = x_rg;
+                pend_cnt += x_count;
+                if (++pend_tiles >= 4) publish();
             }
         }
-        __syncwarp();
-    } else if (warp >= kWarpSoftmax && warp < kWarpEpi) {
-        // -------------------------------------------------------- softmax
-        // One thread per score row, in two passes over the row in TMEM (32
-        // columns at a time, rolled loops to keep the code small): the row
-        // max, then p = exp2(s * scale - m) written to P as bf16.
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const uint32_t lane_off = uint32_t(quad * 32) << 16;
-        for (int g = 0;; ++g) {
-            const int slot = g % kNT, j = g & 1, jp = g % C::kNO;   // S buffer, P buffer
-            if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
-            const int32_t end_flag = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
-            if (end_flag) break;
-            int keys_valid = reinterpret_cast<volatile TileInfo *>(ti + slot)->kv;   // < 64: ragged
-            if (kOpts && a.causal && row < reinterpret_cast<volatile TileInfo *>(ti + slot)->count) {
-                // causal: query i admits the keys j <= i of the block
-                const volatile TileInfo *x = ti + slot;
-                const int32_t i = (pids[slot * kTile + row] >> 5) - x->qbase + x->ibase;
-                keys_valid = min(keys_valid, i - x->j0 + 1);   // <= 0: nothing admitted
-            }
-            if (!tc::mbar_wait(bars + C::bSFull + j, (g >> 1) & 1, status)) break;
-            tc::tc_fence_after();
-            // All 64 scores of the row in one load; the S buffer is released at
-            // once.  Keys past `keys_valid` (a ragged last block, or the causal
-            // limit) are masked out; a warp whose rows are all full skips the
-            // masks.  Both forms do the same arithmetic in the same order (a
-            // masked key adds an exact zero), so a row's result does not depend
-            // on which other rows share its tile.
-            uint32_t s0[32], s1[32];
-            tc::tmem_ld32(tmem + uint32_t(j * kB) + lane_off, s0);
-            tc::tmem_ld32(tmem + uint32_t(j * kB + 32) + lane_off, s1);
-            tc::tmem_ld_wait();
-            tc::tc_fence_before();
-            tc::mbar_arrive(bars + C::bSFree + j);
-            const bool full = __all_sync(kFull, keys_valid == kB);
-            auto row_softmax = [&](auto masked) {
-                constexpr bool kMasked = decltype(masked)::value;
-                auto sc = [&](int c) -> float {       // score of key c, -inf when masked
-                    const float x = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
-                    return (!kMasked || c < keys_valid) ? x : -INFINITY;
-                };
-                float mx[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    // 16 scores per chain, four independent chains
-                    float x[16];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        x[e] = sc(8 * u + e);
-                        x[8 + e] = sc(32 + 8 * u + e);
-                    }
-                    float m = fmax3(x[0], x[1], x[2]);
-#pragma unroll
-                    for (int e = 3; e < 15; e += 2) m = fmax3(m, x[e], x[e + 1]);
-                    mx[u] = fmaxf(m, x[15]);
-                }
-                const float m2 = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * a.scale_log2;
-                auto pr = [&](int c) -> float {       // p of key c, exactly 0 when masked
-                    const float x = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
-                    return (!kMasked || c < keys_valid) ? ex2(fmaf(x, a.scale_log2, -m2)) : 0.f;
-                };
-                float lsum[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk0[16], pk1[16];
-#pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    const float p0 = pr(c), p1 = pr(c + 1), p2 = pr(c + 32), p3 = pr(c + 33);
-                    lsum[(c >> 1) & 3] += (p0 + p1) + (p2 + p3);
-                    pk0[c >> 1] = pack_bf16x2(p0, p1);
-                    pk1[c >> 1] = pack_bf16x2(p2, p3);
-                }
-                if (g >= C::kNO && !tc::mbar_wait(bars + C::bPFree + jp, ((g / C::kNO) - 1) & 1, status))
-                    return false;
-                tc::tmem_st16(tmem + C::cP + uint32_t(jp * 32) + lane_off, pk0);
-                tc::tmem_st16(tmem + C::cP + uint32_t(jp * 32 + 16) + lane_off, pk1);
-                // (m, l) live with the tile slot, which the gather group reuses
-                // only after this tile's epilogue is done
-                ml[slot * kTile + row] = make_float2(m2, (lsum[0] + lsum[1]) + (lsum[2] + lsum[3]));
-                return true;
-            };
-            const bool ok = full ? row_softmax(std::false_type{}) : row_softmax(std::true_type{});
-            if (!ok) break;
-            tc::mbar_arrive(bars + C::bMlFull + slot);
-            tc::tmem_st_wait();
-            tc::tc_fence_before();
-            tc::mbar_arrive(bars + C::bPFull + jp);
-        }
-    } else if (warp >= kWarpEpi && warp < kWarpEpi + 4) {
-        // ------------------------------------------------------- epilogue
-        // Thread `row` owns one pair: o = O / l (bf16) and lse = m + log2 l.
-        // O is read from TMEM 64 columns at a time (the buffer is released
-        // after the last read); each 32-column chunk goes through a small
-        // swizzled shared buffer so that every store instruction writes 64
-        // contiguous bytes of 8 rows instead of 16 bytes of 32 rows.
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        const int et = (warp - kWarpEpi) * 32 + lane;
-        const uint32_t lane_off = uint32_t(quad * 32) << 16;
-        uint8_t *eb = sm + C::oEpi + (warp - kWarpEpi) * 2048;
-        const int srow = lane >> 2, spiece = lane & 3;      // store phase: rows 8i + srow
-        for (int g = 0;; ++g) {
-            const int slot = g % kNT, jo = g % C::kNO;             // O buffer
-            if (!tc::mbar_wait(bars + C::bTiFull + slot, (g / kNT) & 1, status)) break;
-            const int32_t x_end = reinterpret_cast<volatile TileInfo *>(ti + slot)->end;
-            if (x_end) break;
-            const int32_t x_count = reinterpret_cast<volatile TileInfo *>(ti + slot)->count;
-            const int32_t x_rg = reinterpret_cast<volatile TileInfo *>(ti + slot)->rg;
-            const int32_t x_qbase = reinterpret_cast<volatile TileInfo *>(ti + slot)->qbase;
-            const int32_t x_roff = reinterpret_cast<volatile TileInfo *>(ti + slot)->roff;
-            if (!tc::mbar_wait(bars + C::bOFull + jo, (g / C::kNO) & 1, status)) break;
-            if (!tc::mbar_wait(bars + C::bMlFull + slot, (g / kNT) & 1, status)) break;
-            tc::tc_fence_after();
-            const float2 mlv = ml[slot * kTile + row];
-            const bool has = row < x_count;
-            int32_t part = 0;                               // < kPartialRing * range * kpad
-            if (has) {
-                const int32_t pid = pids[slot * kTile + row];
-                part = x_roff + ((pid >> 5) - x_qbase) * int32_t(kpad) + (pid & 31);
-            }
-            int32_t sp[4];                                    // part of rows 8i + srow
-            bool sh[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                sp[i] = __shfl_sync(kFull, part, 8 * i + srow);
-                sh[i] = quad * 32 + 8 * i + srow < x_count;
-            }
-            const float inv_l = 1.f / mlv.y;
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 64) {
-                uint32_t ov[2][32];
-                tc::tmem_ld32(tmem + C::cO + uint32_t(jo * D + c0) + lane_off, ov[0]);
-                tc::tmem_ld32(tmem + C::cO + uint32_t(jo * D + c0 + 32) + lane_off, ov[1]);
-                tc::tmem_ld_wait();
-                if (c0 + 64 == D) {
-                    tc::tc_fence_before();
-                    tc::mbar_arrive(bars + C::bOFree + jo);
-                }
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 val = make_uint4(
-                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 0]) * inv_l, __uint_as_float(ov[hf][8 * v + 1]) * inv_l),
-                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 2]) * inv_l, __uint_as_float(ov[hf][8 * v + 3]) * inv_l),
-                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 4]) * inv_l, __uint_as_float(ov[hf][8 * v + 5]) * inv_l),
-                            pack_bf16x2(__uint_as_float(ov[hf][8 * v + 6]) * inv_l, __uint_as_float(ov[hf][8 * v + 7]) * inv_l));
-                        *reinterpret_cast<uint4 *>(eb + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = 8 * i + srow;
-                        const uint4 val =
-                            *reinterpret_cast<const uint4 *>(eb + r * 64 + ((spiece ^ ((r >> 1) & 3)) << 4));
-                        if (sh[i])
-                            *reinterpret_cast<uint4 *>(a.part_o + int64_t(sp[i]) * D + c0 + hf * 32 + spiece * 8) = val;
-                    }
-                    __syncwarp();
-                }
-            }
-            if (has) a.part_lse[part] = mlv.x + __log2f(mlv.y);
-            // the group's partial stores happen before one release-add
-            tc::named_bar_sync(kBarEpi, 128);
-            if (et == 0) {
-                red_add_release(a.range_done + x_rg, x_count);
-                tc::mbar_arrive(bars + C::bTiFree + slot);
-            }
-        }
+        if (wt == 32) publish();
     } else if (merge_index(warp) >= 0) {
         // ---------------------------------------------------------- merge
         // Each merge warp runs on its own: it takes a merge item, waits for
@@ -774,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         const int n_merge = *a.w.n_merge;
         const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;
         const uint32_t full_mask = full_valid >= 32 ? kFull : ((1u << full_valid) - 1u);
-        const int64_t per_q = kpad * D * 2 + kpad * 4;
+        const int64_t per_q = kpad * D * 2 + kpad * 8;
         const int qs = int(kStageBytes / per_q);                  // queries per stage (>= 2)
         const int64_t o_cap = int64_t(qs) * kpad * D * 2;         // lse offset within a stage
         uint8_t *stage0 = sm + C::oMs + mw * C::kMS * kStageBytes;
@@ -804,12 +761,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             auto issue = [&](int c) {                // lane 0: chunk c into its stage
                 const uint32_t b = (sc + uint32_t(c)) % C::kMS;
                 const int qn = min(qs, nq - c * qs);
-                const uint32_t bo = uint32_t(qn * kpad * D * 2), bl = uint32_t(qn * kpad * 4);
+                const uint32_t bo = uint32_t(qn * kpad * D * 2), bl = uint32_t(qn * kpad * 8);
                 const int64_t sl = slot0 + int64_t(c) * qs * kpad;
                 uint8_t *st = stage0 + b * kStageBytes;
                 tc::mbar_arrive_expect_tx(msbar + b, bo + bl);
                 tc::bulk_g2s(st, a.part_o + sl * D, bo, msbar + b);
-                tc::bulk_g2s(st + o_cap, a.part_lse + sl, bl, msbar + b);
+                tc::bulk_g2s(st + o_cap, a.part_ml + sl, bl, msbar + b);
             };
             if (lane == 0)
                 for (int c = 0; c < min(C::kMS, nch); ++c) issue(c);
@@ -844,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     }
                     float acc[16];
                     const uint16_t *po = reinterpret_cast<const uint16_t *>(st) + jq * kpad * D + gl * 16;
-                    const float *pl = reinterpret_cast<const float *>(st + o_cap) + jq * kpad;
+                    const float *pl = reinterpret_cast<const float *>(st + o_cap) + 2 * jq * kpad;
                     // every lane takes part (the merge shuffles across the warp); a
                     // query with nothing listed was zeroed by the inversion, one
                     // whose listed blocks admit nothing (causal mask) is zeroed here
@@ -872,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
 
     tc::tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == 0) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, C::kTmemCols);
     }
