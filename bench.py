@@ -570,12 +570,16 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
     torch.cuda.synchronize(device)
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     pairs = admitted_pairs(fwd.idx, w)
-    # per admitted (query, key) pair: q.k, dO.v, dQ, dK and dV updates (2d each) + softmax ops
+    # per admitted (query, key) pair: q.k, dO.v, dQ, dK and dV updates (2d each,
+    # tensor cores) + softmax ops; the forward pass the backward repeats for the
+    # rows' log2-sum-exp is not credited
     flops = pairs * (10 * w.d + 5)
     peaks = measured_peaks()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    p_fp32 = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6
     achieved = flops / (ms * 1e-3) / 1e12
+    rl = roofline(10 * w.d * pairs, 5 * pairs, 5 * w.n * w.bh * w.d * 2 + 3 * w.n * w.bh * w.d * 4,
+                  ms, peaks, sms, "fine-stage backward: one bsa_fine_backward call (forward pass for "
+                  "the rows' log2-sum-exp, D = dO.O, list inversion, tensor-core dQ/dK/dV kernel)", None)
     status = bsa.device_status()
     if dist is not None:
         dist.destroy_process_group()
@@ -584,9 +588,7 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
         "value": achieved, "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps,
         "warmup": args.warmup, "n_gpus": 1, "higher_is_better": True, "dtype": "bf16 in, fp32",
         "data": "synthetic", "config": config_of(w),
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": p_fp32 / 1e12,
-                     "unit": "TFLOP/s", "frac": achieved * 1e12 / p_fp32,
-                     "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 x max clock"},
+        "roofline": rl,
         "admitted_pairs": pairs, "flops_per_step": flops, "device_status": status}), flush=True)
     return 0 if status == 0 else 1
 

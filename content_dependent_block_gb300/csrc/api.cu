@@ -202,7 +202,8 @@ bool bm_path(const bsa_shape &s, int32_t kb, int64_t nb) {
 cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const void *v,
                         const int32_t *list, int32_t kb, int32_t topk, bool full_lists,
                         bool causal, const bsa::SelectOpts *sel, float scale_log2, void *out,
-                        char *ws, const BmLayout &L, int32_t *status, cudaStream_t st) {
+                        char *ws, const BmLayout &L, int32_t *status, cudaStream_t st,
+                        float *lse_out = nullptr) {
     const int64_t nb = ceil_div(s.n, kb);
     cudaError_t e = cudaMemsetAsync(ws + L.zero, 0, L.zero_bytes, st);
     if (e != cudaSuccess) return e;
@@ -247,6 +248,7 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     a.part_o = reinterpret_cast<uint16_t *>(ws + L.part_o);
     a.part_ml = reinterpret_cast<float2 *>(ws + L.part_lse);
     a.out = static_cast<uint16_t *>(out);
+    a.lse_out = lse_out;
     a.status = status;
     return bsa::launch_fine_bm(a, st);
 }
@@ -532,7 +534,15 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
 // ---------------------------------------------------------- backward pass
 struct BwdLayout {
     size_t lse = 0, dsum = 0, counts = 0, cursors = 0, offsets = 0, qlist = 0, total = 0;
+    size_t o_scratch = 0, fwd = 0;     // tensor-core path only
 };
+
+// The tensor-core backward (64-key blocks, at most 32 per query) also runs
+// one block-major forward fine stage for the rows' log2-sum-exp: its
+// workspace and a scratch output follow the backward's own buffers.
+bool bwd_tc_path(const bsa_shape &s, int32_t kb, int32_t k) {
+    return bsa::fine_backward_tc_supported(s.d, kb, k) && bm_path(s, kb, ceil_div(s.n, kb));
+}
 
 BwdLayout bwd_layout(const bsa_shape &s, int32_t kb, int32_t k) {
     BwdLayout L;
@@ -549,6 +559,11 @@ BwdLayout bwd_layout(const bsa_shape &s, int32_t kb, int32_t k) {
     L.cursors = take(bins * 4);
     L.offsets = take((bins + 1) * 4);
     L.qlist = take(rows * size_t(k) * 4);
+    if (bwd_tc_path(s, kb, k)) {
+        L.o_scratch = take(rows * size_t(s.d) * 2);
+        L.fwd = at;
+        at = bm_layout(s, kb, k, at).total;
+    }
     L.total = at;
     return L;
 }
@@ -622,6 +637,14 @@ bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, cons
     a.offsets = reinterpret_cast<int32_t *>(base + L.offsets);
     a.qlist = reinterpret_cast<int32_t *>(base + L.qlist);
     a.status = status;
+    if (bwd_tc_path(shape, ld.key_block, ld.max_blocks)) {
+        // the forward fine stage once more, for every row's log2-sum-exp
+        const BmLayout F = bm_layout(shape, ld.key_block, ld.max_blocks, L.fwd);
+        e = run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false, a.causal != 0,
+                        nullptr, a.scale_log2, base + L.o_scratch, base, F, status, st, a.lse);
+        if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "backward (forward pass): %s", cudaGetErrorString(e));
+        return launched(bsa::launch_fine_backward_tc(a, st), "backward launch");
+    }
     return launched(bsa::launch_fine_backward(a, st), "backward launch");
 }
 

@@ -21,6 +21,7 @@
 
 #include "bsa_device.cuh"
 #include "bsa_internal.h"
+#include "tc.cuh"
 
 namespace bsa {
 namespace {
@@ -290,6 +291,303 @@ __global__ void __launch_bounds__(512) bwd_kv_kernel(const BwdArgs a) {
     }
 }
 
+// D_i = dO_i . O_i, one warp per query row (the forward's bf16 output).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dsum_kernel(const BwdArgs a) {
+    const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= a.bh * a.n) return;
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+        const int c = lane + 32 * e;
+        s = fmaf(bf(a.dout[row * D + c]), bf(a.out[row * D + c]), s);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+    if (lane == 0) a.dsum[row] = s;
+}
+
+// ------------------------------------------------------------------------
+// Tensor-core backward for 64-key blocks: one CTA of 128 threads per (head,
+// block) bin -- the queries that listed the block, in tiles of 128 rows, one
+// thread per row.  Per tile (every product on the tensor cores, bf16 operands
+// in 128-byte-swizzled shared memory, fp32 accumulators in tensor memory):
+//   S  = Q K_b^T, dP = dO V_b^T                     (M 128, N 64, K d)
+//   P  = 2^(S scale log2e - lse_i), dS = scale P (dP - D_i)   (one thread per row)
+//   dV_b += P^T dO, dK_b += dS^T Q                  (M 64 keys, N d, K 128 queries:
+//                                                    P, dS and dO, Q read MN-major)
+//   dQ_i += dS K_b                                   (M 128, N d, K 64; added into dQ
+//                                                    with vector atomics, since a
+//                                                    query's blocks are different bins)
+// dK_b and dV_b stay in tensor memory across the bin's tiles and are written
+// once (their rows of an M = 64 accumulator sit in the first 16 lanes of each
+// warp's lane quadrant).  lse_i comes from the forward's merge, D_i from
+// bwd_dsum_kernel.  Every wait is bounded, and its outcome is combined over
+// the CTA at the next barrier so that all threads leave together.
+template <int D>
+struct BwdTc {
+    static constexpr int kSub = D / 64;
+    static constexpr int kKB = 64;                       // keys per block
+    static constexpr int kRows = 128;
+    static constexpr int kKvBytes = kSub * kKB * 128;    // K_b or V_b
+    static constexpr int kRowBytes = kSub * kRows * 128; // Q or dO tile
+    static constexpr int kPBytes = kRows * 128;          // P or dS tile (64 keys)
+    static constexpr int oK = 0, oV = oK + kKvBytes, oQ = oV + kKvBytes, oDo = oQ + kRowBytes;
+    static constexpr int oP = oDo + kRowBytes, oDs = oP + kPBytes, oBar = oDs + kPBytes;
+    static constexpr int kSmem = oBar + 64 + 1024;
+    // tensor memory: S and dP, dQ over them once they are read; dK and dV
+    static constexpr uint32_t cS = 0, cDp = 64, cDq = 0, cDk = 128, cDv = 128 + D;
+    static constexpr uint32_t kCols = D == 64 ? 256 : 512;
+    static_assert(cDv + D <= kCols, "tensor memory");
+};
+
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// Row r of a [rows][64-column sub-tiles] bf16 tile in the 128-byte-swizzled
+// K-major layout: 16-byte chunk c of row r at chunk c ^ (r & 7).
+__device__ __forceinline__ uint8_t *swz(uint8_t *tile, int r, int c) {
+    return tile + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) bwd_tc_kernel(const BwdArgs a) {
+    using C = BwdTc<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = tc::align_smem_1024(smem_raw);
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(sm + C::oBar);
+    uint64_t *bar_g = bar_s + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 2);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int64_t h = blockIdx.y, b = blockIdx.x;
+    const int64_t bin = h * a.nb + b;
+    const int32_t q0 = a.offsets[bin], nq = a.offsets[bin + 1] - q0;
+    const int64_t j0 = b * C::kKB;
+    const int kv_all = int(i64min(C::kKB, a.n - j0));    // keys of the block inside the sequence
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    if (nq == 0) {
+        // no query listed the block: its gradients are zero
+        const int kr = t >> 1, half = t & 1;
+        if (kr < kv_all) {
+            float *dk = a.dk + (h * a.n + j0 + kr) * D + half * (D / 2);
+            float *dv = a.dv + (h * a.n + j0 + kr) * D + half * (D / 2);
+            for (int c = 0; c < D / 2; c += 4) {
+                *reinterpret_cast<float4 *>(dk + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4 *>(dv + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        return;
+    }
+    if (t == 0) {
+        tc::mbar_init(bar_s, 1);
+        tc::mbar_init(bar_g, 1);
+        tc::fence_barrier_init();
+    }
+    if (warp == 0) {
+        tc::tmem_alloc(tmem_slot, C::kCols);
+        tc::tmem_relinquish();
+    }
+    // K_b and V_b rows (threads 0-63 and 64-127); keys past the sequence read as zeros
+    {
+        const int r = t & 63;
+        const bool is_v = t >= 64;
+        const bool ok = r < kv_all;
+        const uint16_t *src = (is_v ? a.vp : a.kp) + (h * a.n + j0 + (ok ? r : 0)) * D;
+        uint8_t *dst = sm + (is_v ? C::oV : C::oK);
+#pragma unroll
+        for (int sub = 0; sub < C::kSub; ++sub)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                tc::cp_async16_zfill(swz(dst + sub * C::kKB * 128, r, c), src + sub * 64 + c * 8, ok);
+    }
+    tc::cp_async_commit();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t aK = tc::smem_u32(sm + C::oK), aV = tc::smem_u32(sm + C::oV);
+    const uint32_t aQ = tc::smem_u32(sm + C::oQ), aDo = tc::smem_u32(sm + C::oDo);
+    const uint32_t aP = tc::smem_u32(sm + C::oP), aDs = tc::smem_u32(sm + C::oDs);
+    constexpr uint32_t id_sdp = tc::idesc_bf16_f32(C::kRows, C::kKB);
+    // dV, dK: A (P or dS transposed) and B (dO or Q) both stored N- / M-contiguous
+    constexpr uint32_t id_kv = tc::idesc_bf16_f32(C::kKB, D, /*b_mn_major=*/true) | (1u << 15);
+    constexpr uint32_t id_q = tc::idesc_bf16_f32(C::kRows, D, /*b_mn_major=*/true);
+    const int ntiles = (nq + C::kRows - 1) / C::kRows;
+    bool ok = true;
+    for (int tile = 0; tile < ntiles; ++tile) {
+        // ---- this row's query, its Q and dO rows, lse and D
+        const int rr = tile * C::kRows + t;
+        const bool live = rr < nq;
+        const int32_t i = live ? a.qlist[q0 + rr] : 0;
+        const int64_t qrow = h * a.n + i;
+        {
+            const uint16_t *sq = a.q + qrow * D, *sdo = a.dout + qrow * D;
+#pragma unroll
+            for (int sub = 0; sub < C::kSub; ++sub)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    tc::cp_async16_zfill(swz(sm + C::oQ + sub * C::kRows * 128, t, c), sq + sub * 64 + c * 8, live);
+                    tc::cp_async16_zfill(swz(sm + C::oDo + sub * C::kRows * 128, t, c), sdo + sub * 64 + c * 8, live);
+                }
+        }
+        const float lse = live ? a.lse[qrow] : -INFINITY;
+        const float dsum = live ? a.dsum[qrow] : 0.f;
+        int kv = kv_all;
+        if (a.causal) kv = int(i64min(kv, int64_t(i) - j0 + 1));   // keys j <= i
+        if (!live || !(lse > -INFINITY)) kv = 0;                      // the row adds nothing
+        tc::cp_async_wait_all();
+        tc::fence_proxy_async_smem();            // cp.async writes -> the MMAs' reads
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+        // ---- S and dP
+        if (t == 0) {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t oq = uint32_t((kk >> 2) * C::kRows * 128 + (kk & 3) * 32);
+                const uint32_t ok_ = uint32_t((kk >> 2) * C::kKB * 128 + (kk & 3) * 32);
+                tc::mma_bf16(tmem + C::cS, tc::smem_desc_sw128(aQ + oq, 1024), tc::smem_desc_sw128(aK + ok_, 1024),
+                             id_sdp, kk > 0);
+                tc::mma_bf16(tmem + C::cDp, tc::smem_desc_sw128(aDo + oq, 1024), tc::smem_desc_sw128(aV + ok_, 1024),
+                             id_sdp, kk > 0);
+            }
+            tc::mma_commit(bar_s);
+        }
+        ok = tc::mbar_wait(bar_s, uint32_t(tile) & 1, a.status);
+        // ---- P and dS, one row per thread
+        if (ok) {
+            tc::tc_fence_after();
+            uint32_t sv[2][32], dpv[2][32];
+            tc::tmem_ld32(tmem + C::cS + lane_off, sv[0]);
+            tc::tmem_ld32(tmem + C::cS + 32 + lane_off, sv[1]);
+            tc::tmem_ld32(tmem + C::cDp + lane_off, dpv[0]);
+            tc::tmem_ld32(tmem + C::cDp + 32 + lane_off, dpv[1]);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                uint32_t pk[4], dk[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    float p2[2], d2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int c = c8 * 8 + e + u;
+                        const float sc = __uint_as_float(sv[c >> 5][c & 31]);
+                        const float dp = __uint_as_float(dpv[c >> 5][c & 31]);
+                        const float p = c < kv ? ex2(fmaf(sc, a.scale_log2, -lse)) : 0.f;
+                        p2[u] = p;
+                        d2[u] = p * (dp - dsum) * a.scale;
+                    }
+                    pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                    dk[e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                }
+                *reinterpret_cast<uint4 *>(swz(sm + C::oP, t, c8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(swz(sm + C::oDs, t, c8)) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+            }
+        }
+        tc::fence_proxy_async_smem();            // P, dS stores -> the MMAs' reads
+        tc::tc_fence_before();
+        if (!__syncthreads_and(ok)) {            // S and dP read; P and dS written
+            ok = false;
+            break;
+        }
+        tc::tc_fence_after();
+        // ---- dV += P^T dO, dK += dS^T Q, dQ = dS K_b
+        if (t == 0) {
+#pragma unroll
+            for (int kq = 0; kq < C::kRows / 16; ++kq) {
+                const uint32_t off = uint32_t(kq * 2048);       // 16 query rows
+                const uint32_t acc = (tile > 0 || kq > 0) ? 1u : 0u;
+                tc::mma_bf16(tmem + C::cDv, tc::smem_desc_sw128_mn(aP + off, 8192, 1024),
+                             tc::smem_desc_sw128_mn(aDo + off, C::kRows * 128, 1024), id_kv, acc);
+                tc::mma_bf16(tmem + C::cDk, tc::smem_desc_sw128_mn(aDs + off, 8192, 1024),
+                             tc::smem_desc_sw128_mn(aQ + off, C::kRows * 128, 1024), id_kv, acc);
+            }
+#pragma unroll
+            for (int kk = 0; kk < C::kKB / 16; ++kk)
+                tc::mma_bf16(tmem + C::cDq, tc::smem_desc_sw128(aDs + uint32_t(kk * 32), 1024),
+                             tc::smem_desc_sw128_mn(aK + uint32_t(kk * 2048), C::kKB * 128, 1024), id_q, kk > 0);
+            tc::mma_commit(bar_g);
+        }
+        ok = tc::mbar_wait(bar_g, uint32_t(tile) & 1, a.status);
+        // ---- dQ of this row into the global sum
+        if (ok) {
+            tc::tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(tmem + C::cDq + uint32_t(c0) + lane_off, v);
+                tc::tmem_ld_wait();
+                if (kv > 0) {
+                    float *dst = a.dq + qrow * D + c0;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        red_add_v4(dst + c, __uint_as_float(v[c]), __uint_as_float(v[c + 1]),
+                                   __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+                }
+            }
+        }
+        tc::tc_fence_before();
+        if (!__syncthreads_and(ok)) {            // dQ read; next tile may overwrite
+            ok = false;
+            break;
+        }
+    }
+    // ---- dK_b and dV_b: row kr of the M = 64 accumulators is lane 32 (kr / 16) + kr % 16
+    if (ok) {
+        tc::tc_fence_after();
+        const int kr = warp * 16 + lane;
+        const bool mine = lane < 16 && kr < kv_all;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t vk[32], vv[32];
+            tc::tmem_ld32(tmem + C::cDk + uint32_t(c0) + lane_off, vk);
+            tc::tmem_ld32(tmem + C::cDv + uint32_t(c0) + lane_off, vv);
+            tc::tmem_ld_wait();
+            if (mine) {
+                float *dk = a.dk + (h * a.n + j0 + kr) * D + c0;
+                float *dv = a.dv + (h * a.n + j0 + kr) * D + c0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    *reinterpret_cast<float4 *>(dk + c) = make_float4(
+                        __uint_as_float(vk[c]), __uint_as_float(vk[c + 1]), __uint_as_float(vk[c + 2]),
+                        __uint_as_float(vk[c + 3]));
+                    *reinterpret_cast<float4 *>(dv + c) = make_float4(
+                        __uint_as_float(vv[c]), __uint_as_float(vv[c + 1]), __uint_as_float(vv[c + 2]),
+                        __uint_as_float(vv[c + 3]));
+                }
+            }
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, C::kCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_tc_d(const BwdArgs &a, cudaStream_t st) {
+    const int64_t rows = a.bh * a.n;
+    bwd_dsum_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, st>>>(a);
+    const dim3 ge(unsigned((a.n * a.k + 255) / 256), unsigned(a.bh));
+    bwd_count_kernel<<<ge, 256, 0, st>>>(a);
+    bwd_scan_kernel<<<1, kScanThreads, 0, st>>>(a);
+    bwd_scatter_kernel<<<ge, 256, 0, st>>>(a);
+    cudaError_t e = cudaMemsetAsync(a.dq, 0, size_t(rows) * D * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    auto kern = bwd_tc_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdTc<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(unsigned(a.nb), unsigned(a.bh)), 128, BwdTc<D>::kSmem, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_d(const BwdArgs &a, cudaStream_t st) {
     const dim3 gq(unsigned((a.n + kQWarps - 1) / kQWarps), unsigned(a.bh));
@@ -306,6 +604,15 @@ cudaError_t launch_d(const BwdArgs &a, cudaStream_t st) {
 
 bool fine_backward_supported(int32_t d, int32_t kb) {
     return (d == 64 || d == 128) && kb * (d / 16) <= 512;
+}
+
+bool fine_backward_tc_supported(int32_t d, int32_t kb, int32_t k) {
+    return (d == 64 || d == 128) && kb == 64 && k >= 1 && k <= 32;
+}
+
+cudaError_t launch_fine_backward_tc(const BwdArgs &a, cudaStream_t st) {
+    if (!fine_backward_tc_supported(a.d, a.kb, a.k)) return cudaErrorInvalidValue;
+    return a.d == 64 ? launch_tc_d<64>(a, st) : launch_tc_d<128>(a, st);
 }
 
 cudaError_t launch_fine_backward(const BwdArgs &a, cudaStream_t st) {

@@ -60,6 +60,11 @@ struct BwdArgs {
 };
 bool fine_backward_supported(int32_t d, int32_t kb);   // one CTA of kb * d / 16 <= 512 threads
 cudaError_t launch_fine_backward(const BwdArgs &a, cudaStream_t st);
+// Tensor-core backward (64-key blocks, at most 32 per query): a.lse must hold
+// every query's log2-sum-exp (the forward's merge writes it); a.dsum and the
+// inversion buffers are filled here; dq is zeroed and accumulated.
+bool fine_backward_tc_supported(int32_t d, int32_t kb, int32_t k);
+cudaError_t launch_fine_backward_tc(const BwdArgs &a, cudaStream_t st);
 
 // One small kernel whose bounded wait nothing completes (kind 0: an mbarrier,
 // 1: a global counter); it records BSA_ERR_TIMEOUT after about limit_ns.
@@ -147,6 +152,8 @@ struct FineBmArgs {
     uint16_t *part_o;             // [ring][range * kpad][d] bf16
     float2 *part_ml;              // [ring][range * kpad] (m, l) of each pair, log2 units
     uint16_t *out;
+    float *lse_out;               // optional [bh * n]: each query's log2-sum-exp over
+                                  // its admitted keys (-inf when none), for the backward
     int32_t *status;
 };
 bool fine_bm_supported(int32_t d, int32_t key_block);

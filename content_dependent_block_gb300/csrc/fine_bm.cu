@@ -170,12 +170,13 @@ __device__ __forceinline__ float ex2(float x) {
 // shared by shuffles.  Neighbouring queries read their two chunks in
 // opposite order, so that a quarter warp touches all 32 banks once.  The
 // slot loop is rolled (four slots per trip) to keep the code small.  Returns
-// false when nothing is listed; else acc holds the merged channels.  kOpts:
+// false when nothing is listed; else acc holds the merged channels and lse
+// the query's log2-sum-exp, M + log2 sum_s w_s l_s.  kOpts:
 // a listed slot may hold a partial that admitted no key (m = -inf, under the
 // causal mask); it weighs 0.
 template <int D, bool kOpts>
 __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pml, uint32_t vm, int k,
-                                            int lane, float (&acc)[16]) {
+                                            int lane, float (&acc)[16], float &lse) {
     constexpr int LPQ = D / 16;
     constexpr int SPL = 32 / LPQ;              // slots per lane (k <= 32)
     const int gl = lane % LPQ, gbase = lane - gl;
@@ -235,6 +236,7 @@ __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pml
             for (int t = 0; t + 1 < SPL; ++t) w[t] = w[t + 1];
         }
     }
+    lse = L > 0.f ? M + __log2f(L) : -INFINITY;
     if (L == 0.f) return false;
     const float invL = 1.f / L;
 #pragma unroll
@@ -805,7 +807,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     // every lane takes part (the merge shuffles across the warp); a
                     // query with nothing listed was zeroed by the inversion, one
                     // whose listed blocks admit nothing (causal mask) is zeroed here
-                    const bool any = merge_query<D, kOpts>(po, pl, vm, k, lane, acc);
+                    float lse = -INFINITY;
+                    const bool any = merge_query<D, kOpts>(po, pl, vm, k, lane, acc, lse);
+                    if (a.lse_out != nullptr && act && gl == 0) a.lse_out[qrow] = lse;
                     if (act && (any || kOpts)) {
                         if (!any) {
 #pragma unroll

@@ -1,4 +1,5 @@
-"""CUDA backward pass of the fine stage vs the fp64 oracle (lists fixed).
+"""Backward pass of the fine stage vs the fp64 oracle (lists fixed): the
+tensor-core kernel for 64-key blocks, the CUDA-core kernels for other sizes.
 
 The GPU takes D_i = dO_i . O_i from the bf16 forward output, the oracle the
 exact sum_j p_ij dP_ij; the bf16 rounding of O (2^-9 relative) bounds the
@@ -59,6 +60,12 @@ def _random_lists(bh, n, kb, k, seed, causal):
     (1, 700, 128, 64, 4, True, "selected"),
     (2, 513, 64, 32, 6, False, "random"),        # empty rows, one-token last block
     (1, 300, 128, 32, 16, True, "random"),
+    # 64-key blocks run on the tensor cores: random lists with empty rows, a
+    # one-token last block, the causal mask, d 128, more than one 128-row tile
+    # per block
+    (2, 513, 64, 64, 6, False, "random"),
+    (1, 300, 128, 64, 5, True, "random"),
+    (2, 4100, 64, 64, 16, True, "selected"),
 ])
 def test_backward_matches_oracle(bh, n, d, kb, k, causal, lists):
     import torch
