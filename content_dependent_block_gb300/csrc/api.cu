@@ -555,15 +555,17 @@ BwdLayout bwd_layout(const bsa_shape &s, int32_t kb, int32_t k) {
     };
     L.lse = take(rows * 4);
     L.dsum = take(rows * 4);
+    if (bwd_tc_path(s, kb, k)) {
+        // the forward fine stage's workspace holds the lists' inversion
+        L.o_scratch = take(rows * size_t(s.d) * 2);
+        L.fwd = at;
+        L.total = bm_layout(s, kb, k, at).total;
+        return L;
+    }
     L.counts = take(bins * 4);
     L.cursors = take(bins * 4);
     L.offsets = take((bins + 1) * 4);
     L.qlist = take(rows * size_t(k) * 4);
-    if (bwd_tc_path(s, kb, k)) {
-        L.o_scratch = take(rows * size_t(s.d) * 2);
-        L.fwd = at;
-        at = bm_layout(s, kb, k, at).total;
-    }
     L.total = at;
     return L;
 }
@@ -608,9 +610,13 @@ bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, cons
     if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     char *base = static_cast<char *>(ws);
-    // counts and cursors are adjacent: one memset
-    cudaError_t e = cudaMemsetAsync(base + L.counts, 0, L.offsets - L.counts, st);
-    if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    const bool tc_path = bwd_tc_path(shape, ld.key_block, ld.max_blocks);
+    cudaError_t e = cudaSuccess;
+    if (!tc_path) {
+        // counts and cursors are adjacent: one memset
+        e = cudaMemsetAsync(base + L.counts, 0, L.offsets - L.counts, st);
+        if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "memset: %s", cudaGetErrorString(e));
+    }
     bsa::BwdArgs a{};
     a.q = static_cast<const uint16_t *>(q);
     a.kp = static_cast<const uint16_t *>(k);
@@ -637,12 +643,16 @@ bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, cons
     a.offsets = reinterpret_cast<int32_t *>(base + L.offsets);
     a.qlist = reinterpret_cast<int32_t *>(base + L.qlist);
     a.status = status;
-    if (bwd_tc_path(shape, ld.key_block, ld.max_blocks)) {
-        // the forward fine stage once more, for every row's log2-sum-exp
+    if (tc_path) {
+        // the forward fine stage once more: every row's log2-sum-exp, and the
+        // lists inverted by (head, query range, block)
         const BmLayout F = bm_layout(shape, ld.key_block, ld.max_blocks, L.fwd);
         e = run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false, a.causal != 0,
                         nullptr, a.scale_log2, base + L.o_scratch, base, F, status, st, a.lse);
         if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "backward (forward pass): %s", cudaGetErrorString(e));
+        a.bin_offsets = reinterpret_cast<const int32_t *>(base + F.offsets);
+        a.entries = reinterpret_cast<const int32_t *>(base + F.entries);
+        a.nranges = F.plan.nranges;
         return launched(bsa::launch_fine_backward_tc(a, st), "backward launch");
     }
     return launched(bsa::launch_fine_backward(a, st), "backward launch");

@@ -310,7 +310,8 @@ __global__ void __launch_bounds__(256) bwd_dsum_kernel(const BwdArgs a) {
 
 // ------------------------------------------------------------------------
 // Tensor-core backward for 64-key blocks: one CTA of 128 threads per (head,
-// block) bin -- the queries that listed the block, in tiles of 128 rows, one
+// block) -- the queries that listed the block, read from the forward fine
+// stage's inversion (one bin per query range), in tiles of 128 rows, one
 // thread per row.  Per tile (every product on the tensor cores, bf16 operands
 // in 128-byte-swizzled shared memory, fp32 accumulators in tensor memory):
 //   S  = Q K_b^T, dP = dO V_b^T                     (M 128, N 64, K d)
@@ -364,8 +365,11 @@ __global__ void __launch_bounds__(128) bwd_tc_kernel(const BwdArgs a) {
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar_s + 2);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t h = blockIdx.y, b = blockIdx.x;
-    const int64_t bin = h * a.nb + b;
-    const int32_t q0 = a.offsets[bin], nq = a.offsets[bin + 1] - q0;
+    int32_t nq = 0;                                      // pairs over all query ranges
+    for (int64_t r = 0; r < a.nranges; ++r) {
+        const int64_t bin = (h * a.nranges + r) * a.nb + b;
+        nq += a.bin_offsets[bin + 1] - a.bin_offsets[bin];
+    }
     const int64_t j0 = b * C::kKB;
     const int kv_all = int(i64min(C::kKB, a.n - j0));    // keys of the block inside the sequence
     const uint32_t lane_off = uint32_t(warp * 32) << 16;
@@ -416,14 +420,24 @@ __global__ void __launch_bounds__(128) bwd_tc_kernel(const BwdArgs a) {
     // dV, dK: A (P or dS transposed) and B (dO or Q) both stored N- / M-contiguous
     constexpr uint32_t id_kv = tc::idesc_bf16_f32(C::kKB, D, /*b_mn_major=*/true) | (1u << 15);
     constexpr uint32_t id_q = tc::idesc_bf16_f32(C::kRows, D, /*b_mn_major=*/true);
-    const int ntiles = (nq + C::kRows - 1) / C::kRows;
     bool ok = true;
-    for (int tile = 0; tile < ntiles; ++tile) {
+    int tile = 0;
+    int64_t r = 0;
+    int32_t e0 = 0, cnt_r = 0, base = 0;                 // current bin and its next tile
+    for (;; ++tile, base += C::kRows) {
+        while (base >= cnt_r && r < a.nranges) {         // next bin with pairs left
+            const int64_t bin = (h * a.nranges + r) * a.nb + b;
+            e0 = a.bin_offsets[bin];
+            cnt_r = a.bin_offsets[bin + 1] - e0;
+            base = 0;
+            ++r;
+        }
+        if (base >= cnt_r) break;
         // ---- this row's query, its Q and dO rows, lse and D
-        const int rr = tile * C::kRows + t;
-        const bool live = rr < nq;
-        const int32_t i = live ? a.qlist[q0 + rr] : 0;
-        const int64_t qrow = h * a.n + i;
+        const int rr = base + t;
+        const bool live = rr < cnt_r;
+        const int64_t qrow = live ? int64_t(a.entries[e0 + rr] >> 5) : h * a.n;   // flat row
+        const int32_t i = int32_t(qrow - h * a.n);
         {
             const uint16_t *sq = a.q + qrow * D, *sdo = a.dout + qrow * D;
 #pragma unroll
@@ -575,10 +589,6 @@ template <int D>
 cudaError_t launch_tc_d(const BwdArgs &a, cudaStream_t st) {
     const int64_t rows = a.bh * a.n;
     bwd_dsum_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, st>>>(a);
-    const dim3 ge(unsigned((a.n * a.k + 255) / 256), unsigned(a.bh));
-    bwd_count_kernel<<<ge, 256, 0, st>>>(a);
-    bwd_scan_kernel<<<1, kScanThreads, 0, st>>>(a);
-    bwd_scatter_kernel<<<ge, 256, 0, st>>>(a);
     cudaError_t e = cudaMemsetAsync(a.dq, 0, size_t(rows) * D * sizeof(float), st);
     if (e != cudaSuccess) return e;
     auto kern = bwd_tc_kernel<D>;

@@ -56,13 +56,19 @@ struct BwdArgs {
     int32_t *counts, *cursors;    // [bh * nb] workspace, zeroed
     int32_t *offsets;             // [bh * nb + 1] workspace
     int32_t *qlist;               // [bh * n * k] workspace: queries by (head, block)
+    // tensor-core path: the forward fine stage's inversion -- pair ids
+    // ((h * n + i) << 5 | slot) grouped by bin (head, query range, block)
+    const int32_t *bin_offsets;   // [bh * nranges * nb + 1]
+    const int32_t *entries;
+    int64_t nranges;
     int32_t *status;
 };
 bool fine_backward_supported(int32_t d, int32_t kb);   // one CTA of kb * d / 16 <= 512 threads
 cudaError_t launch_fine_backward(const BwdArgs &a, cudaStream_t st);
 // Tensor-core backward (64-key blocks, at most 32 per query): a.lse must hold
-// every query's log2-sum-exp (the forward's merge writes it); a.dsum and the
-// inversion buffers are filled here; dq is zeroed and accumulated.
+// every query's log2-sum-exp and a.bin_offsets / a.entries the inversion of
+// the lists, both from the forward fine stage; a.dsum is filled here; dq is
+// zeroed and accumulated.
 bool fine_backward_tc_supported(int32_t d, int32_t kb, int32_t k);
 cudaError_t launch_fine_backward_tc(const BwdArgs &a, cudaStream_t st);
 
