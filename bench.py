@@ -534,8 +534,11 @@ def run_static(args, w, device, dist):
 def run_backward(args, w, fwd, q, k, v, device, dist):
     """The fine stage's backward pass over the lists (and output) of one
     forward: bsa_fine_backward timed alone, CUDA events, L2 flushed before
-    every step; one JSON line.  It runs on the CUDA cores, so the roofline is
-    the FP32 peak."""
+    every step, clocks sampled around the timed steps; one JSON line.  With
+    64-key blocks it runs on the tensor cores (bwd_tc_kernel in
+    csrc/backward.cu); the roofline takes its contractions at the tensor
+    peak, its softmax ops at the FP32 peak and its bytes at the HBM
+    bandwidth."""
     import torch
     from content_dependent_block_gb300 import bsa
     gen = torch.Generator(device="cpu").manual_seed(1)
@@ -564,19 +567,24 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
         return 0 if status == 0 else 1
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(device)
-    evs = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        evs.append((e0, e1))
-    torch.cuda.synchronize(device)
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else device.index
+    with ClockSampler(gpu_index) as clocks:
+        preroll(step, args.preroll_s, lambda: torch.cuda.synchronize(device))
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize(device)
+        evs = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+    clk = clocks.summary()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     pairs = admitted_pairs(fwd.idx, w)
     # per admitted (query, key) pair: q.k, dO.v, dQ, dK and dV updates (2d each,
@@ -598,7 +606,8 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
         "warmup": args.warmup, "n_gpus": 1, "higher_is_better": True, "dtype": "bf16 in, fp32",
         "data": "synthetic", "config": config_of(w),
         "roofline": rl,
-        "admitted_pairs": pairs, "flops_per_step": flops, "device_status": status}), flush=True)
+        "admitted_pairs": pairs, "flops_per_step": flops, "clocks": clk,
+        "device_status": status}), flush=True)
     return 0 if status == 0 else 1
 
 
