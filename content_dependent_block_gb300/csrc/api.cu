@@ -457,9 +457,13 @@ size_t bsa_forward_workspace_size(bsa_shape shape, int32_t key_block, int32_t to
 int32_t bsa_forward_launches(bsa_shape shape, int32_t key_block, int32_t topk) {
     if (check_shape(shape) != BSA_OK || check_key_block(key_block) != BSA_OK || topk < 1 || topk > 32)
         return -int32_t(BSA_ERR_INVALID_ARG);
-    // pool (+ hi/lo), score + top-k, then either the query-major fine kernel
-    // or count + scan + scatter + block-major fine
-    return bm_path(shape, key_block, ceil_div(shape.n, key_block)) ? 6 : 3;
+    // a small problem: one fused launch; else pool (+ hi/lo), score + top-k,
+    // then either the query-major fine kernel or count + scan + scatter +
+    // block-major fine
+    const int64_t nb = ceil_div(shape.n, key_block);
+    if (shape.dtype == BSA_BF16 && bsa::small_forward_supported(shape.d, nb, topk, shape.bh * shape.n))
+        return 1;
+    return bm_path(shape, key_block, nb) ? 6 : 3;
 }
 
 bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void *v,
@@ -494,6 +498,23 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
     const int64_t nb = ceil_div(shape.n, key_block);
     int32_t *status = device_status_ptr();
     if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
+    if (!has_options(opts) && bsa::small_forward_supported(shape.d, nb, topk, shape.bh * shape.n)) {
+        // a small problem: pooling, selection and the fine stage in one launch
+        bsa::FineArgs a{};
+        a.q = q;
+        a.k = k;
+        a.v = v;
+        a.out = out;
+        a.bh = shape.bh;
+        a.n = shape.n;
+        a.nb = nb;
+        a.kb = key_block;
+        a.d = shape.d;
+        a.mask_kind = BSA_MASK_NONE;
+        a.scale_log2 = softmax_scale_log2(scale, shape.d);
+        a.status = status;
+        return launched(bsa::launch_small_forward(a, topk, idx, st), "fused forward launch");
+    }
 
     BSA_TRY(launched(bsa::launch_pool(k, shape.bh, shape.n, shape.d, key_block, kbar, hi, lo, nb,
                                       st), "pool launch"));

@@ -167,6 +167,13 @@ cudaError_t launch_fine_bm(const FineBmArgs &a, cudaStream_t st);
 
 cudaError_t launch_fine_query_major(const FineArgs &a, int32_t dtype,
                                     cudaStream_t st);
+// The whole forward of a small problem (bf16, d in {64, 128}, at most 64
+// blocks, top-k <= 16, at most kSmallForwardRows rows of bh * n, no
+// selection options) in one launch: pooling, scores, top-k and the fine
+// stage (query-major, CUDA cores).  Writes out and idx [bh][n][topk].
+constexpr int64_t kSmallForwardRows = 16384;
+bool small_forward_supported(int32_t d, int64_t nb, int32_t topk, int64_t rows);
+cudaError_t launch_small_forward(const FineArgs &a, int32_t topk, int32_t *idx, cudaStream_t st);
 // Static or dense lists of bf16 inputs on the tensor cores: d in {64, 128},
 // 64-key blocks, one list row per 128-query tile (or no list), at most 512
 // listed blocks per row.

@@ -170,3 +170,11 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 def test_wait_selftest_rejects_bad_arguments(L, kind, limit):
     assert L.bsa_selftest_wait_timeout(kind, limit, None) == 1
     assert b"kind" in L.bsa_last_error() or b"limit" in L.bsa_last_error()
+
+
+def test_forward_launch_counts(L):
+    """A small problem runs as one fused launch; the 32k-token one as pool,
+    scores + top-k, the three inversion kernels and the fine kernel."""
+    assert L.bsa_forward_launches(_shape(bh=2, n=1024), 64, 4) == 1
+    assert L.bsa_forward_launches(_shape(bh=8, n=8192), 64, 16) == 6
+    assert L.bsa_forward_launches(_shape(bh=8, n=32768), 64, 16) == 6

@@ -165,18 +165,30 @@ def _small(bh, n, d, seed, dtype="bf16", sigma=0.0, kb=64):
     return t, tuple(parity.to_device(getattr(t, x), dtype) for x in "qkv")
 
 
-@pytest.mark.parametrize("bh,n,d,kb,topk", [
+EDGE_SHAPES = [
     (1, 1000, 64, 64, 4),      # ragged last block (40 tokens)
     (2, 300, 128, 32, 5),      # d=128, ragged, odd k
     (1, 40, 64, 64, 2),        # n < B: one partial block, k > nb
     (1, 1, 64, 16, 1),         # a single token
     (3, 256, 64, 64, 8),       # k*B >= n: dense attention
     (1, 4100, 64, 16, 32),     # many blocks, k = 32
-    (2, 700, 128, 64, 6),      # d=128 on the tensor-core fine stage, ragged
-])
-def test_forward_edge_shapes(bh, n, d, kb, topk):
+    (2, 700, 128, 64, 6),      # d=128, ragged
+]
+
+
+@pytest.mark.parametrize("bh,n,d,kb,topk", EDGE_SHAPES)
+@pytest.mark.parametrize("staged", [False, True], ids=["forward", "staged"])
+def test_forward_edge_shapes(bh, n, d, kb, topk, staged):
+    """bsa_forward (small problems: the single fused launch) and, staged,
+    the same method as three calls -- pool, scores + top-k, fine attention
+    over the selection (tensor-core scoring, block-major fine stage for
+    64-key blocks)."""
     t, (q, k, v) = _small(bh, n, d, seed=n + d, sigma=0.5, kb=kb)
-    out, idx = bsa.forward(q, k, v, kb, topk)
+    if staged:
+        idx = bsa.coarse_topk(q, bsa.pool_blocks(k, kb), kb, topk)
+        out = bsa.fine_attention(q, k, v, idx, key_block=kb)
+    else:
+        out, idx = bsa.forward(q, k, v, kb, topk)
     rows = oracle.all_rows(bh, n)
     nb = -(-n // kb)
     s = oracle.scores(t.q, oracle.pool(t.k, kb), rows)
