@@ -779,11 +779,10 @@ def main(argv=None):
                        fine_ms, peaks, sms,
                        "fine attention stage: one bsa_fine_attention call over the top-k list "
                        "(list inversion + fine_ws_kernel)",
-                       kernel_traffic("fine_stage" if fwd.launches == 6 else "fine_query_major",
-                                      w.name))
+                       kernel_traffic("fine_stage", w.name))
     cfg = config_of(w)
-    cfg["launch"] = ("one CUDA-graph replay per forward" if args.graph
-                     else "one bsa_forward_ex call per forward")
+    cfg["launch"] = (f"one CUDA-graph replay per forward ({fwd.launches} kernels)" if args.graph
+                     else f"one bsa_forward_ex call per forward ({fwd.launches} kernels)")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
