@@ -149,7 +149,7 @@ struct BmLayout {
     size_t zero = 0, zero_bytes = 0;     // counts, cursors, queue heads, range counters
     size_t counts = 0, cursors = 0, fine_head = 0, merge_head = 0, range_done = 0, merge_done = 0;
     size_t offsets = 0, fitem_off = 0, fpre = 0, mpre = 0, range_total = 0, range_merges = 0;
-    size_t n_fine = 0, n_merge = 0, fine_items = 0, merge_items = 0, entries = 0;
+    size_t n_fine = 0, n_merge = 0, fine_items = 0, merge_items = 0, entries = 0, vmask = 0;
     size_t part_o = 0, part_lse = 0, total = 0;
 };
 
@@ -185,6 +185,7 @@ BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     L.fine_items = take(size_t(L.plan.fine_cap) * sizeof(int2));
     L.merge_items = take(size_t(L.plan.merge_cap) * sizeof(int2));
     L.entries = take(size_t(s.bh) * s.n * k * 4);
+    L.vmask = take(size_t(s.bh) * s.n * 4);
     off = round_up(off, 256);
     L.part_o = take(ring_slots * s.d * 2);
     off = round_up(off, 256);
@@ -221,6 +222,7 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     w.n_fine = reinterpret_cast<int32_t *>(ws + L.n_fine);
     w.n_merge = reinterpret_cast<int32_t *>(ws + L.n_merge);
     w.entries = reinterpret_cast<int32_t *>(ws + L.entries);
+    w.vmask = reinterpret_cast<uint32_t *>(ws + L.vmask);
     e = bsa::launch_invert(list, s.bh, s.n, nb, topk, L.plan, w, static_cast<uint16_t *>(out), s.d,
                            status, st);
     if (e != cudaSuccess) return e;

@@ -128,6 +128,7 @@ struct InvertBuffers {
     int32_t *n_fine;
     int32_t *n_merge;
     int32_t *entries;       // [bh * n * k] pair ids (flat query row << 5) | slot, by bin
+    uint32_t *vmask;        // [bh * n] per query: bit s set when slot s holds a block (nullable)
 };
 // count + scan + scatter launches
 cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,

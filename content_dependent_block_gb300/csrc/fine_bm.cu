@@ -746,18 +746,23 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (it >= n_merge) break;
             const int2 item = a.w.merge_items[it];
             const int64_t rg = item.x;
+            const int64_t h = rg / nranges, rr = rg % nranges;
+            const int64_t i_begin = rr * range + item.y;
+            const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
+            const int nq = int(i_end - i_begin);
+            // lists with padding: the slot mask of query (i_begin + lane), loaded
+            // while the range's pairs are still being finished
+            uint32_t vml = 0u;
+            if (full_valid == 0 && !(kOpts && a.sel_lists) && lane < nq)
+                vml = __ldg(a.w.vmask + h * n + i_begin + lane);
             int got = 1;
             if (lane == 0) {
                 got = tc::wait_counter(a.range_done + rg, a.w.range_total[rg], status);
                 tc::fence_proxy_async_global();      // partials were written by generic stores
             }
             if (!__shfl_sync(kFull, got, 0)) break;
-            const int64_t h = rg / nranges, rr = rg % nranges;
-            const int64_t i_begin = rr * range + item.y;
             // lists from the selection: the valid slots follow from the budget
             const int kr_h = kOpts && a.head_k != nullptr ? min(max(__ldg(a.head_k + h), 0), k) : k;
-            const int64_t i_end = i64min(i64min(n, rr * range + range), i_begin + a.p.qm);
-            const int nq = int(i_end - i_begin);
             const int nch = (nq + qs - 1) / qs;
             const int64_t slot0 = (rg % kPartialRing) * ring_stride + (i_begin - rr * range) * kpad;
             auto issue = [&](int c) {                // lane 0: chunk c into its stage
@@ -793,13 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                         vm = act ? (cnt >= 32 ? kFull : (1u << cnt) - 1u) : 0u;
                     } else if (full_valid == 0) {
                         // lists with padding: a slot counts only if its id is a block
-                        vm = 0u;
-                        for (int s = gl; act && s < k; s += LPQ) {
-                            const int32_t bb = __ldg(a.list + qrow * k + s);
-                            if (bb >= 0 && bb < nb) vm |= 1u << s;
-                        }
-#pragma unroll
-                        for (int o = 1; o < LPQ; o <<= 1) vm |= __shfl_xor_sync(kFull, vm, o);
+                        vm = __shfl_sync(kFull, vml, (q0 + jq) & 31);
+                        if (!act) vm = 0u;
                     }
                     float acc[16];
                     const uint16_t *po = reinterpret_cast<const uint16_t *>(st) + jq * kpad * D + gl * 16;

@@ -18,7 +18,8 @@
 //            range, see scan_kernel)
 //   scatter  writes every pair id p = ((h*n + i) << 5) | s into its block's
 //            range (order inside a range is arbitrary; results do not
-//            depend on it); queries with no valid slot get O = 0 here
+//            depend on it) and every query's mask of valid slots (for the
+//            merge); queries with no valid slot get O = 0 here
 //
 // Entries outside [0, nb) are skipped and reported (BSA_ERR_BAD_INDEX);
 // -1 entries are padding.
@@ -208,11 +209,13 @@ template <typename OutT>
 __global__ void __launch_bounds__(kThreads) scatter_kernel(
     const int32_t *__restrict__ list, int64_t n, int64_t nb, int32_t k, int64_t range,
     int64_t nranges, const int32_t *__restrict__ offsets, int32_t *__restrict__ cursors,
-    int32_t *__restrict__ entries, OutT *__restrict__ out, int32_t d) {
+    int32_t *__restrict__ entries, uint32_t *__restrict__ vmask, OutT *__restrict__ out,
+    int32_t d) {
     extern __shared__ int32_t sm[];
     int32_t *hist = sm;          // pairs of this CTA per block
     int32_t *base = sm + nb;     // first slot of this CTA inside the block's range
-    int32_t *any = sm + 2 * nb;  // per query of the CTA: some slot is a block
+    // per query of the CTA: bit s set when slot s holds a block
+    uint32_t *any = reinterpret_cast<uint32_t *>(sm + 2 * nb);
     const int64_t h = blockIdx.y;
     const int64_t i0 = int64_t(blockIdx.x) * kQueriesPerCta;
     const int64_t i1 = i64min(n, i0 + kQueriesPerCta);
@@ -241,12 +244,14 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(
             const int32_t il = int32_t(div_small(uint32_t(e), magic));
             const int32_t r = atomicAdd(&hist[b], 1);
             entries[base[b] + r] = ((row0 + il) << 5) | (e - il * k);
-            any[il] = 1;
+            atomicOr(&any[il], 1u << (e - il * k));
         }
     }
     __syncthreads();
-    // queries whose list admits nothing: their output is zero
+    // the slot masks, for the merge; queries whose list admits nothing:
+    // their output is zero
     for (int64_t i = i0 + threadIdx.x; i < i1; i += kThreads) {
+        if (vmask != nullptr) vmask[h * n + i] = any[i - i0];
         if (!any[i - i0]) {
             OutT *o = out + (h * n + i) * d;
             for (int c = 0; c < d; ++c) o[c] = OutT(0);
@@ -302,7 +307,7 @@ cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb
                                     w.n_merge);
     scatter_kernel<uint16_t><<<grid, kThreads, smem2, st>>>(list, n, nb, k, p.range,
                                                                 p.nranges, w.offsets, w.cursors,
-                                                                w.entries, out_bf16, d);
+                                                                w.entries, w.vmask, out_bf16, d);
     return cudaGetLastError();
 }
 
