@@ -1,5 +1,6 @@
 // C-ABI layer of libbsa.so: argument validation, workspace carving and the
 // launch sequence of every entry point declared in include/bsa.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -158,7 +159,16 @@ BmLayout bm_layout(const bsa_shape &s, int32_t kb, int32_t k, size_t base) {
     const int64_t nb = ceil_div(s.n, kb);
     L.plan = bsa::invert_plan(s.bh, s.n, nb, k);
     const size_t nbins = size_t(L.plan.nbins), nr = size_t(L.plan.nr);
-    const size_t ring_slots = size_t(bsa::kPartialRing) * size_t(L.plan.range) * size_t(L.plan.kpad);
+    // as many query ranges in flight as fit the byte budget (a range's
+    // partial states: range x kpad x (2d + 8) bytes): a power of two in
+    // [4, 16], so that the kernel finds a range's entry with a mask
+    const int64_t range_bytes = L.plan.range * L.plan.kpad * (2 * int64_t(s.d) + 8);
+    int32_t ring = bsa::kPartialRing;
+    while (ring < bsa::kPartialRingMax && 2 * ring * range_bytes <= bsa::kPartialRingBytes &&
+           ring < L.plan.nr)
+        ring *= 2;
+    L.plan.ring = ring;
+    const size_t ring_slots = size_t(L.plan.ring) * size_t(L.plan.range) * size_t(L.plan.kpad);
     size_t off = base;
     auto take = [&](size_t bytes) {
         const size_t at = off;

@@ -104,13 +104,16 @@ cudaError_t launch_coarse_topk_tc(const void *q, const uint16_t *kbar_hi, const 
 // ---- block-major fine stage over per-query lists [bh][n][k] ----------
 constexpr int32_t kFineBmItemPairs = 512;   // pairs per fine work item (<= 4 tiles)
 constexpr int32_t kMergeQueries = 32;       // queries per merge work item
-constexpr int32_t kPartialRing = 4;         // query ranges whose partials coexist
+constexpr int32_t kPartialRing = 4;         // query ranges whose partials coexist, at least
+constexpr int32_t kPartialRingMax = 16;     // and at most
+constexpr int64_t kPartialRingBytes = int64_t(72) << 20;   // partial-state bytes aimed at
 
 // Bins are (head, query range of `range` queries, key block).
 struct InvertPlan {
     int64_t range = 0, nranges = 0, nr = 0, nbins = 0, fine_cap = 0, merge_cap = 0;
     int32_t item_pairs = 0, qm = 0;
     int32_t kpad = 0;       // partial slots per query in the ring (k rounded up to 4)
+    int32_t ring = 0;       // query ranges whose partial states coexist, a power of two (set by the fine stage)
 };
 InvertPlan invert_plan(int64_t bh, int64_t n, int64_t nb, int32_t k);
 

@@ -9,7 +9,8 @@
 // handing work over mbarriers in shared memory:
 //
 //   prefetch  (warp 12)     takes fine items (one bin, <= 512 pairs) from a
-//                           global queue, stages each item's descriptor and
+//                           global queue (claiming the next while it stages
+//                           the current one), stages each item's descriptor and
 //                           pair ids in a shared-memory ring and starts the
 //                           TMA loads of its K_b and V_b (128-byte swizzle,
 //                           one buffer per item in flight)
@@ -38,8 +39,9 @@
 //                           each query's k states in slot order (the
 //                           online-softmax merge of (m, l, acc))
 //
-// Partial states of a range live in ring entry (range mod kPartialRing); a
-// fine item of range r waits until range r - kPartialRing is merged.  Every
+// Partial states of a range live in ring entry (range mod R), R the ring
+// depth (4, 8 or 16 ranges: as many as fit about 72 MB of partial states); a
+// fine item of range r waits until range r - R is merged.  Every
 // wait is on work taken from a queue earlier or on this CTA's own progress,
 // and a group counts its finished pairs before it waits for a tile that may
 // depend on other CTAs, so the schedule cannot deadlock; every wait is
@@ -307,24 +309,35 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
     const int64_t n = a.n, nb = a.nb, range = a.p.range, nranges = a.p.nranges;
     const int64_t kpad = a.p.kpad;
     const int64_t ring_stride = range * kpad;
+    const int32_t ring = a.p.ring, ring_mask = ring - 1;   // a power of two
 
     if (warp == kWarpFetch) {
         // ----------------------------------------------------- prefetcher
         // dequeues fine items and stages descriptor + pair ids in shared memory
         const int n_fine = *a.w.n_fine;
+        // the next item is claimed, and its descriptor loaded, while the
+        // current one is staged (claims stay in queue order, and every CTA
+        // stages its items in the order it claimed them)
+        int it = 0;
+        if (lane == 0) it = atomicAdd(a.fine_head, 1);
+        it = __shfl_sync(kFull, it, 0);
+        int2 item = make_int2(0, 0);
+        int32_t off = 0, off1 = 0;
+        if (it < n_fine) {
+            item = a.w.fine_items[it];
+            off = a.w.offsets[item.x];
+            off1 = a.w.offsets[item.x + 1];
+        }
         for (int u = 0;; ++u) {
             const int slot = u % kNI;
-            if (u >= kNI && !tc::mbar_wait(bars + C::bItFree + slot, ((u / kNI) - 1) & 1, status)) break;
-            int it = 0;
-            if (lane == 0) it = atomicAdd(a.fine_head, 1);
-            it = __shfl_sync(kFull, it, 0);
-            StagedItem *si = items + slot;
             const bool valid = it < n_fine;
+            int it_next = n_fine;
+            if (valid && lane == 0) it_next = atomicAdd(a.fine_head, 1);
+            if (u >= kNI && !tc::mbar_wait(bars + C::bItFree + slot, ((u / kNI) - 1) & 1, status)) break;
+            StagedItem *si = items + slot;
             if (valid) {
-                const int2 item = a.w.fine_items[it];
                 const int64_t bin = item.x;
-                const int32_t off = a.w.offsets[bin];
-                const int32_t end = min(a.w.offsets[bin + 1] - off, item.y + a.p.item_pairs);
+                const int32_t end = min(off1 - off, item.y + a.p.item_pairs);
                 const int32_t *ent = a.w.entries + off;
                 int32_t v[kItemMax / 32];
 #pragma unroll
@@ -345,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     si->b = int32_t(b);
                     si->kv = int32_t(i64min(kB, n - b * kB));
                     si->qbase = int32_t(h * n + rr * range);
-                    si->roff = int32_t((rg % kPartialRing) * ring_stride);
+                    si->roff = int32_t((int32_t(rg) & ring_mask) * ring_stride);
                     si->ibase = int32_t(rr * range);
                     si->j0 = int32_t(b * kB);
                 }
@@ -380,6 +393,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             __syncwarp();
             tc::mbar_arrive(bars + C::bItFull + slot);
             if (!valid) break;
+            it = __shfl_sync(kFull, it_next, 0);
+            if (it < n_fine) {
+                item = a.w.fine_items[it];
+                off = a.w.offsets[item.x];
+                off1 = a.w.offsets[item.x + 1];
+            }
         }
     } else if (gather_index(warp) >= 0) {
         // --------------------------------------------------------- gather
@@ -410,12 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             const int32_t first = si->first, end = si->end, bin = si->bin, rg = si->rg;
             const int32_t kv = si->kv, qbase = si->qbase, roff = si->roff;
             const int32_t ibase = si->ibase, j0 = si->j0;
-            if (gw == 0 && rg >= kPartialRing) {
+            if (gw == 0 && rg >= ring) {
                 // the ring entry must have been merged by its previous range
                 int got = 1;
                 if (lane == 0)
-                    got = tc::wait_counter(a.merge_done + (rg - kPartialRing),
-                                           a.w.range_merges[rg - kPartialRing], status);
+                    got = tc::wait_counter(a.merge_done + (rg - ring), a.w.range_merges[rg - ring],
+                                           status);
                 if (!__shfl_sync(kFull, got, 0)) {
                     ok = false;
                     break;
@@ -659,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 // bytes of 8 rows instead of 16 bytes of 32 rows.
                 tc::tc_fence_after();
                 const bool has = row < x_count;
-                int32_t part = 0;                               // < kPartialRing * range * kpad
+                int32_t part = 0;                               // < ring * range * kpad
                 if (has) {
                     const int32_t pid = tpid[row];
                     part = x_roff + ((pid >> 5) - x_qbase) * int32_t(kpad) + (pid & 31);
@@ -764,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             // lists from the selection: the valid slots follow from the budget
             const int kr_h = kOpts && a.head_k != nullptr ? min(max(__ldg(a.head_k + h), 0), k) : k;
             const int nch = (nq + qs - 1) / qs;
-            const int64_t slot0 = (rg % kPartialRing) * ring_stride + (i_begin - rr * range) * kpad;
+            const int64_t slot0 = (int32_t(rg) & ring_mask) * ring_stride + (i_begin - rr * range) * kpad;
             auto issue = [&](int c) {                // lane 0: chunk c into its stage
                 const uint32_t b = (sc + uint32_t(c)) % C::kMS;
                 const int qn = min(qs, nq - c * qs);
