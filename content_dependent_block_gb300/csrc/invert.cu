@@ -33,9 +33,26 @@ constexpr int kThreads = 256;
 constexpr int kQueriesPerCta = 256;    // queries of one head per count/scatter CTA
 constexpr int kScanThreads = 1024;
 constexpr int kScanV = 4;              // bins per thread per scan chunk
+constexpr int kScanG = 4;              // chunks whose counts are loaded together
 static_assert(kFineBmItemPairs == 512, "fine items are cut at 512 pairs (shift below)");
 
 __device__ __forceinline__ bool valid_block(int32_t b, int64_t nb) { return b >= 0 && b < nb; }
+
+// A CTA's list entries, kQueriesPerCta x k <= kThreads x kEntriesMax: thread
+// t holds entries t + j * kThreads, all loaded before any is used (the
+// shared-memory atomics that follow would otherwise keep the compiler from
+// overlapping the loads).
+constexpr int kEntriesMax = kQueriesPerCta * 32 / kThreads;
+struct CtaEntries {
+    int32_t v[kEntriesMax];
+    __device__ __forceinline__ void load(const int32_t *__restrict__ base, int32_t m) {
+#pragma unroll
+        for (int j = 0; j < kEntriesMax; ++j) {
+            const int32_t e = int32_t(threadIdx.x) + j * kThreads;
+            v[j] = e < m ? __ldg(base + e) : -1;
+        }
+    }
+};
 
 // floor(e / k) for 0 <= e < 2^16 and 1 <= k <= 32: e * ceil(2^32 / k) / 2^32,
 // exact because the rounding error (< e / 2^32) stays below 1 / k.
@@ -53,11 +70,13 @@ __global__ void __launch_bounds__(kThreads) count_kernel(const int32_t *__restri
     const int64_t i1 = i64min(n, i0 + kQueriesPerCta);
     for (int64_t b = threadIdx.x; b < nb; b += kThreads) hist[b] = 0;
     __syncthreads();
-    const int32_t *base = list + (h * n + i0) * k;
     const int32_t m = int32_t((i1 - i0) * k);
+    CtaEntries ent;
+    ent.load(list + (h * n + i0) * k, m);
     bool bad = false;
-    for (int32_t e = threadIdx.x; e < m; e += kThreads) {
-        const int32_t b = __ldg(base + e);
+#pragma unroll
+    for (int j = 0; j < kEntriesMax; ++j) {
+        const int32_t b = ent.v[j];
         if (valid_block(b, nb)) atomicAdd(&hist[b], 1);
         else if (b >= 0 || b < -1) bad = true;
     }
@@ -115,7 +134,8 @@ __device__ __forceinline__ void block_scan2(int32_t &a, int32_t &b, int32_t &ta,
 // the two work lists of the fine stage: fine items {bin, first pair} (at
 // most 512 pairs each) in bin order, and merge items {range, first query}
 // (qm queries each) in range order.  Bins are scanned in coalesced chunks of
-// 4 bins per thread with a running carry.
+// 4 bins per thread with a running carry; the counts of four chunks are
+// loaded at once.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(
     const int32_t *__restrict__ counts, int64_t nb, int64_t nr, int64_t nranges, int64_t range,
     int64_t n, int32_t item_pairs, int32_t qm, int32_t *__restrict__ offsets,
@@ -128,36 +148,47 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(
     const int32_t nbins = int32_t(nr * nb);
     // 1. bins: pair offsets, fine-item offsets and the fine items themselves
     int32_t carry_p = 0, carry_f = 0;
-    for (int32_t base = 0; base < nbins; base += kScanThreads * kScanV) {
-        const int32_t e = base + t * kScanV;
-        int32_t c[kScanV];
-        if (e + kScanV <= nbins) {
-            const int4 v = *reinterpret_cast<const int4 *>(counts + e);   // 16-byte aligned
-            c[0] = v.x, c[1] = v.y, c[2] = v.z, c[3] = v.w;
-        } else {
+    for (int32_t base0 = 0; base0 < nbins; base0 += kScanThreads * kScanV * kScanG) {
+        int4 cv[kScanG];
 #pragma unroll
-            for (int j = 0; j < kScanV; ++j) c[j] = e + j < nbins ? counts[e + j] : 0;
+        for (int g = 0; g < kScanG; ++g) {
+            const int32_t e = base0 + g * kScanThreads * kScanV + t * kScanV;
+            if (e + kScanV <= nbins) {
+                cv[g] = *reinterpret_cast<const int4 *>(counts + e);   // 16-byte aligned
+            } else {
+                cv[g].x = e < nbins ? counts[e] : 0;
+                cv[g].y = e + 1 < nbins ? counts[e + 1] : 0;
+                cv[g].z = e + 2 < nbins ? counts[e + 2] : 0;
+                cv[g].w = e + 3 < nbins ? counts[e + 3] : 0;
+            }
         }
-        int32_t p = 0, f = 0;
 #pragma unroll
-        for (int j = 0; j < kScanV; ++j) {
-            p += c[j];
-            f += (c[j] + 511) >> 9;
-        }
-        int32_t tp, tf;
-        block_scan2(p, f, tp, tf, wa, wb);
-        p += carry_p;
-        f += carry_f;
+        for (int g = 0; g < kScanG; ++g) {
+            const int32_t base = base0 + g * kScanThreads * kScanV;
+            if (base >= nbins) break;                 // uniform over the CTA
+            const int32_t e = base + t * kScanV;
+            const int32_t c[kScanV] = {cv[g].x, cv[g].y, cv[g].z, cv[g].w};
+            int32_t p = 0, f = 0;
 #pragma unroll
-        for (int j = 0; j < kScanV; ++j) {
-            if (e + j >= nbins) break;
-            offsets[e + j] = p;
-            fitem_off[e + j] = f;
-            for (int32_t x = 0; x < c[j]; x += 512) fine_items[f++] = make_int2(e + j, x);
-            p += c[j];
+            for (int q = 0; q < kScanV; ++q) {
+                p += c[q];
+                f += (c[q] + 511) >> 9;
+            }
+            int32_t tp, tf;
+            block_scan2(p, f, tp, tf, wa, wb);
+            p += carry_p;
+            f += carry_f;
+#pragma unroll
+            for (int q = 0; q < kScanV; ++q) {
+                if (e + q >= nbins) break;
+                offsets[e + q] = p;
+                fitem_off[e + q] = f;
+                for (int32_t x = 0; x < c[q]; x += 512) fine_items[f++] = make_int2(e + q, x);
+                p += c[q];
+            }
+            carry_p += tp;
+            carry_f += tf;
         }
-        carry_p += tp;
-        carry_f += tf;
     }
     if (t == 0) {
         offsets[nbins] = carry_p;
@@ -286,6 +317,7 @@ InvertPlan invert_plan(int64_t bh, int64_t n, int64_t nb, int32_t k) {
 cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb, int32_t k,
                           const InvertPlan &p, const InvertBuffers &w, uint16_t *out_bf16,
                           int32_t d, int32_t *status, cudaStream_t st) {
+    if (k < 1 || k > 32) return cudaErrorInvalidValue;   // CtaEntries holds 32 per query
     const dim3 grid(unsigned((n + kQueriesPerCta - 1) / kQueriesPerCta), unsigned(bh));
     const size_t smem1 = size_t(nb) * sizeof(int32_t);
     const size_t smem2 = 2 * smem1 + kQueriesPerCta * sizeof(int32_t);
