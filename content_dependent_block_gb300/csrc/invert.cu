@@ -34,6 +34,7 @@ constexpr int kQueriesPerCta = 256;    // queries of one head per count/scatter 
 constexpr int kScanThreads = 1024;
 constexpr int kScanV = 4;              // bins per thread per scan chunk
 constexpr int kScanG = 4;              // chunks whose counts are loaded together
+constexpr int kScanStage = 8192;       // fine items of a chunk staged in shared memory
 static_assert(kFineBmItemPairs == 512, "fine items are cut at 512 pairs (shift below)");
 
 __device__ __forceinline__ bool valid_block(int32_t b, int64_t nb) { return b >= 0 && b < nb; }
@@ -135,7 +136,10 @@ __device__ __forceinline__ void block_scan2(int32_t &a, int32_t &b, int32_t &ta,
 // most 512 pairs each) in bin order, and merge items {range, first query}
 // (qm queries each) in range order.  Bins are scanned in coalesced chunks of
 // 4 bins per thread with a running carry; the counts of four chunks are
-// loaded at once.
+// loaded at once, and a chunk's offsets are stored 16 bytes per thread and
+// its fine items staged in shared memory and copied out contiguously (one
+// CTA's scattered small stores would otherwise each cost an L2 transaction).
+// Dynamic shared memory: kScanStage int2.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(
     const int32_t *__restrict__ counts, int64_t nb, int64_t nr, int64_t nranges, int64_t range,
     int64_t n, int32_t item_pairs, int32_t qm, int32_t *__restrict__ offsets,
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(
     int2 *__restrict__ fine_items, int2 *__restrict__ merge_items, int32_t *__restrict__ n_fine,
     int32_t *__restrict__ n_merge) {
     __shared__ int32_t wa[32], wb[32];
+    extern __shared__ int2 stage[];
     const int t = threadIdx.x;
     const int32_t nbins = int32_t(nr * nb);
     // 1. bins: pair offsets, fine-item offsets and the fine items themselves
@@ -178,14 +183,30 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(
             block_scan2(p, f, tp, tf, wa, wb);
             p += carry_p;
             f += carry_f;
+            int32_t po[kScanV], fo[kScanV];
 #pragma unroll
             for (int q = 0; q < kScanV; ++q) {
-                if (e + q >= nbins) break;
-                offsets[e + q] = p;
-                fitem_off[e + q] = f;
-                for (int32_t x = 0; x < c[q]; x += 512) fine_items[f++] = make_int2(e + q, x);
+                po[q] = p;
+                fo[q] = f;
+                for (int32_t x = 0; x < c[q]; x += 512, ++f) {
+                    const int32_t at = f - carry_f;        // chunk-local item index
+                    if (at < kScanStage) stage[at] = make_int2(e + q, x);
+                    else fine_items[f] = make_int2(e + q, x);
+                }
                 p += c[q];
             }
+            if (e + kScanV <= nbins) {
+                *reinterpret_cast<int4 *>(offsets + e) = make_int4(po[0], po[1], po[2], po[3]);
+                *reinterpret_cast<int4 *>(fitem_off + e) = make_int4(fo[0], fo[1], fo[2], fo[3]);
+            } else {
+                for (int q = 0; q < kScanV && e + q < nbins; ++q) {
+                    offsets[e + q] = po[q];
+                    fitem_off[e + q] = fo[q];
+                }
+            }
+            __syncthreads();
+            for (int32_t i = t; i < min(tf, kScanStage); i += kScanThreads) fine_items[carry_f + i] = stage[i];
+            __syncthreads();
             carry_p += tp;
             carry_f += tf;
         }
@@ -326,6 +347,9 @@ cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb
         (e = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   int(smem1))) != cudaSuccess)
         return e;
+    if ((e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(kScanStage * sizeof(int2)))) != cudaSuccess)
+        return e;
     if (smem2 > 48 * 1024 &&
         (e = cudaFuncSetAttribute(scatter_kernel<uint16_t>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem2))) !=
@@ -333,10 +357,10 @@ cudaError_t launch_invert(const int32_t *list, int64_t bh, int64_t n, int64_t nb
         return e;
     count_kernel<<<grid, kThreads, smem1, st>>>(list, n, nb, k, p.range, p.nranges, w.counts,
                                                status);
-    scan_kernel<<<1, kScanThreads, 0, st>>>(w.counts, nb, p.nr, p.nranges, p.range, n, p.item_pairs, p.qm,
-                                    w.offsets, w.fitem_off, w.fpre, w.mpre, w.range_total,
-                                    w.range_merges, w.fine_items, w.merge_items, w.n_fine,
-                                    w.n_merge);
+    scan_kernel<<<1, kScanThreads, kScanStage * sizeof(int2), st>>>(
+        w.counts, nb, p.nr, p.nranges, p.range, n, p.item_pairs, p.qm, w.offsets, w.fitem_off,
+        w.fpre, w.mpre, w.range_total, w.range_merges, w.fine_items, w.merge_items, w.n_fine,
+        w.n_merge);
     scatter_kernel<uint16_t><<<grid, kThreads, smem2, st>>>(list, n, nb, k, p.range,
                                                                 p.nranges, w.offsets, w.cursors,
                                                                 w.entries, w.vmask, out_bf16, d);
