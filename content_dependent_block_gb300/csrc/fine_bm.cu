@@ -672,10 +672,13 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             if (ok) {
                 // ---- epilogue: this row's pair state, the unnormalised O (bf16)
                 // and (m, l); the merge divides once per query.  O is read from
-                // TMEM 64 columns at a time;
-                // each 32-column chunk goes through a small swizzled shared
-                // buffer so that every store instruction writes 64 contiguous
-                // bytes of 8 rows instead of 16 bytes of 32 rows.
+                // TMEM 64 columns at a time and goes through a small swizzled
+                // shared buffer per warp, so that a store instruction writes
+                // whole row segments: at d = 64 each 32-column half as 64
+                // contiguous bytes of 8 rows; at d = 128 each 64-column chunk
+                // as 128 bytes of 4 rows, staged 16 rows at a time (measured:
+                // the first form is faster at d = 64, the second at d = 128;
+                // one 16-byte store per row per instruction is far slower).
                 tc::tc_fence_after();
                 const bool has = row < x_count;
                 int32_t part = 0;                               // < ring * range * kpad
@@ -683,40 +686,80 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                     const int32_t pid = tpid[row];
                     part = x_roff + ((pid >> 5) - x_qbase) * int32_t(kpad) + (pid & 31);
                 }
-                int32_t sp[4];                                  // part of rows 8i + srow
-                bool sh[4];
+                if constexpr (D == 64) {
+                    int32_t sp[4];                                  // part of rows 8i + srow
+                    bool sh[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    sp[i] = __shfl_sync(kFull, part, 8 * i + srow);
-                    sh[i] = quad * 32 + 8 * i + srow < x_count;
-                }
+                    for (int i = 0; i < 4; ++i) {
+                        sp[i] = __shfl_sync(kFull, part, 8 * i + srow);
+                        sh[i] = quad * 32 + 8 * i + srow < x_count;
+                    }
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 64) {
-                    uint32_t ov[2][32];
-                    tc::tmem_ld32(tO + uint32_t(c0) + lane_off, ov[0]);
-                    tc::tmem_ld32(tO + uint32_t(c0 + 32) + lane_off, ov[1]);
-                    tc::tmem_ld_wait();
+                    for (int c0 = 0; c0 < D; c0 += 64) {
+                        uint32_t ov[2][32];
+                        tc::tmem_ld32(tO + uint32_t(c0) + lane_off, ov[0]);
+                        tc::tmem_ld32(tO + uint32_t(c0 + 32) + lane_off, ov[1]);
+                        tc::tmem_ld_wait();
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
+                        for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint4 val = make_uint4(
-                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 0]), __uint_as_float(ov[hf][8 * v + 1])),
-                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 2]), __uint_as_float(ov[hf][8 * v + 3])),
-                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 4]), __uint_as_float(ov[hf][8 * v + 5])),
-                                pack_bf16x2(__uint_as_float(ov[hf][8 * v + 6]), __uint_as_float(ov[hf][8 * v + 7])));
-                            *reinterpret_cast<uint4 *>(eb + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
+                            for (int v = 0; v < 4; ++v) {
+                                const uint4 val = make_uint4(
+                                    pack_bf16x2(__uint_as_float(ov[hf][8 * v + 0]), __uint_as_float(ov[hf][8 * v + 1])),
+                                    pack_bf16x2(__uint_as_float(ov[hf][8 * v + 2]), __uint_as_float(ov[hf][8 * v + 3])),
+                                    pack_bf16x2(__uint_as_float(ov[hf][8 * v + 4]), __uint_as_float(ov[hf][8 * v + 5])),
+                                    pack_bf16x2(__uint_as_float(ov[hf][8 * v + 6]), __uint_as_float(ov[hf][8 * v + 7])));
+                                *reinterpret_cast<uint4 *>(eb + lane * 64 + ((v ^ ((lane >> 1) & 3)) << 4)) = val;
+                            }
+                            __syncwarp();
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = 8 * i + srow;
+                                const uint4 val =
+                                    *reinterpret_cast<const uint4 *>(eb + r * 64 + ((spiece ^ ((r >> 1) & 3)) << 4));
+                                if (sh[i])
+                                    *reinterpret_cast<uint4 *>(a.part_o + int64_t(sp[i]) * D + c0 + hf * 32 + spiece * 8) = val;
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 64) {
+                        uint32_t ov[2][32];
+                        tc::tmem_ld32(tO + uint32_t(c0) + lane_off, ov[0]);
+                        tc::tmem_ld32(tO + uint32_t(c0 + 32) + lane_off, ov[1]);
+                        tc::tmem_ld_wait();
+                        // two passes of 16 rows: lanes 16p .. 16p + 15 put their 128-byte
+                        // row segment into the buffer (row r, chunk c at c ^ (r & 7)),
+                        // then every store instruction writes four whole rows
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int r = 8 * i + srow;
-                            const uint4 val =
-                                *reinterpret_cast<const uint4 *>(eb + r * 64 + ((spiece ^ ((r >> 1) & 3)) << 4));
-                            if (sh[i])
-                                *reinterpret_cast<uint4 *>(a.part_o + int64_t(sp[i]) * D + c0 + hf * 32 + spiece * 8) = val;
+                        for (int ps = 0; ps < 2; ++ps) {
+                            if ((lane >> 4) == ps) {
+                                const int r = lane & 15;
+#pragma unroll
+                                for (int v = 0; v < 8; ++v) {
+                                    const int hf = v >> 2, vv = v & 3;
+                                    const uint4 val = make_uint4(
+                                        pack_bf16x2(__uint_as_float(ov[hf][8 * vv + 0]), __uint_as_float(ov[hf][8 * vv + 1])),
+                                        pack_bf16x2(__uint_as_float(ov[hf][8 * vv + 2]), __uint_as_float(ov[hf][8 * vv + 3])),
+                                        pack_bf16x2(__uint_as_float(ov[hf][8 * vv + 4]), __uint_as_float(ov[hf][8 * vv + 5])),
+                                        pack_bf16x2(__uint_as_float(ov[hf][8 * vv + 6]), __uint_as_float(ov[hf][8 * vv + 7])));
+                                    *reinterpret_cast<uint4 *>(eb + r * 128 + ((v ^ (r & 7)) << 4)) = val;
+                                }
+                            }
+                            __syncwarp();
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int r = 4 * i + (lane >> 3), ch = lane & 7;   // buffer row, chunk
+                                const int src = 16 * ps + r;                         // lane of the row
+                                const int32_t pr = __shfl_sync(kFull, part, src);
+                                const uint4 val = *reinterpret_cast<const uint4 *>(eb + r * 128 + ((ch ^ (r & 7)) << 4));
+                                if (quad * 32 + src < x_count)
+                                    *reinterpret_cast<uint4 *>(a.part_o + int64_t(pr) * D + c0 + ch * 8) = val;
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
                     }
                 }
                 if (has) a.part_ml[part] = make_float2(m2, lrow);
