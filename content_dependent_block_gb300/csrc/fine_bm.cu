@@ -79,7 +79,6 @@ __device__ __forceinline__ int gather_index(int w) { return w >= 8 && w < 12 ? w
 __device__ __forceinline__ int merge_index(int w) { return w >= 13 ? w - 13 : -1; }
 constexpr int kGather = 128;             // gather threads (warps 8-11)
 constexpr int kMergeWarps = 3;
-constexpr int kStageBytes = 17408;       // one merge stage: >= 2 queries at d = 128, k = 32
 constexpr unsigned kFull = 0xffffffffu;
 
 // Per-tile constants, computed once by the gather group: keys in the block
@@ -102,7 +101,9 @@ struct Cfg {
     static constexpr int kSub = D / 64;
     static constexpr int kNQ = D == 64 ? 3 : 2;            // Q stages
     static constexpr int kNKV = D == 64 ? 3 : 2;           // K/V buffers (items in flight)
-    static constexpr int kMS = D == 64 ? 2 : 1;            // merge stages per merge warp
+    static constexpr int kMS = 2;                          // merge stages per merge warp
+    // one merge stage: >= 4 queries at d = 64, >= 1 at d = 128 (k <= 32)
+    static constexpr int kStageBytes = D == 64 ? 17408 : 8704;
     static constexpr int kQBytes = kSub * kTile * 128;
     static constexpr int kKBytes = kSub * kB * 128;        // K or V of one block
     static constexpr int oQ = 0;
@@ -246,6 +247,50 @@ __device__ __forceinline__ bool merge_query(const uint16_t *po, const float *pml
         acc[c] = (c0 == 0 ? a0[c] : a1[c]) * invL;
         acc[8 + c] = (c0 == 0 ? a1[c] : a0[c]) * invL;
     }
+    return true;
+}
+
+// The same merge at d = 128, one query per warp: lane l owns channels
+// [4 l, 4 l + 4) (one 8-byte chunk per slot; a slot's row is 256 contiguous
+// bytes, so the lanes read it without bank conflicts) and slot l's (m, l).
+// A stage of such queries is small, so that two fit per merge warp.  The
+// weights and chunks of eight slots are fetched before their FMAs (the loop
+// is latency-bound: one shuffle and one shared load per slot).
+template <bool kOpts>
+__device__ __forceinline__ bool merge_query_w(const uint16_t *po, const float *pml, uint32_t vm, int k,
+                                              int lane, float (&acc)[4], float &lse) {
+    const bool listed = ((vm >> lane) & 1u) != 0;
+    const float m = listed ? pml[2 * lane] : -INFINITY;
+    const float lv = listed ? pml[2 * lane + 1] : 0.f;
+    const float M = warp_max(m);
+    // unlisted slots hold -inf, and so does a partial that admitted no key
+    const bool use = kOpts ? m > -INFINITY : listed;
+    const float w = use ? ex2(m - M) : 0.f;
+    const float L = warp_sum(w * lv);
+    float a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int s0 = 0; s0 < k; s0 += 8) {
+        float ws[8];
+        uint2 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            ws[u] = __shfl_sync(kFull, w, (s0 + u) & 31);
+            ws[u] = s0 + u < k ? ws[u] : 0.f;
+            x[u] = ws[u] != 0.f ? *reinterpret_cast<const uint2 *>(po + (s0 + u) * 128) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            a4[0] = fmaf(ws[u], bf16_low_half(x[u].x), a4[0]);
+            a4[1] = fmaf(ws[u], bf16_high_half(x[u].x), a4[1]);
+            a4[2] = fmaf(ws[u], bf16_low_half(x[u].y), a4[2]);
+            a4[3] = fmaf(ws[u], bf16_high_half(x[u].y), a4[3]);
+        }
+    }
+    lse = L > 0.f ? M + __log2f(L) : -INFINITY;
+    if (L == 0.f) return false;
+    const float invL = 1.f / L;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = a4[c] * invL;
     return true;
 }
 
@@ -788,7 +833,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         // shared-memory stages (one bulk copy for the partial o block and one
         // for the lse values of up to qs consecutive queries).  A group of
         // D/16 lanes merges one query, each lane owning 16 channels.
-        constexpr int LPQ = D / 16;                  // lanes per query
+        constexpr bool kWide = D == 128;             // one query per warp (merge_query_w)
+        constexpr int LPQ = kWide ? 32 : D / 16;     // lanes per query
+        constexpr int CPL = D / LPQ;                 // channels per lane
         constexpr int QP = 32 / LPQ;                 // queries per pass
         const int mw = merge_index(warp);
         const int gq = lane / LPQ, gl = lane % LPQ;
@@ -796,9 +843,9 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
         const int32_t full_valid = a.full_lists ? int32_t(i64min(k, nb)) : 0;
         const uint32_t full_mask = full_valid >= 32 ? kFull : ((1u << full_valid) - 1u);
         const int64_t per_q = kpad * D * 2 + kpad * 8;
-        const int qs = int(kStageBytes / per_q);                  // queries per stage (>= 2)
+        const int qs = int(C::kStageBytes / per_q);               // queries per stage (>= QP)
         const int64_t o_cap = int64_t(qs) * kpad * D * 2;         // lse offset within a stage
-        uint8_t *stage0 = sm + C::oMs + mw * C::kMS * kStageBytes;
+        uint8_t *stage0 = sm + C::oMs + mw * C::kMS * C::kStageBytes;
         uint64_t *msbar = bars + C::bMsFull + mw * C::kMS;
         uint32_t sc = 0;                                          // stages used so far
         for (;;) {
@@ -832,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                 const int qn = min(qs, nq - c * qs);
                 const uint32_t bo = uint32_t(qn * kpad * D * 2), bl = uint32_t(qn * kpad * 8);
                 const int64_t sl = slot0 + int64_t(c) * qs * kpad;
-                uint8_t *st = stage0 + b * kStageBytes;
+                uint8_t *st = stage0 + b * C::kStageBytes;
                 tc::mbar_arrive_expect_tx(msbar + b, bo + bl);
                 tc::bulk_g2s(st, a.part_o + sl * D, bo, msbar + b);
                 tc::bulk_g2s(st + o_cap, a.part_ml + sl, bl, msbar + b);
@@ -843,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
             for (int c = 0; c < nch; ++c) {
                 const uint32_t u = sc + uint32_t(c), b = u % C::kMS;
                 const int q0 = c * qs, qn = min(qs, nq - q0);
-                const uint8_t *st = stage0 + b * kStageBytes;
+                const uint8_t *st = stage0 + b * C::kStageBytes;
                 if (!tc::mbar_wait(msbar + b, (u / C::kMS) & 1, status)) {
                     ok = false;
                     break;
@@ -863,25 +910,32 @@ __global__ void __launch_bounds__(kThreads, 1) fine_ws_kernel(
                         vm = __shfl_sync(kFull, vml, (q0 + jq) & 31);
                         if (!act) vm = 0u;
                     }
-                    float acc[16];
-                    const uint16_t *po = reinterpret_cast<const uint16_t *>(st) + jq * kpad * D + gl * 16;
+                    float acc[CPL];
+                    const uint16_t *po = reinterpret_cast<const uint16_t *>(st) + jq * kpad * D + gl * CPL;
                     const float *pl = reinterpret_cast<const float *>(st + o_cap) + 2 * jq * kpad;
                     // every lane takes part (the merge shuffles across the warp); a
                     // query with nothing listed was zeroed by the inversion, one
                     // whose listed blocks admit nothing (causal mask) is zeroed here
                     float lse = -INFINITY;
-                    const bool any = merge_query<D, kOpts>(po, pl, vm, k, lane, acc, lse);
+                    bool any;
+                    if constexpr (kWide) any = merge_query_w<kOpts>(po, pl, vm, k, lane, acc, lse);
+                    else any = merge_query<D, kOpts>(po, pl, vm, k, lane, acc, lse);
                     if (a.lse_out != nullptr && act && gl == 0) a.lse_out[qrow] = lse;
                     if (act && (any || kOpts)) {
                         if (!any) {
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+                            for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
                         }
-                        uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow * D + gl * 16);
-                        dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                            pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-                        dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                            pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+                        if constexpr (CPL == 16) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(a.out + qrow * D + gl * 16);
+                            dst[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                            dst[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                                pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+                        } else {
+                            *reinterpret_cast<uint2 *>(a.out + qrow * D + gl * 4) =
+                                make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+                        }
                     }
                 }
                 __syncwarp();                             // stage read by every lane
