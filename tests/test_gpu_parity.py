@@ -224,6 +224,31 @@ def test_fine_empty_rows_give_zeros_and_bad_index_is_reported():
     assert nb == 8
 
 
+@pytest.mark.parametrize("bh,n,d,k", [(16, 8192, 64, 16), (4, 8192, 128, 12)])
+def test_fine_padded_lists_across_query_ranges(bh, n, d, k):
+    """Caller lists with padding (a quarter of the slots -1, every 97th row
+    empty) through the block-major fine stage, at sizes with several query
+    ranges per head and more ranges than the partial-state ring holds (the
+    ring is reused): the merge takes each query's valid slots from the
+    inversion's slot masks."""
+    import torch
+    t, (q, kk, v) = _small(bh, n, d, seed=11 + d, sigma=0.5)
+    nb = -(-n // 64)
+    rng = np.random.Generator(np.random.PCG64(7 + d))
+    lst = rng.random((bh * n, nb)).argsort(axis=1)[:, :k].astype(np.int32)
+    lst[rng.random((bh * n, k)) < 0.25] = -1
+    lst[::97] = -1
+    out = bsa.fine_attention(q, kk, v, torch.from_numpy(lst).cuda().reshape(bh, n, k), key_block=64)
+    assert bsa.device_status() == 0
+    rows = workloads.sample_rows(bh, n, 40, extra=(63, 64, 97 * 3, n // 2))
+    got = parity.from_device(out).reshape(-1, d)[rows]
+    empty = (lst[rows] < 0).all(axis=1)
+    assert empty.any() and (~empty).any()
+    assert (parity.out_f64(got[empty]) == 0).all()
+    o_ref, _, _ = oracle.fine(t.q, t.k, t.v, 64, lst[rows][~empty], rows[~empty])
+    parity.assert_close(got[~empty], o_ref, "bf16", "padded lists")
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 def test_fine_explicit_scale_and_dtype(dtype):
     import torch
