@@ -37,7 +37,9 @@
 //                           done, pulls the queries' partial states into
 //                           shared-memory stages with bulk copies and merges
 //                           each query's k states in slot order (the
-//                           online-softmax merge of (m, l, acc))
+//                           online-softmax merge of (m, l, acc)); the valid
+//                           slots come from the inversion's per-query masks
+//                           (padded lists); at d = 128 one query per warp
 //
 // Partial states of a range live in ring entry (range mod R), R the ring
 // depth (4, 8 or 16 ranges: as many as fit about 72 MB of partial states); a
@@ -110,7 +112,7 @@ struct Cfg {
     static constexpr int oK = oQ + kNQ * kQBytes;
     static constexpr int oV = oK + kNKV * kKBytes;
     static constexpr int oMs = oV + kNKV * kKBytes;        // merge stages
-    static constexpr int oEpi = oMs + kMergeWarps * kMS * kStageBytes;  // 8 warps x 32 rows x 64 B
+    static constexpr int oEpi = oMs + kMergeWarps * kMS * kStageBytes;  // 8 owner warps x 2 KB
     static constexpr int oPid = oEpi + 8 * 2048;           // int32  [2][kNTW][128]
     static constexpr int oTi = oPid + 2 * kNTW * kTile * 4;     // TileInfo [2][kNTW]
     static constexpr int oItem = oTi + 2 * kNTW * int(sizeof(TileInfo));   // StagedItem [kNI]
