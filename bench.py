@@ -533,9 +533,12 @@ def run_static(args, w, device, dist):
 
 def run_backward(args, w, fwd, q, k, v, device, dist):
     """The fine stage's backward pass over the lists (and output) of one
-    forward: bsa_fine_backward timed alone, CUDA events, L2 flushed before
-    every step, clocks sampled around the timed steps; one JSON line.  With
-    64-key blocks it runs on the tensor cores (bwd_tc_kernel in
+    forward: bsa_fine_backward_lse timed alone, given the rows' log2-sum-exp
+    that the forward saved (bsa_fine_attention_lse, untimed, as a training
+    step keeps it), CUDA events, L2 flushed before every step, clocks sampled
+    around the timed steps; one JSON line, which also reports the same steps
+    through bsa_fine_backward (statistics recomputed by a forward pass).
+    With 64-key blocks it runs on the tensor cores (bwd_tc_kernel in
     csrc/backward.cu); the roofline takes its contractions at the tensor
     peak, its softmax ops at the FP32 peak and its bytes at the HBM
     bandwidth."""
@@ -550,8 +553,16 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
     ws_n = L.bsa_fine_backward_workspace_size(fwd.shape, ld)
     ws = bsa._workspace(ws_n, device)
     P = bsa._ptr
+    # the rows' log2-sum-exp as the forward saves it (same lists, same output)
+    _, lse = bsa.fine_attention_lse(q, k, v, fwd.idx.contiguous(), key_block=w.key_block,
+                                    causal=w.causal)
 
     def step():
+        bsa._check(L.bsa_fine_backward_lse(fwd.shape, P(q), P(k), P(v), P(fwd.out), P(dout),
+                                           P(fwd.idx), ld, m, 0.0, P(lse), P(dq), P(dk), P(dv),
+                                           P(ws), ws_n, bsa._stream()))
+
+    def step_recompute():
         bsa._check(L.bsa_fine_backward(fwd.shape, P(q), P(k), P(v), P(fwd.out), P(dout),
                                        P(fwd.idx), ld, m, 0.0, P(dq), P(dk), P(dv), P(ws), ws_n,
                                        bsa._stream()))
@@ -569,10 +580,9 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
     stream = torch.cuda.current_stream(device)
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or 0) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else device.index
-    with ClockSampler(gpu_index) as clocks:
-        preroll(step, args.preroll_s, lambda: torch.cuda.synchronize(device))
+    def timed(fn):
         for _ in range(args.warmup):
-            step()
+            fn()
         torch.cuda.synchronize(device)
         evs = []
         for _ in range(args.steps):
@@ -580,23 +590,28 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step()
+            fn()
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize(device)
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    with ClockSampler(gpu_index) as clocks:
+        preroll(step, args.preroll_s, lambda: torch.cuda.synchronize(device))
+        ms = timed(step)
+        ms_recompute = timed(step_recompute)
     clk = clocks.summary()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     pairs = admitted_pairs(fwd.idx, w)
     # per admitted (query, key) pair: q.k, dO.v, dQ, dK and dV updates (2d each,
-    # tensor cores) + softmax ops; the forward pass the backward repeats for the
-    # rows' log2-sum-exp is not credited
+    # tensor cores) + softmax ops
     flops = pairs * (10 * w.d + 5)
     peaks = measured_peaks()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     achieved = flops / (ms * 1e-3) / 1e12
     rl = roofline(10 * w.d * pairs, 5 * pairs, 5 * w.n * w.bh * w.d * 2 + 3 * w.n * w.bh * w.d * 4,
-                  ms, peaks, sms, "fine-stage backward: one bsa_fine_backward call (forward pass for "
-                  "the rows' log2-sum-exp, D = dO.O, list inversion, tensor-core dQ/dK/dV kernel)", None)
+                  ms, peaks, sms, "fine-stage backward: one bsa_fine_backward_lse call (list "
+                  "inversion, D = dO.O, tensor-core dQ/dK/dV kernel; the rows' log2-sum-exp saved by "
+                  "the forward)", None)
     status = bsa.device_status()
     if dist is not None:
         dist.destroy_process_group()
@@ -607,6 +622,8 @@ def run_backward(args, w, fwd, q, k, v, device, dist):
         "data": "synthetic", "config": config_of(w),
         "roofline": rl,
         "admitted_pairs": pairs, "flops_per_step": flops, "clocks": clk,
+        "recompute_stats": {"call": "bsa_fine_backward (a forward pass recomputes the rows' "
+                                    "log2-sum-exp)", "ms_per_step": ms_recompute},
         "device_status": status}), flush=True)
     return 0 if status == 0 else 1
 

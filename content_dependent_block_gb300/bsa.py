@@ -27,7 +27,8 @@ STATUS = {0: "BSA_OK", 1: "BSA_ERR_INVALID_ARG", 2: "BSA_ERR_UNSUPPORTED",
 EXPORTS = (
     "bsa_pool_blocks", "bsa_coarse_topk_workspace_size", "bsa_coarse_topk",
     "bsa_coarse_topk_ex", "bsa_fine_attention_workspace_size", "bsa_fine_attention",
-    "bsa_fine_backward_workspace_size", "bsa_fine_backward",
+    "bsa_fine_attention_lse", "bsa_fine_backward_workspace_size", "bsa_fine_backward",
+    "bsa_fine_backward_lse",
     "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_ex", "bsa_forward_noalloc",
     "bsa_forward_launches", "bsa_forward_graph_create", "bsa_graph_launch", "bsa_graph_destroy",
     "bsa_static_max_blocks",
@@ -90,9 +91,13 @@ def lib():
                                i32),
         "bsa_fine_attention_workspace_size": ([Shape, ListDesc, Mask], sz),
         "bsa_fine_attention": ([Shape, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, sz, vp], i32),
+        "bsa_fine_attention_lse": ([Shape, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, vp, sz, vp],
+                                   i32),
         "bsa_fine_backward_workspace_size": ([Shape, ListDesc], sz),
         "bsa_fine_backward": ([Shape, vp, vp, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, vp, vp, sz,
                                vp], i32),
+        "bsa_fine_backward_lse": ([Shape, vp, vp, vp, vp, vp, vp, ListDesc, Mask, f32, vp, vp, vp, vp,
+                                   vp, sz, vp], i32),
         "bsa_forward_workspace_size": ([Shape, i32, i32], sz),
         "bsa_forward": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp], i32),
         "bsa_forward_ex": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp, vp, vp,
@@ -219,11 +224,33 @@ def fine_attention(q, k, v, block_list=None, *, key_block: int, q_group: int = 1
     return out
 
 
+def fine_attention_lse(q, k, v, block_list, *, key_block: int, causal: bool = False,
+                       scale: float = 0.0, out=None):
+    """(O, lse): fine attention over the per-query lists ``block_list``
+    [bh, n, k] and each query's log2-sum-exp (fp32 [bh, n]) for
+    fine_backward(..., lse=lse); see bsa_fine_attention_lse in bsa.h."""
+    torch = _torch()
+    s = _shape(q)
+    if block_list.dtype != torch.int32 or not block_list.is_contiguous():
+        raise TypeError("block_list must be a contiguous int32 tensor")
+    ld = ListDesc(1, key_block, block_list.shape[-1], 1)
+    m = mask_struct(MASK_CAUSAL if causal else MASK_NONE)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    ws_n = lib().bsa_fine_attention_workspace_size(s, ld, m)
+    ws = _workspace(ws_n, q.device)
+    _check(lib().bsa_fine_attention_lse(s, _ptr(q), _ptr(k), _ptr(v), _ptr(block_list), ld, m,
+                                        float(scale), _ptr(out), _ptr(lse), _ptr(ws), ws_n,
+                                        _stream()))
+    return out, lse
+
+
 def fine_backward(q, k, v, out, dout, block_list, *, key_block: int, causal: bool = False,
-                  scale: float = 0.0):
+                  scale: float = 0.0, lse=None):
     """Gradients (dq, dk, dv), fp32 [bh, n, d], of the fine stage over the
-    per-query lists ``block_list`` [bh, n, k] (held fixed); see
-    bsa_fine_backward in bsa.h."""
+    per-query lists ``block_list`` [bh, n, k] (held fixed); with ``lse``
+    (from fine_attention_lse on the same inputs) the softmax statistics are
+    not recomputed.  See bsa_fine_backward / bsa_fine_backward_lse in bsa.h."""
     torch = _torch()
     s = _shape(q)
     if block_list.dtype != torch.int32 or not block_list.is_contiguous():
@@ -233,9 +260,17 @@ def fine_backward(q, k, v, out, dout, block_list, *, key_block: int, causal: boo
     dq, dk, dv = (torch.empty(q.shape, dtype=torch.float32, device=q.device) for _ in range(3))
     ws_n = lib().bsa_fine_backward_workspace_size(s, ld)
     ws = _workspace(ws_n, q.device)
-    _check(lib().bsa_fine_backward(s, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
-                                   _ptr(block_list), ld, m, float(scale), _ptr(dq), _ptr(dk),
-                                   _ptr(dv), _ptr(ws), ws_n, _stream()))
+    if lse is None:
+        _check(lib().bsa_fine_backward(s, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                       _ptr(block_list), ld, m, float(scale), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), _ptr(ws), ws_n, _stream()))
+    else:
+        if lse.dtype != torch.float32 or not lse.is_contiguous():
+            raise TypeError("lse must be a contiguous float32 tensor [bh, n]")
+        _check(lib().bsa_fine_backward_lse(s, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                           _ptr(block_list), ld, m, float(scale), _ptr(lse),
+                                           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws_n,
+                                           _stream()))
     return dq, dk, dv
 
 

@@ -209,16 +209,16 @@ bool bm_path(const bsa_shape &s, int32_t kb, int64_t nb) {
            s.bh * s.n * int64_t(32) < (int64_t(1) << 31);
 }
 
-// Invert the lists and run the block-major fine stage; ws points at L.
-cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const void *v,
-                        const int32_t *list, int32_t kb, int32_t topk, bool full_lists,
-                        bool causal, const bsa::SelectOpts *sel, float scale_log2, void *out,
-                        char *ws, const BmLayout &L, int32_t *status, cudaStream_t st,
-                        float *lse_out = nullptr) {
+// The lists' inversion and the block-major stage's work lists (count ->
+// scan -> scatter) into the workspace at L; rows whose list admits nothing
+// get zeros in out.
+cudaError_t run_invert_bm(const bsa_shape &s, const int32_t *list, int32_t kb, int32_t topk,
+                          void *out, char *ws, const BmLayout &L, int32_t *status,
+                          cudaStream_t st, bsa::InvertBuffers &w) {
     const int64_t nb = ceil_div(s.n, kb);
     cudaError_t e = cudaMemsetAsync(ws + L.zero, 0, L.zero_bytes, st);
     if (e != cudaSuccess) return e;
-    bsa::InvertBuffers w{};
+    w = bsa::InvertBuffers{};
     w.counts = reinterpret_cast<int32_t *>(ws + L.counts);
     w.cursors = reinterpret_cast<int32_t *>(ws + L.cursors);
     w.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
@@ -233,8 +233,19 @@ cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const 
     w.n_merge = reinterpret_cast<int32_t *>(ws + L.n_merge);
     w.entries = reinterpret_cast<int32_t *>(ws + L.entries);
     w.vmask = reinterpret_cast<uint32_t *>(ws + L.vmask);
-    e = bsa::launch_invert(list, s.bh, s.n, nb, topk, L.plan, w, static_cast<uint16_t *>(out), s.d,
-                           status, st);
+    return bsa::launch_invert(list, s.bh, s.n, nb, topk, L.plan, w, static_cast<uint16_t *>(out),
+                              s.d, status, st);
+}
+
+// Invert the lists and run the block-major fine stage; ws points at L.
+cudaError_t run_fine_bm(const bsa_shape &s, const void *q, const void *k, const void *v,
+                        const int32_t *list, int32_t kb, int32_t topk, bool full_lists,
+                        bool causal, const bsa::SelectOpts *sel, float scale_log2, void *out,
+                        char *ws, const BmLayout &L, int32_t *status, cudaStream_t st,
+                        float *lse_out = nullptr) {
+    const int64_t nb = ceil_div(s.n, kb);
+    bsa::InvertBuffers w{};
+    cudaError_t e = run_invert_bm(s, list, kb, topk, out, ws, L, status, st, w);
     if (e != cudaSuccess) return e;
     bsa::FineBmArgs a{};
     a.k_ptr = k;
@@ -391,9 +402,13 @@ size_t bsa_fine_attention_workspace_size(bsa_shape shape, bsa_list_desc ld, bsa_
     return 0;   // the query-major path needs none
 }
 
-bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, const void *v,
-                              const int32_t *list, bsa_list_desc ld, bsa_mask mask, float scale,
-                              void *out, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+
+// bsa_fine_attention, with each row's log2-sum-exp into lse_out (non-NULL
+// only on the block-major path)
+bsa_status fine_attention_impl(bsa_shape shape, const void *q, const void *k, const void *v,
+                               const int32_t *list, bsa_list_desc ld, bsa_mask mask, float scale,
+                               void *out, float *lse_out, void *ws, size_t ws_bytes, void *stream) {
     BSA_TRY(check_shape(shape));
     BSA_TRY(check_key_block(ld.key_block));
     BSA_TRY(check_ptr(q, "q"));
@@ -420,7 +435,7 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
         const BmLayout L = bm_layout(shape, ld.key_block, ld.max_blocks, 0);
         return launched(run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false,
                                     mask.kind == BSA_MASK_CAUSAL, nullptr, sl2, out,
-                                    static_cast<char *>(ws), L, status, st),
+                                    static_cast<char *>(ws), L, status, st, lse_out),
                         "fine attention (block-major) launch");
     }
     bsa::FineArgs a{};
@@ -455,6 +470,31 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, con
         return launched(bsa::launch_fine_static_tc(a, st), "fine attention (tensor-core tiles) launch");
     }
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
+}
+
+}  // namespace
+
+bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k, const void *v,
+                              const int32_t *list, bsa_list_desc ld, bsa_mask mask, float scale,
+                              void *out, void *ws, size_t ws_bytes, void *stream) {
+    return fine_attention_impl(shape, q, k, v, list, ld, mask, scale, out, nullptr, ws, ws_bytes,
+                               stream);
+}
+
+bsa_status bsa_fine_attention_lse(bsa_shape shape, const void *q, const void *k, const void *v,
+                                  const int32_t *list, bsa_list_desc ld, bsa_mask mask,
+                                  float scale, void *out, float *lse_out, void *ws,
+                                  size_t ws_bytes, void *stream) {
+    BSA_TRY(check_shape(shape));
+    BSA_TRY(check_key_block(ld.key_block));
+    if (lse_out == nullptr) return fail(BSA_ERR_INVALID_ARG, "lse_out is NULL");
+    if (!aligned(lse_out, 4)) return fail(BSA_ERR_ALIGNMENT, "lse_out is not 4-byte aligned");
+    if (!fine_uses_bm(shape, list, ld, mask))
+        return fail(BSA_ERR_UNSUPPORTED,
+                    "the log2-sum-exp output needs the block-major path (per-query lists, bf16, "
+                    "key_block 64, max_blocks <= 32, no mask or the causal one)");
+    return fine_attention_impl(shape, q, k, v, list, ld, mask, scale, out, lse_out, ws, ws_bytes,
+                               stream);
 }
 
 size_t bsa_forward_workspace_size(bsa_shape shape, int32_t key_block, int32_t topk) {
@@ -613,10 +653,15 @@ size_t bsa_fine_backward_workspace_size(bsa_shape shape, bsa_list_desc ld) {
     return bwd_layout(shape, ld.key_block, ld.max_blocks).total;
 }
 
-bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, const void *v,
-                             const void *out, const void *dout, const int32_t *list,
-                             bsa_list_desc ld, bsa_mask mask, float scale, float *dq, float *dk,
-                             float *dv, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+
+// bsa_fine_backward; with lse_in (the forward's log2-sum-exp per row) the
+// tensor-core path inverts the lists and skips the statistics pass
+bsa_status fine_backward_impl(bsa_shape shape, const void *q, const void *k, const void *v,
+                              const void *out, const void *dout, const int32_t *list,
+                              bsa_list_desc ld, bsa_mask mask, float scale, const float *lse_in,
+                              float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
+                              void *stream) {
     BSA_TRY(check_shape(shape));
     if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "the backward pass takes bf16");
     BSA_TRY(check_key_block(ld.key_block));
@@ -677,18 +722,49 @@ bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, cons
     a.qlist = reinterpret_cast<int32_t *>(base + L.qlist);
     a.status = status;
     if (tc_path) {
-        // the forward fine stage once more: every row's log2-sum-exp, and the
-        // lists inverted by (head, query range, block)
         const BmLayout F = bm_layout(shape, ld.key_block, ld.max_blocks, L.fwd);
-        e = run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false, a.causal != 0,
-                        nullptr, a.scale_log2, base + L.o_scratch, base, F, status, st, a.lse);
-        if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "backward (forward pass): %s", cudaGetErrorString(e));
+        if (lse_in != nullptr) {
+            // the lists inverted by (head, query range, block); the row
+            // statistics are the forward's (read only by the gradient kernel)
+            bsa::InvertBuffers w{};
+            e = run_invert_bm(shape, list, ld.key_block, ld.max_blocks, base + L.o_scratch, base, F,
+                              status, st, w);
+            a.lse = const_cast<float *>(lse_in);
+        } else {
+            // the forward fine stage once more: every row's log2-sum-exp, and
+            // the lists inverted by (head, query range, block)
+            e = run_fine_bm(shape, q, k, v, list, ld.key_block, ld.max_blocks, false,
+                            a.causal != 0, nullptr, a.scale_log2, base + L.o_scratch, base, F,
+                            status, st, a.lse);
+        }
+        if (e != cudaSuccess) return fail(BSA_ERR_CUDA, "backward (statistics): %s", cudaGetErrorString(e));
         a.bin_offsets = reinterpret_cast<const int32_t *>(base + F.offsets);
         a.entries = reinterpret_cast<const int32_t *>(base + F.entries);
         a.nranges = F.plan.nranges;
         return launched(bsa::launch_fine_backward_tc(a, st), "backward launch");
     }
     return launched(bsa::launch_fine_backward(a, st), "backward launch");
+}
+
+}  // namespace
+
+bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k, const void *v,
+                             const void *out, const void *dout, const int32_t *list,
+                             bsa_list_desc ld, bsa_mask mask, float scale, float *dq, float *dk,
+                             float *dv, void *ws, size_t ws_bytes, void *stream) {
+    return fine_backward_impl(shape, q, k, v, out, dout, list, ld, mask, scale, nullptr, dq, dk,
+                              dv, ws, ws_bytes, stream);
+}
+
+bsa_status bsa_fine_backward_lse(bsa_shape shape, const void *q, const void *k, const void *v,
+                                 const void *out, const void *dout, const int32_t *list,
+                                 bsa_list_desc ld, bsa_mask mask, float scale, const float *lse,
+                                 float *dq, float *dk, float *dv, void *ws, size_t ws_bytes,
+                                 void *stream) {
+    if (lse == nullptr) return fail(BSA_ERR_INVALID_ARG, "lse is NULL");
+    if (!aligned(lse, 4)) return fail(BSA_ERR_ALIGNMENT, "lse is not 4-byte aligned");
+    return fine_backward_impl(shape, q, k, v, out, dout, list, ld, mask, scale, lse, dq, dk, dv,
+                              ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------- failure path

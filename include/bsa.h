@@ -199,6 +199,25 @@ bsa_status bsa_fine_attention(bsa_shape shape, const void *q, const void *k,
                               void *stream);
 
 /*
+ * bsa_fine_attention that also returns each query's log2-sum-exp
+ * lse_i = log2 sum_{j in T_i} 2^(s_ij * scale * log2 e), the softmax's
+ * normaliser in base 2 ("The Triton kernel": the row statistics m and l of
+ * the online softmax, lse = m + log2 l), for a backward pass to reuse
+ * (bsa_fine_backward_lse).  A query whose list admits no key gets -inf.
+ *   lse_out  [bh][n] fp32 (device), 4-byte aligned.
+ * Only where bsa_fine_attention takes its block-major path: per-query lists
+ * (q_group 1, per_head 1, max_blocks <= 32), bf16, d in {64, 128},
+ * key_block 64, at most 16384 blocks, no mask or the causal one; other calls
+ * return BSA_ERR_UNSUPPORTED.  Workspace and everything else as
+ * bsa_fine_attention.
+ */
+bsa_status bsa_fine_attention_lse(bsa_shape shape, const void *q, const void *k,
+                                  const void *v, const int32_t *list,
+                                  bsa_list_desc ld, bsa_mask mask, float scale,
+                                  void *out, float *lse_out, void *ws,
+                                  size_t ws_bytes, void *stream);
+
+/*
  * Backward pass of the fine stage (page "sparse-attention-triton-bench",
  * What's next: a backward pass through the sparse softmax-weighted sum over
  * the selected blocks).  The selection is a discrete choice and is held
@@ -230,6 +249,24 @@ bsa_status bsa_fine_backward(bsa_shape shape, const void *q, const void *k,
                              bsa_mask mask, float scale, float *dq, float *dk,
                              float *dv, void *ws, size_t ws_bytes,
                              void *stream);
+
+/*
+ * bsa_fine_backward given the forward's log2-sum-exp per query (as
+ * bsa_fine_attention_lse writes it, for the same inputs, lists, mask and
+ * scale), so that the softmax statistics are not recomputed: on the
+ * tensor-core path (key_block 64, max_blocks <= 32) the call inverts the
+ * lists and runs the gradient kernels only.  Other shapes recompute the
+ * statistics as bsa_fine_backward does and ignore lse.
+ *   lse  [bh][n] fp32 (device), 4-byte aligned; not modified.
+ * Same workspace (bsa_fine_backward_workspace_size) and outputs as
+ * bsa_fine_backward.
+ */
+bsa_status bsa_fine_backward_lse(bsa_shape shape, const void *q, const void *k,
+                                 const void *v, const void *out, const void *dout,
+                                 const int32_t *list, bsa_list_desc ld,
+                                 bsa_mask mask, float scale, const float *lse,
+                                 float *dq, float *dk, float *dv, void *ws,
+                                 size_t ws_bytes, void *stream);
 
 /*
  * The whole dynamic forward: pool -> score + top-k -> fine attention, all

@@ -100,3 +100,47 @@ def test_backward_bad_index_is_reported():
     lst[0, 5, 2] = 99
     bsa.fine_backward(q, kk, v, out, parity.to_device(do, "bf16"), lst, key_block=64)
     assert bsa.device_status() == 3                           # BSA_ERR_BAD_INDEX
+
+
+@pytest.mark.parametrize("bh,n,d,k,causal", [
+    (2, 513, 64, 6, False),       # random lists with empty rows, a one-token last block
+    (1, 700, 128, 5, True),
+    (2, 4100, 64, 16, True),
+])
+def test_saved_lse_forward_and_backward(bh, n, d, k, causal):
+    """bsa_fine_attention_lse: the same O as bsa_fine_attention and each row's
+    log2-sum-exp equal to the oracle's (its natural-log lse / ln 2; -inf for
+    an empty row); bsa_fine_backward_lse with that lse: the oracle's
+    gradients without the statistics pass."""
+    import torch
+    kb = 64
+    t, do = _inputs(bh, n, d, seed=n + d + k + 3, kb=kb)
+    q, kk, v = (parity.to_device(getattr(t, x), "bf16") for x in "qkv")
+    dout = parity.to_device(do, "bf16")
+    idx_np = _random_lists(bh, n, kb, k, seed=11, causal=causal)
+    lst = torch.from_numpy(idx_np).cuda().reshape(bh, n, k)
+    mask = bsa.mask_struct(bsa.MASK_CAUSAL if causal else bsa.MASK_NONE)
+    out = bsa.fine_attention(q, kk, v, lst, key_block=kb, mask=mask)
+    out2, lse = bsa.fine_attention_lse(q, kk, v, lst, key_block=kb, causal=causal)
+    assert torch.equal(out, out2)
+    rows = oracle.all_rows(bh, n)
+    _, ref_lse, _ = oracle.fine(t.q, t.k, t.v, kb, idx_np, rows, causal=causal)
+    got = lse.cpu().numpy().reshape(-1).astype(np.float64)
+    ref2 = ref_lse / np.log(2.0)
+    empty = ~np.isfinite(ref2)
+    assert empty.any() and (got[empty] == -np.inf).all()
+    assert np.abs(got[~empty] - ref2[~empty]).max() <= 1e-3 * max(1.0, np.abs(ref2[~empty]).max())
+    dq, dk, dv = bsa.fine_backward(q, kk, v, out, dout, lst, key_block=kb, causal=causal, lse=lse)
+    rq, rk, rv = oracle.fine_backward(t.q, t.k, t.v, do, kb, idx_np, causal=causal)
+    for name, g, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        _grad_close(g.cpu().numpy(), ref, f"{name} (saved lse) bh={bh} n={n} d={d} k={k}")
+    assert bsa.device_status() == 0
+
+
+def test_saved_lse_outside_the_block_major_path_is_unsupported():
+    import torch
+    t, _ = _inputs(1, 256, 64, seed=2, kb=32)
+    q, kk, v = (parity.to_device(getattr(t, x), "bf16") for x in "qkv")
+    lst = torch.zeros((1, 256, 2), dtype=torch.int32, device="cuda")
+    with pytest.raises(bsa.BsaError):
+        bsa.fine_attention_lse(q, kk, v, lst, key_block=32)
