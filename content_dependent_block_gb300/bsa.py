@@ -29,7 +29,8 @@ EXPORTS = (
     "bsa_coarse_topk_ex", "bsa_fine_attention_workspace_size", "bsa_fine_attention",
     "bsa_fine_attention_lse", "bsa_fine_backward_workspace_size", "bsa_fine_backward",
     "bsa_fine_backward_lse",
-    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_ex", "bsa_forward_noalloc",
+    "bsa_forward_workspace_size", "bsa_forward", "bsa_forward_ex", "bsa_forward_lse",
+    "bsa_forward_noalloc",
     "bsa_forward_launches", "bsa_forward_graph_create", "bsa_graph_launch", "bsa_graph_destroy",
     "bsa_static_max_blocks",
     "bsa_static_blocks", "bsa_get_device_status", "bsa_selftest_wait_timeout", "bsa_status_string",
@@ -102,6 +103,8 @@ def lib():
         "bsa_forward": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp, sz, vp], i32),
         "bsa_forward_ex": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp, vp, vp,
                             sz, vp], i32),
+        "bsa_forward_lse": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp, vp, vp,
+                             vp, sz, vp], i32),
         "bsa_forward_noalloc": ([Shape, vp, vp, vp, i32, i32, f32, vp, vp, vp], i32),
         "bsa_forward_graph_create": ([Shape, vp, vp, vp, i32, i32, ctypes.POINTER(Select), f32, vp,
                                       vp, vp, sz, ctypes.POINTER(vp)], i32),
@@ -346,6 +349,25 @@ def forward(q, k, v, key_block: int, topk: int, scale: float = 0.0, *, head_topk
                 head_topk=head_topk, causal=causal, local_block=local_block)
     out = f(q, k, v, keep_idx=True)
     return out, f.idx
+
+
+def forward_lse(q, k, v, key_block: int, topk: int, scale: float = 0.0, *, head_topk=None,
+                causal: bool = False, local_block: bool = False):
+    """Whole dynamic forward that also keeps each query's log2-sum-exp for
+    fine_backward(..., lse=lse); returns (out, idx, lse).  See
+    bsa_forward_lse in bsa.h."""
+    torch = _torch()
+    s = _shape(q)
+    out = torch.empty_like(q)
+    idx = torch.empty((s.bh, s.n, topk), dtype=torch.int32, device=q.device)
+    lse = torch.empty((s.bh, s.n), dtype=torch.float32, device=q.device)
+    sel = _select(head_topk, causal, local_block)
+    ws_n = lib().bsa_forward_workspace_size(s, key_block, topk)
+    ws = _workspace(ws_n, q.device)
+    _check(lib().bsa_forward_lse(s, _ptr(q), _ptr(k), _ptr(v), key_block, topk,
+                                 None if sel is None else ctypes.byref(sel), float(scale),
+                                 _ptr(out), _ptr(idx), _ptr(lse), _ptr(ws), ws_n, _stream()))
+    return out, idx, lse
 
 
 def forward_noalloc(q, k, v, key_block: int, topk: int, scale: float = 0.0, out=None, idx=None):

@@ -525,9 +525,13 @@ bsa_status bsa_forward(bsa_shape shape, const void *q, const void *k, const void
                           ws_bytes, stream);
 }
 
-bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const void *v,
-                          int32_t key_block, int32_t topk, const bsa_select *sel, float scale,
-                          void *out, int32_t *idx_out, void *ws, size_t ws_bytes, void *stream) {
+namespace {
+
+// bsa_forward_ex; with lse_out the rows' log2-sum-exp too (block-major path)
+bsa_status forward_impl(bsa_shape shape, const void *q, const void *k, const void *v,
+                        int32_t key_block, int32_t topk, const bsa_select *sel, float scale,
+                        void *out, int32_t *idx_out, float *lse_out, void *ws, size_t ws_bytes,
+                        void *stream) {
     BSA_TRY(check_shape(shape));
     if (shape.dtype != BSA_BF16) return fail(BSA_ERR_UNSUPPORTED, "the dynamic forward takes bf16");
     BSA_TRY(check_key_block(key_block));
@@ -550,7 +554,11 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
     const int64_t nb = ceil_div(shape.n, key_block);
     int32_t *status = device_status_ptr();
     if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
-    if (!has_options(opts) && bsa::small_forward_supported(shape.d, nb, topk, shape.bh * shape.n)) {
+    if (lse_out != nullptr && !bm_path(shape, key_block, nb))
+        return fail(BSA_ERR_UNSUPPORTED,
+                    "the log2-sum-exp output needs the block-major fine stage (key_block 64)");
+    if (lse_out == nullptr && !has_options(opts) &&
+        bsa::small_forward_supported(shape.d, nb, topk, shape.bh * shape.n)) {
         // a small problem: pooling, selection and the fine stage in one launch
         bsa::FineArgs a{};
         a.q = q;
@@ -578,7 +586,7 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
         // options leave -1 padding (budgets, early causal queries): lists are not full
         return launched(run_fine_bm(shape, q, k, v, idx, key_block, topk, !has_options(opts),
                                     opts.causal != 0, has_options(opts) ? &opts : nullptr, sl2,
-                                    out, base, B, status, st),
+                                    out, base, B, status, st, lse_out),
                         "fine attention (block-major) launch");
     }
     bsa::FineArgs a{};
@@ -602,6 +610,25 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const v
     if (bsa::fine_static_tc_supported(a, shape.dtype))
         return launched(bsa::launch_fine_static_tc(a, st), "fine attention (tensor-core tiles) launch");
     return launched(bsa::launch_fine_query_major(a, shape.dtype, st), "fine attention launch");
+}
+
+}  // namespace
+
+bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k, const void *v,
+                          int32_t key_block, int32_t topk, const bsa_select *sel, float scale,
+                          void *out, int32_t *idx_out, void *ws, size_t ws_bytes, void *stream) {
+    return forward_impl(shape, q, k, v, key_block, topk, sel, scale, out, idx_out, nullptr, ws,
+                        ws_bytes, stream);
+}
+
+bsa_status bsa_forward_lse(bsa_shape shape, const void *q, const void *k, const void *v,
+                           int32_t key_block, int32_t topk, const bsa_select *sel, float scale,
+                           void *out, int32_t *idx_out, float *lse_out, void *ws, size_t ws_bytes,
+                           void *stream) {
+    if (lse_out == nullptr) return fail(BSA_ERR_INVALID_ARG, "lse_out is NULL");
+    if (!aligned(lse_out, 4)) return fail(BSA_ERR_ALIGNMENT, "lse_out is not 4-byte aligned");
+    return forward_impl(shape, q, k, v, key_block, topk, sel, scale, out, idx_out, lse_out, ws,
+                        ws_bytes, stream);
 }
 
 // ---------------------------------------------------------- backward pass

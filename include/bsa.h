@@ -297,6 +297,24 @@ bsa_status bsa_forward_ex(bsa_shape shape, const void *q, const void *k,
                           void *stream);
 
 /*
+ * bsa_forward_ex that also writes each query's log2-sum-exp (as
+ * bsa_fine_attention_lse defines it) for a backward pass over the same
+ * selection (bsa_fine_backward_lse with idx_out as the list), so that a
+ * training step computes the softmax statistics once.  The forward then
+ * always runs as separate launches (the one-launch form for small problems
+ * keeps no statistics).
+ *   lse_out  [bh][n] fp32 (device), 4-byte aligned.
+ * Only where the fine stage takes its block-major path (key_block 64, at most
+ * 16384 blocks); other shapes return BSA_ERR_UNSUPPORTED.  Workspace and
+ * everything else as bsa_forward_ex.
+ */
+bsa_status bsa_forward_lse(bsa_shape shape, const void *q, const void *k,
+                           const void *v, int32_t key_block, int32_t topk,
+                           const bsa_select *sel, float scale, void *out,
+                           int32_t *idx_out, float *lse_out, void *ws,
+                           size_t ws_bytes, void *stream);
+
+/*
  * The whole forward as one CUDA graph (page "sparse-attention-triton-bench",
  * The Triton kernel: the forward as a few fused launches instead of the
  * hundreds of a Python loop; here every launch of bsa_forward_ex is captured

@@ -144,3 +144,36 @@ def test_saved_lse_outside_the_block_major_path_is_unsupported():
     lst = torch.zeros((1, 256, 2), dtype=torch.int32, device="cuda")
     with pytest.raises(bsa.BsaError):
         bsa.fine_attention_lse(q, kk, v, lst, key_block=32)
+
+
+@pytest.mark.parametrize("bh,n,d,k,causal", [
+    (1, 1000, 64, 4, False),      # small enough for the one-launch forward without statistics
+    (2, 4100, 64, 16, True),
+    (1, 2100, 128, 8, False),
+])
+def test_training_step_forward_lse_then_backward(bh, n, d, k, causal):
+    """bsa_forward_lse: a selection the oracle's check accepts, the output
+    and the rows' log2-sum-exp of the oracle over that selection;
+    bsa_fine_backward_lse over it then matches the oracle's gradients."""
+    kb = 64
+    t, do = _inputs(bh, n, d, seed=n + 5 * d + k, kb=kb)
+    q, kk, v = (parity.to_device(getattr(t, x), "bf16") for x in "qkv")
+    dout = parity.to_device(do, "bf16")
+    out, idx, lse = bsa.forward_lse(q, kk, v, kb, k, causal=causal)
+    idx_np = idx.cpu().numpy().reshape(-1, k)
+    rows = oracle.all_rows(bh, n)
+    if not causal:
+        s = oracle.scores(t.q, oracle.pool(t.k, kb), rows)
+        oidx, kth = oracle.topk(s, k)
+        parity.check_selection(idx_np, oidx, s, kth, -(-n // kb))
+    o_ref, ref_lse, _ = oracle.fine(t.q, t.k, t.v, kb, idx_np, rows, causal=causal)
+    parity.assert_close(parity.from_device(out).reshape(-1, d), o_ref, "bf16", "forward_lse output")
+    ref2 = ref_lse / np.log(2.0)
+    got = lse.cpu().numpy().reshape(-1).astype(np.float64)
+    assert np.isfinite(ref2).all()
+    assert np.abs(got - ref2).max() <= 1e-3 * max(1.0, np.abs(ref2).max())
+    dq, dk, dv = bsa.fine_backward(q, kk, v, out, dout, idx, key_block=kb, causal=causal, lse=lse)
+    rq, rk, rv = oracle.fine_backward(t.q, t.k, t.v, do, kb, idx_np, causal=causal)
+    for name, g, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        _grad_close(g.cpu().numpy(), ref, f"{name} (training step) bh={bh} n={n} d={d} k={k}")
+    assert bsa.device_status() == 0
