@@ -542,6 +542,9 @@ bsa_status forward_impl(bsa_shape shape, const void *q, const void *k, const voi
     BSA_TRY(check_ptr(out, "out"));
     if (idx_out != nullptr) BSA_TRY(check_ptr(idx_out, "idx_out"));
     BSA_TRY(check_select(sel));
+    if (lse_out != nullptr && !bm_path(shape, key_block, ceil_div(shape.n, key_block)))
+        return fail(BSA_ERR_UNSUPPORTED,
+                    "the log2-sum-exp output needs the block-major fine stage (key_block 64)");
     const bsa::SelectOpts opts = select_opts(sel, key_block);
     const ForwardLayout L = forward_layout(shape, key_block, topk);
     BSA_TRY(check_ws(ws, ws_bytes, bsa_forward_workspace_size(shape, key_block, topk)));
@@ -554,9 +557,6 @@ bsa_status forward_impl(bsa_shape shape, const void *q, const void *k, const voi
     const int64_t nb = ceil_div(shape.n, key_block);
     int32_t *status = device_status_ptr();
     if (status == nullptr) return fail(BSA_ERR_CUDA, "status word unavailable");
-    if (lse_out != nullptr && !bm_path(shape, key_block, nb))
-        return fail(BSA_ERR_UNSUPPORTED,
-                    "the log2-sum-exp output needs the block-major fine stage (key_block 64)");
     if (lse_out == nullptr && !has_options(opts) &&
         bsa::small_forward_supported(shape.d, nb, topk, shape.bh * shape.n)) {
         // a small problem: pooling, selection and the fine stage in one launch

@@ -138,6 +138,31 @@ def test_backward_rejects_bad_arguments(L):
     assert L.bsa_fine_backward_workspace_size(s, bsa.ListDesc(128, 64, 4, 0)) == 0
 
 
+def test_saved_statistics_entry_points_reject_bad_arguments(L):
+    s = _shape(n=256)
+    ld = bsa.ListDesc(1, 64, 4, 1)
+    none = bsa.mask_struct()
+    need = L.bsa_fine_attention_workspace_size(s, ld, none)
+    odd = ctypes.c_void_p(0x10002)                 # not 4-byte aligned
+    fa = lambda lse, ld_=ld: L.bsa_fine_attention_lse(s, FAKE, FAKE, FAKE, FAKE, ld_, none, 0.0,
+                                                      FAKE, lse, FAKE, need, None)
+    assert fa(None) == 1
+    assert fa(odd) == 7
+    assert fa(FAKE, bsa.ListDesc(1, 32, 4, 1)) == 2            # not the block-major path
+    assert fa(FAKE, bsa.ListDesc(128, 64, 4, 0)) == 2          # static tile lists
+    nbw = L.bsa_fine_backward_workspace_size(s, ld)
+    fb = lambda lse: L.bsa_fine_backward_lse(s, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ld, none, 0.0,
+                                             lse, FAKE, FAKE, FAKE, FAKE, nbw, None)
+    assert fb(None) == 1
+    assert fb(odd) == 7
+    nf = L.bsa_forward_workspace_size(s, 64, 4)
+    fw = lambda kb, lse: L.bsa_forward_lse(s, FAKE, FAKE, FAKE, kb, 4, None, 0.0, FAKE, None, lse,
+                                           FAKE, nf, None)
+    assert fw(64, None) == 1
+    assert fw(64, odd) == 7
+    assert fw(32, FAKE) == 2                                  # not the block-major path
+
+
 def test_static_path_workspace_is_optional_and_sized(L):
     m = bsa.mask_struct(bsa.MASK_SLIDING, sliding=256)
     s = _shape(bh=2, n=1000, d=128)
